@@ -1,0 +1,360 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by mathematics.
+
+Nothing here reuses the oracle's own formulas: each check is a closed form, a
+library routine on a special case, an invariant, a brute force written
+independently (pure Python, its own bf16 decode, math.fsum), or a finite
+difference.
+"""
+import json
+import math
+import os
+import struct
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _dec(bits):
+    """bf16 bits -> Python float, independent of the oracle's decoder."""
+    return struct.unpack("<f", struct.pack("<I", (int(bits) & 0xFFFF) << 16))[0]
+
+
+def _zeros_like_W(part, H):
+    return [np.zeros((e - s, H), np.uint16) for s, e in part.ranges]
+
+
+def _bias_bits(vals):
+    return synth.bf16_bits(np.asarray(vals, np.float32))
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_w_zero_gives_uniform_over_real_vocab_with_padding():
+    # z == 0 on the real ids: logp = -log V_real, LSE = entropy = log V_real.
+    # With 24 padded ids, -log(1024) would differ from -log(1000) by 0.0237.
+    part = synth.even_partition(1000, 4, vocab_padded=1024)
+    T, H = 5, 16
+    rng = np.random.default_rng(0)
+    X = synth.bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    y = rng.integers(0, 1000, T).astype(np.int32)
+    r = oracle.forward(X, _zeros_like_W(part, H), None, part, y, 0.7)
+    np.testing.assert_allclose(r.logp, -math.log(1000), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r.lse, math.log(1000), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r.entropy, math.log(1000), rtol=0, atol=1e-12)
+
+
+def test_constant_bias_shifts_lse_by_c_over_tau():
+    part = synth.even_partition(96, 3)
+    T, H, c, tau = 3, 8, 1.5, 0.75
+    b = [_bias_bits(np.full(32, c)) for _ in range(3)]
+    X = np.zeros((T, H), np.uint16)
+    y = np.array([0, 50, 95], np.int32)
+    r = oracle.forward(X, _zeros_like_W(part, H), b, part, y, tau)
+    np.testing.assert_allclose(r.lse, c / tau + math.log(96), atol=1e-12)
+    np.testing.assert_allclose(r.logp, -math.log(96), atol=1e-12)
+
+
+def test_two_level_logits_closed_form():
+    # k ids at alpha = b/tau, the rest at 0:
+    # LSE = log(k e^a + V - k); entropy = LSE - k a e^a / Z.
+    V, k, tau, bval = 200, 7, 0.5, 2.0
+    alpha = bval / tau
+    part = synth.even_partition(V, 2)
+    hot = np.zeros(V, np.float32)
+    hot[[3, 17, 99, 100, 150, 151, 199]] = bval
+    b = [_bias_bits(hot[:100]), _bias_bits(hot[100:])]
+    X = np.zeros((2, 4), np.uint16)
+    y = np.array([17, 5], np.int32)
+    r = oracle.forward(X, _zeros_like_W(part, 4), b, part, y, tau)
+    Z = k * math.exp(alpha) + (V - k)
+    lse = math.log(Z)
+    ent = lse - k * alpha * math.exp(alpha) / Z
+    np.testing.assert_allclose(r.lse, lse, atol=1e-12)
+    np.testing.assert_allclose(r.entropy, ent, atol=1e-12)
+    np.testing.assert_allclose(r.logp, [alpha - lse, -lse], atol=1e-12)
+
+
+def test_one_dominant_logit_gives_logp_zero_entropy_zero():
+    # z_y = 1000, the other 63 ids 0: exp(-1000) underflows, so LSE = 1000,
+    # logp = 0 and entropy = 0 exactly in float64
+    V, tau = 64, 1.0
+    part = synth.even_partition(V, 1)
+    hot = np.zeros(V, np.float32)
+    hot[11] = 1000.0                       # exactly representable in bf16
+    X = np.zeros((1, 8), np.uint16)
+    r = oracle.forward(X, _zeros_like_W(part, 8), [_bias_bits(hot)], part,
+                       np.array([11], np.int32), tau)
+    assert r.logp[0] == 0.0
+    assert abs(r.entropy[0]) < 1e-12
+    assert r.lse[0] == 1000.0
+
+
+def test_empty_shard_convention_printed_on_the_pages():
+    # tests/golden/empty_shard.json holds the values the replay page prints for a
+    # vocabulary shard with no candidates
+    with open(os.path.join(GOLDEN, "empty_shard.json")) as f:
+        gold = json.load(f)["local"]
+    part = synth.ranges_partition(40, 48, [0, 16, 32, 48])
+    inp = synth.forward_inputs(2, 8, part, tau=0.7, seed=0, w_std=0.3)
+    ids = np.full((2, 64), -1, np.int32)
+    ids[0, :3] = [1, 2, 20]                  # shard 2 ([32,48)) empty in row 0
+    ids[1, :2] = [35, 36]                    # shards 0 and 1 empty in row 1
+    y = np.array([20, 35], np.int32)
+    rep = oracle.top_p_replay(inp.X, inp.W, None, part, ids, y, inp.tau)
+    for k, t in [(2, 0), (0, 1), (1, 1)]:
+        assert rep.shard_lse[k, t] == float(gold["lse"])
+        assert rep.shard_t[k, t] == gold["target_logit"]
+    # the dense path: a shard made only of padding ids is empty too
+    part2 = synth.ranges_partition(32, 48, [0, 16, 32, 48])
+    r = oracle.forward(inp.X, inp.W, None, part2, np.array([3, 17], np.int32), inp.tau)
+    assert np.all(r.shards[2].lse == float(gold["lse"]))
+    assert np.all(r.shards[2].t == gold["target_logit"])
+
+
+@pytest.mark.parametrize("V,k,tau,bval", [(50, 1, 1.0, 3.0), (1000, 10, 0.7, 0.5), (7, 6, 2.0, -4.0)])
+def test_two_level_closed_form_parametrized(V, k, tau, bval):
+    part = synth.even_partition(V, 1)
+    hot = np.zeros(V, np.float32)
+    hot[:k] = bval
+    X = np.zeros((1, 4), np.uint16)
+    r = oracle.forward(X, _zeros_like_W(part, 4), [_bias_bits(hot)], part, np.array([V - 1], np.int32), tau)
+    a = bval / tau                          # bval is exactly representable in bf16
+    Z = k * math.exp(a) + (V - k)
+    lse = math.log(Z)
+    np.testing.assert_allclose(r.lse[0], lse, atol=1e-12)
+    np.testing.assert_allclose(r.logp[0], -lse, atol=1e-12)
+    np.testing.assert_allclose(r.entropy[0], lse - k * a * math.exp(a) / Z, atol=1e-12)
+
+
+# ------------------------------------------------------- library special case
+
+def test_matches_torch_log_softmax_float64():
+    torch = pytest.importorskip("torch")
+    part = synth.ranges_partition(300, 320, [0, 100, 100, 250, 320])   # one empty shard
+    inp = synth.forward_inputs(6, 24, part, tau=0.7, seed=3, w_std=0.3, bias_std=0.5)
+    r = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau)
+    X = torch.from_numpy(oracle.bf16_to_f64(inp.X))
+    W = torch.cat([torch.from_numpy(oracle.bf16_to_f64(w)) for w in inp.W])[:300]
+    b = torch.cat([torch.from_numpy(oracle.bf16_to_f64(x)) for x in inp.bias])[:300]
+    z = (X @ W.T + b) / inp.tau
+    ls = torch.log_softmax(z, dim=1)
+    ref_logp = ls[torch.arange(6), torch.from_numpy(inp.y.astype(np.int64))].numpy()
+    ref_lse = torch.logsumexp(z, dim=1).numpy()
+    ref_ent = -(ls.exp() * ls).sum(dim=1).numpy()
+    np.testing.assert_allclose(r.logp, ref_logp, atol=1e-11)
+    np.testing.assert_allclose(r.lse, ref_lse, atol=1e-11)
+    np.testing.assert_allclose(r.entropy, ref_ent, atol=1e-11)
+
+
+# ------------------------------------------------------------------ brute force
+
+def _brute(X, W, b, part, y, tau):
+    """Pure-Python forward with math.fsum; returns lists logp, lse, entropy."""
+    out = []
+    for t in range(len(y)):
+        zs = {}
+        for k, (vs, ve) in enumerate(part.ranges):
+            for j in range(ve - vs):
+                v = vs + j
+                if v >= part.vocab_real:
+                    continue
+                a = math.fsum(_dec(X[t][h]) * _dec(W[k][j][h]) for h in range(len(X[t])))
+                if b is not None:
+                    a += _dec(b[k][j])
+                zs[v] = a / tau
+        M = max(zs.values())
+        lse = M + math.log(math.fsum(math.exp(z - M) for z in zs.values()))
+        ent = -math.fsum(math.exp(z - lse) * (z - lse) for z in zs.values())
+        out.append((zs[int(y[t])] - lse, lse, ent))
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_brute_force_tiny_multishard_padded(seed):
+    part = synth.ranges_partition(50, 64, [0, 13, 13, 40, 64])
+    inp = synth.forward_inputs(4, 16, part, tau=0.7, seed=seed, w_std=0.4, bias_std=0.3)
+    r = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau)
+    ref = _brute(inp.X, inp.W, inp.bias, part, inp.y, inp.tau)
+    np.testing.assert_allclose(r.logp, [o[0] for o in ref], atol=1e-12)
+    np.testing.assert_allclose(r.lse, [o[1] for o in ref], atol=1e-12)
+    np.testing.assert_allclose(r.entropy, [o[2] for o in ref], atol=1e-12)
+
+
+def test_brute_force_logits_reuse_applies_tau_once():
+    part = synth.ranges_partition(40, 48, [0, 20, 48])
+    L, y, tau = synth.logits_inputs(3, part, 0.7, seed=5, peak_frac=0.1)
+    r = oracle.forward_from_logits(L, part, y, tau)
+    for t in range(3):
+        zs = []
+        for k, (vs, ve) in enumerate(part.ranges):
+            for j in range(ve - vs):
+                if vs + j < 40:
+                    zs.append(_dec(L[k][t][j]) / tau)
+        M = max(zs)
+        lse = M + math.log(math.fsum(math.exp(z - M) for z in zs))
+        assert abs(r.lse[t] - lse) < 1e-12
+        assert abs(r.logp[t] - (zs[int(y[t])] - lse)) < 1e-12
+        ent = -math.fsum(math.exp(z - lse) * (z - lse) for z in zs)
+        assert abs(r.entropy[t] - ent) < 1e-12
+
+
+# ------------------------------------------------------------------------ merge
+
+def test_merge_of_shards_equals_unsharded():
+    part = synth.ranges_partition(500, 512, [0, 100, 100, 300, 499, 512])  # empty + tiny shards
+    inp = synth.forward_inputs(8, 32, part, tau=0.6, seed=9, w_std=0.2, bias_std=0.2)
+    r = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau)
+    logp, lse, ent = oracle.merge_shards(r.shards, inp.y.astype(np.int64), part.ranges)
+    np.testing.assert_allclose(logp, r.logp, atol=1e-12)
+    np.testing.assert_allclose(lse, r.lse, atol=1e-12)
+    np.testing.assert_allclose(ent, r.entropy, atol=1e-12)
+    # the empty shard [100,100) and the all-padding shard [499..512) minus id 499
+    assert np.all(np.isneginf(r.shards[1].lse))
+    assert np.all(r.shards[1].t == 0) and np.all(r.shards[1].mu == 0)
+
+
+def test_merge_all_empty_row_convention():
+    st = [oracle.ShardStats(np.array([-np.inf]), np.zeros(1), np.zeros(1)) for _ in range(3)]
+    logp, lse, ent = oracle.merge_shards(st, np.array([5]), ((0, 4), (4, 8), (8, 12)))
+    assert np.isneginf(lse[0]) and np.isneginf(logp[0]) and ent[0] == 0.0
+
+
+def test_shard_stats_match_local_closed_form():
+    # shard local LSE with z == 0: log(#real ids in shard)
+    part = synth.ranges_partition(90, 96, [0, 30, 60, 96])
+    X = np.zeros((2, 4), np.uint16)
+    r = oracle.forward(X, _zeros_like_W(part, 4), None, part, np.array([1, 70], np.int32), 0.7)
+    np.testing.assert_allclose([s.lse[0] for s in r.shards], np.log([30, 30, 30]), atol=1e-12)
+
+
+# ----------------------------------------------------------------------- replay
+
+def _full_set_ids(T, V):
+    ids = np.full((T, 64), -1, np.int32)
+    for t in range(T):
+        ids[t, :V] = np.random.default_rng(t).permutation(V)
+    return ids
+
+
+def test_replay_with_whole_vocab_equals_dense():
+    part = synth.ranges_partition(60, 64, [0, 16, 32, 48, 64])
+    inp = synth.forward_inputs(5, 32, part, tau=0.7, seed=4, w_std=0.3, bias_std=0.2)
+    ids = _full_set_ids(5, 60)
+    dense = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau)
+    rep = oracle.top_p_replay(inp.X, inp.W, inp.bias, part, ids, inp.y, inp.tau)
+    np.testing.assert_allclose(rep.lse, dense.lse, atol=1e-12)
+    np.testing.assert_allclose(rep.logp, dense.logp, atol=1e-12)
+    for k in range(4):
+        np.testing.assert_allclose(rep.shard_lse[k], dense.shards[k].lse, atol=1e-12)
+        np.testing.assert_allclose(rep.shard_t[k], dense.shards[k].t, atol=1e-12)
+
+
+def test_replay_single_id_and_missing_target():
+    part = synth.even_partition(100, 2)
+    inp = synth.forward_inputs(2, 16, part, tau=0.7, seed=1, w_std=0.3)
+    ids = np.full((2, 64), -1, np.int32)
+    ids[0, [5, 9, 40]] = 77                  # one distinct id, duplicated
+    ids[1, 0] = 3
+    y = np.array([77, 4], np.int32)          # row 1's target is not in its set
+    rep = oracle.top_p_replay(inp.X, inp.W, None, part, ids, y, inp.tau)
+    z77 = math.fsum(_dec(inp.X[0][h]) * _dec(inp.W[1][27][h]) for h in range(16)) / inp.tau
+    assert rep.logp[0] == 0.0
+    assert abs(rep.lse[0] - z77) < 1e-12
+    assert np.isneginf(rep.logp[1]) and np.isfinite(rep.lse[1])
+    assert np.isneginf(rep.shard_lse[0, 0]) and rep.shard_t[0, 0] == 0.0   # empty shard 0 in row 0
+
+
+def test_replay_invariant_to_slot_order_and_duplicates():
+    part = synth.even_partition(1000, 4)
+    inp = synth.forward_inputs(16, 32, part, tau=0.7, seed=2, w_std=0.3)
+    ids, y = synth.replay_ids(16, part, seed=3)
+    a = oracle.top_p_replay(inp.X, inp.W, None, part, ids, y, inp.tau)
+    rng = np.random.default_rng(0)
+    ids2 = ids.copy()
+    for t in range(16):
+        live = ids2[t][ids2[t] != -1]
+        free = 64 - live.size
+        extra = rng.choice(live, size=min(free, 3))
+        row = np.concatenate([live, extra, np.full(64 - live.size - extra.size, -1)])
+        ids2[t] = rng.permutation(row)
+    b = oracle.top_p_replay(inp.X, inp.W, None, part, ids2, y, inp.tau)
+    np.testing.assert_array_equal(a.lse, b.lse)
+    np.testing.assert_array_equal(a.logp, b.logp)
+
+
+def test_replay_rejects_out_of_range_ids():
+    with pytest.raises(ValueError):
+        oracle.replay_set(np.array([3, 1000, -1]), 1000)
+    with pytest.raises(ValueError):
+        oracle.replay_set(np.array([-2]), 1000)
+
+
+# --------------------------------------------------------------------- backward
+
+def _loss(Xd, Wd, bd, ranges, Vr, y, tau, g):
+    z = oracle.logits_f64(Xd, Wd, bd, ranges, Vr, tau)
+    M = z.max(axis=1, keepdims=True)
+    lse = (M + np.log(np.exp(z - M).sum(axis=1, keepdims=True)))[:, 0]
+    return float(np.dot(g, z[np.arange(len(y)), y] - lse))
+
+
+def test_backward_central_finite_differences():
+    part = synth.ranges_partition(20, 24, [0, 10, 24])
+    rng = np.random.default_rng(11)
+    T, H, tau = 3, 5, 0.7
+    Xd = rng.standard_normal((T, H))
+    Wd = [rng.standard_normal((e - s, H)) * 0.5 for s, e in part.ranges]
+    bd = [rng.standard_normal(e - s) * 0.5 for s, e in part.ranges]
+    y = np.array([2, 19, 11])
+    g = rng.standard_normal(T)
+    r = oracle.backward_f64(Xd, Wd, bd, part.ranges, 20, y, tau, g)
+    eps = 1e-6
+
+    def fd(arr, idx):
+        old = arr[idx]
+        arr[idx] = old + eps
+        lp = _loss(Xd, Wd, bd, part.ranges, 20, y, tau, g)
+        arr[idx] = old - eps
+        lm = _loss(Xd, Wd, bd, part.ranges, 20, y, tau, g)
+        arr[idx] = old
+        return (lp - lm) / (2 * eps)
+
+    num_dX = np.array([[fd(Xd, (t, h)) for h in range(H)] for t in range(T)])
+    np.testing.assert_allclose(r.dX, num_dX, rtol=1e-6, atol=1e-8)
+    for k in range(2):
+        Vk = Wd[k].shape[0]
+        num_dW = np.array([[fd(Wd[k], (v, h)) for h in range(H)] for v in range(Vk)])
+        num_db = np.array([fd(bd[k], (v,)) for v in range(Vk)])
+        np.testing.assert_allclose(r.dW[k], num_dW, rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(r.db[k], num_db, rtol=1e-6, atol=1e-8)
+    # padded ids (>= 20) have exactly zero gradient
+    assert np.all(r.dW[1][10:] == 0) and np.all(r.db[1][10:] == 0)
+
+
+def test_backward_bias_grad_sums_to_zero_per_row_invariant():
+    part = synth.even_partition(300, 3)
+    inp = synth.forward_inputs(7, 16, part, tau=0.7, seed=6, w_std=0.3, bias_std=0.1)
+    g = synth.upstream_grad(7, seed=6)
+    r = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g)
+    total = sum(float(d.sum()) for d in r.db)
+    assert abs(total) < 1e-12
+
+
+def test_backward_sampled_matches_full():
+    part = synth.ranges_partition(200, 208, [0, 104, 208])
+    inp = synth.forward_inputs(9, 16, part, tau=0.7, seed=8, w_std=0.3, bias_std=0.1)
+    g = synth.upstream_grad(9, seed=8)
+    full = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g)
+    dx_rows = [0, 4, 8]
+    dw_rows = [[0, 50, 103], [0, 95, 96, 103]]       # 96.. are padded ids (>= 200)
+    dX, dW, db = oracle.backward_sampled(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g,
+                                         dx_rows, dw_rows)
+    np.testing.assert_allclose(dX, full.dX[dx_rows], atol=1e-12)
+    for k in range(2):
+        np.testing.assert_allclose(dW[k], full.dW[k][dw_rows[k]], atol=1e-12)
+        np.testing.assert_allclose(db[k], full.db[k][dw_rows[k]], atol=1e-12)
