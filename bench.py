@@ -1,0 +1,394 @@
+"""Benchmark of the deterministic fused linear-logp operator on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline (one JSON line on rank 0): the fused forward on the Qwen3-8B-shaped LM head,
+T=4096 rows, H=4096, V=151936 bf16, tau=0.7, logp + LSE + entropy, in tokens/s, with
+the tensor-core roofline of the fused GEMM kernel. The other hot-path rows are timed
+alongside in "paths": logits reuse (T=8192 x 151936 bf16 logits, HBM-bound), compact
+top-p replay (T=8192, 4 shards), and the vocabulary-sharded forward + backward
+(T=4096, V=151936 padded to 152064 in 4 shards, bias).
+
+Every input is synthetic and seeded; the weights and logits are larger than the
+129 MB L2, so no flush is needed between timed steps. --impl reference times the fp64
+CPU oracle on the host cores on a bounded row sample of the same workload.
+N > 1 (torchrun): every rank runs the same workload on its own GPU (replicas, no
+collective on the data path); the value is all rows over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused linear-logp tokens/s (T×4096→151936 bf16) and % of dense bf16 tensor peak"
+UNIT = "tokens/s"
+T_FWD, H, V = 4096, 4096, 151936
+TAU = 0.7
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CSRC = os.path.join(ROOT, "lm_head_linear_tcgen05_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ----------------------------------------------------------------- utilities
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash() -> str:
+    """Hash of the kernel sources: a stored ncu traffic figure is valid only for this hash."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("source_hash") == source_hash():
+            return float(e["bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    c = [x.strip() for x in line.split(",")]
+                    if len(c) < 9:
+                        continue
+                    try:
+                        sm.append(float(c[1]))
+                        mx.append(float(c[2]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, c[5:9]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+            os.unlink(self.path)
+        except Exception:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_steps(fn, steps, warmup, stream):
+    """Average ms per step over `steps` calls of fn(), CUDA events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+# -------------------------------------------------------------- our GPU arm
+
+def run_ours(args, rank, world, dist):
+    import numpy as np
+    import torch
+
+    import lm_head_linear_tcgen05_gb300 as lp
+    import synth
+
+    from lm_head_linear_tcgen05_gb300 import _build
+    _build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not lp.lp_device_supported():
+        raise RuntimeError("this GPU cannot run liblp.so (sm_103a build)")
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+
+    # ---- headline: fused forward, T=4096, H=4096, V=151936, tau=0.7, no bias
+    part = synth.even_partition(V, 1)
+    P = lp.VocabPartition(part.vocab_real, part.vocab_padded, part.ranges)
+    X, W, _, y = synth.device_forward_inputs(T_FWD, H, part, TAU, dev, seed=0)
+    ws = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD, T_FWD, H, P), dtype=torch.uint8, device=dev)
+    step = lambda: lp.lp_forward(X, W, None, P, y, TAU, workspace=ws)
+    if dist is not None:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        ms = time_steps(step, args.steps, args.warmup, stream)
+    if lp.lp_get_device_error() != 0:
+        raise RuntimeError("device error during the timed forward")
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    flops = 2.0 * T_FWD * H * V
+    tflops = flops / (ms * 1e-3) / 1e12
+    value = world * T_FWD / (ms * 1e-3)
+
+    # ---- end to end through the public API: pinned host X, y in; logp, lse, entropy out
+    hX = torch.empty((T_FWD, H), dtype=torch.bfloat16, pin_memory=True)
+    hX.copy_(X.cpu())
+    hy = y.cpu().pin_memory()
+    dX = torch.empty_like(X)
+    dy = torch.empty_like(y)
+    h_out = [torch.empty(T_FWD, dtype=torch.float32, pin_memory=True) for _ in range(3)]
+
+    def e2e_step():
+        dX.copy_(hX, non_blocking=True)
+        dy.copy_(hy, non_blocking=True)
+        o = lp.lp_forward(dX, W, None, P, dy, TAU, workspace=ws)
+        h_out[0].copy_(o["logp"], non_blocking=True)
+        h_out[1].copy_(o["lse"], non_blocking=True)
+        h_out[2].copy_(o["entropy"], non_blocking=True)
+
+    ms_e2e = time_steps(e2e_step, args.steps, args.warmup, stream)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    del hX
+    paths = {}
+    if not args.headline_only:
+        paths = time_other_paths(args, lp, synth, dev, stream, peaks)
+
+    if rank != 0:
+        return
+    traffic = stored_traffic("fused_forward")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "Qwen3-8B-shaped LM-head fused forward, T=4096 rows, H=4096, V=151936, "
+                               "tau=0.7, no bias, logp+LSE+entropy",
+                   "T": T_FWD, "H": H, "V": V, "tau": TAU, "shards": 1,
+                   "l2": "inputs larger than L2 (W 1.245 GB > 129 MB); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "clocks": clk.summary(),
+        "e2e": {"value": world * T_FWD / (ms_e2e * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": T_FWD * H * 2 + T_FWD * 4, "d2h_bytes_per_step": 3 * T_FWD * 4,
+                "ms_per_step": ms_e2e},
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tflops / peaks["bf16_tflops"], "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense burst",
+                     "timed": "whole lp_forward call (fused GEMM kernel + row merge kernel)",
+                     "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"]},
+        "paths": paths,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_forward(rows=64)
+    print(json.dumps(line), flush=True)
+
+
+def time_other_paths(args, lp, synth, dev, stream, peaks):
+    import torch
+    out = {}
+    # logits reuse: T=8192 x 151936 bf16 logits
+    part = synth.even_partition(V, 1)
+    P = lp.VocabPartition(part.vocab_real, part.vocab_padded, part.ranges)
+    L, y = synth.device_logits(8192, part, dev, seed=4)
+    ms = time_steps(lambda: lp.lp_forward_from_logits(L, P, y, TAU), args.steps, args.warmup, stream)
+    nbytes = 8192 * V * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["logits_reuse"] = {"workload": "T=8192, V=151936 bf16 logits N(0,9), 1% peaked, tau=0.7",
+                           "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
+                           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
+                                        "traffic": stored_traffic("stream_logits")}}
+    del L
+    torch.cuda.empty_cache()
+
+    # compact top-p replay: T=8192, 4 shards of 37984
+    part4 = synth.even_partition(V, 4)
+    P4 = lp.VocabPartition(part4.vocab_real, part4.vocab_padded, part4.ranges)
+    X, W, _, _ = synth.device_forward_inputs(8192, H, part4, TAU, dev, seed=5)
+    ids, yr = synth.replay_ids(8192, part4, seed=5)
+    ids_d = torch.from_numpy(ids).to(dev)
+    yr_d = torch.from_numpy(yr).to(dev)
+    ms = time_steps(lambda: lp.lp_top_p_replay(X, W, None, P4, ids_d, yr_d, TAU), args.steps, args.warmup, stream)
+    uniq = sum(len(set(r[r >= 0].tolist())) for r in ids)
+    distinct = len(set(ids[ids >= 0].tolist()))
+    gathered = 8192 * H * 2 + uniq * H * 2
+    distinct_b = 8192 * H * 2 + distinct * H * 2
+    out["top_p_replay"] = {"workload": "T=8192, H=4096, V=151936 in 4 shards, 1-64 ids/row (+10% dups), tau=0.7",
+                           "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
+                           "gathered_bytes": gathered, "distinct_bytes": distinct_b,
+                           "roofline": {"bound": "hbm", "achieved": gathered / (ms * 1e-3) / 1e9,
+                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": gathered / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                        "traffic": stored_traffic("replay")}}
+    del X, W
+    torch.cuda.empty_cache()
+
+    # vocabulary-sharded forward + backward: V padded to 152064 in 4 shards, bias
+    part3 = synth.ranges_partition(V, 152064, [0, 38016, 76032, 114048, 152064])
+    P3 = lp.VocabPartition(part3.vocab_real, part3.vocab_padded, part3.ranges)
+    X, W, b, y = synth.device_forward_inputs(T_FWD, H, part3, TAU, dev, seed=3, bias_std=0.01)
+    g = torch.randn(T_FWD, generator=torch.Generator(device=dev).manual_seed(3), device=dev)
+    wsf = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(lp.lp_workspace_size(lp.LP_OP_BACKWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
+    fwd = lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf)
+    ms_f = time_steps(lambda: lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf), args.steps, args.warmup, stream)
+    ms_b = time_steps(lambda: lp.lp_backward(X, W, b, P3, y, TAU, fwd["lse"], g, workspace=wsb),
+                      max(3, args.steps // 2), args.warmup, stream)
+    f_fl = 2.0 * T_FWD * H * V
+    out["sharded_fwd_bwd"] = {"workload": "T=4096, H=4096, V=151936 padded to 152064, 4 shards, bias, tau=0.7",
+                              "fwd_tokens_per_s": T_FWD / (ms_f * 1e-3), "fwd_ms": ms_f,
+                              "bwd_tokens_per_s": T_FWD / (ms_b * 1e-3), "bwd_ms": ms_b,
+                              "fwd_bwd_tokens_per_s": T_FWD / ((ms_f + ms_b) * 1e-3),
+                              "fwd_tflops": f_fl / (ms_f * 1e-3) / 1e12,
+                              "bwd_tflops_3gemm": 3 * f_fl / (ms_b * 1e-3) / 1e12,
+                              "bwd_frac_3gemm": 3 * f_fl / (ms_b * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+    if lp.lp_get_device_error() != 0:
+        raise RuntimeError("device error in the path timings")
+    return out
+
+
+# ------------------------------------------------------------ oracle (CPU) arm
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_forward(rows: int):
+    """The fp64 oracle on `rows` rows of the headline workload (full H and V)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    part = synth.even_partition(V, 1)
+    inp = synth.forward_inputs(rows, H, part, tau=TAU, seed=0)
+    t0 = time.perf_counter()
+    oracle.forward(inp.X, inp.W, None, part, inp.y, inp.tau)
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{rows} of {T_FWD} rows of the headline workload (full H={H}, V={V}), fp64 numpy oracle; "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    rows = args.ref_rows
+    part = synth.even_partition(V, 1)
+    inp = synth.forward_inputs(rows, H, part, tau=TAU, seed=0)
+    for _ in range(args.warmup):
+        oracle.forward(inp.X, inp.W, None, part, inp.y, inp.tau)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(inp.X, inp.W, None, part, inp.y, inp.tau)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = rows / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "Qwen3-8B-shaped LM-head fused forward, T=4096 rows, H=4096, V=151936, "
+                                   "tau=0.7, no bias, logp+LSE+entropy", "T": T_FWD, "H": H, "V": V, "tau": TAU,
+                       "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{rows} of {T_FWD} rows per step (full H, V), fp64 numpy oracle"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true", help="time only the fused forward")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per reference step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * lp.h - C ABI of the deterministic linear-logp operator for GB300 (sm_103a).
+ *
+ * What the operator computes (page "feat(rl-kernel): add CUDA linear logp
+ * provider integration", Motivation and Changes / Megatron integration): from
+ * output-layer hidden states X[T,H], the local LM-head projection weight W and
+ * bias b of each tensor-parallel vocabulary shard, the real/padded vocabulary
+ * sizes and target ids y[T], it returns selected-token log probabilities and
+ * optional entropy of softmax(z), z = (X W^T + b) / tau, without materialising
+ * the logits. Temperature is applied exactly once (page "feat(rl-kernel): add
+ * ROCm linear logp provider integration", Changes). Shards are reduced in rank
+ * order and an empty shard gives zero probabilities, LSE = -inf, target logit 0
+ * and logp = -inf, never NaN (page "Perf/cuda compact top p replay", Summary
+ * and Walkthrough).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory. Scratch comes from the caller through
+ *    `workspace`, sized by lp_workspace_size(). Host-side structs
+ *    (lp_vocab_partition, lp_outputs, the shard range array and the arrays of
+ *    per-shard pointers) are read during the call only.
+ *  - bf16 tensors are row-major; rows of X, W and logits must start on a
+ *    16-byte boundary (pointer % 16 == 0 and row stride % 8 elements == 0).
+ *  - Vocabulary ids are GLOBAL ids. A partition lists n_shards (1..LP_MAX_SHARDS)
+ *    contiguous ranges in ascending order that tile [0, vocab_padded) exactly;
+ *    ids in [vocab_real, vocab_padded) are padding and excluded from the softmax.
+ *    A shard may be empty (vocab_start == vocab_end).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and never synchronises, except lp_get_device_error().
+ *  - Results are bitwise deterministic run to run and batch invariant: a row's
+ *    outputs depend only on that row's inputs, never on T or on the row's
+ *    position. Reductions over the vocabulary follow a fixed order that
+ *    depends only on the partition and compile-time tile sizes.
+ *  - Host-side validation errors are returned before anything is launched.
+ *    Errors found on the device (a target or replay id out of range, a
+ *    pipeline wait that timed out) are recorded in a sticky per-device error
+ *    word read by lp_get_device_error(); the affected rows get logp = -inf.
+ *  - A call made while the current device is not sm_100-family (GB300 is
+ *    sm_103) returns LP_ERR_UNSUPPORTED_DEVICE. There is no CPU fallback.
+ */
+#ifndef LP_H_
+#define LP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LP_MAX_SHARDS 8     /* shards per call */
+#define LP_REPLAY_SLOTS 64  /* replay id slots per row */
+
+#if defined(__GNUC__)
+#define LP_API __attribute__((visibility("default")))
+#else
+#define LP_API
+#endif
+
+typedef struct CUstream_st* lp_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  LP_OK = 0,
+  LP_ERR_INVALID_ARG = 1,          /* null pointer, bad size, bad partition, tau not finite or <= 0 */
+  LP_ERR_ALIGNMENT = 2,            /* a pointer or row stride breaks the 16-byte rule */
+  LP_ERR_UNSUPPORTED_DEVICE = 3,   /* current device is not sm_100 family, or no device */
+  LP_ERR_WORKSPACE_TOO_SMALL = 4,  /* ws_bytes < lp_workspace_size(...) */
+  LP_ERR_TARGET_OUT_OF_RANGE = 5,  /* device: some y not in [0, vocab_real) */
+  LP_ERR_REPLAY_ID_OUT_OF_RANGE = 6, /* device: a replay id not in {-1} U [0, vocab_real) */
+  LP_ERR_DEVICE_TIMEOUT = 7,       /* device: a pipeline wait ran past its limit */
+  LP_ERR_CUDA = 8,                 /* a CUDA runtime call failed */
+  LP_ERR_REPLAY_TOO_MANY_IDS = 9   /* device: a keep-mask row kept more than 64 ids */
+} lp_status;
+
+typedef enum {
+  LP_OP_FORWARD = 0,
+  LP_OP_FORWARD_FROM_LOGITS = 1,
+  LP_OP_TOP_P_REPLAY = 2,
+  LP_OP_BACKWARD = 3,
+  LP_OP_TOP_P_REPLAY_DENSE_MASK = 4
+} lp_op;
+
+/* Global id range [vocab_start, vocab_end) of one shard. */
+typedef struct {
+  int64_t vocab_start;
+  int64_t vocab_end;
+} lp_shard_range;
+
+/* Tensor-parallel vocabulary partition: the real and padded vocabulary sizes and
+ * the shards in rank order (page "feat(rl-kernel): add CUDA linear logp provider
+ * integration", Changes / Megatron integration). `shards` is a host array. */
+typedef struct {
+  int64_t vocab_real;
+  int64_t vocab_padded;
+  int32_t n_shards;
+  const lp_shard_range* shards;
+} lp_vocab_partition;
+
+/* Per-row outputs, fp32 device arrays of length T.
+ *   logp        z[y] - LSE (or -inf: target outside the support or device error)
+ *   lse         log sum over the support of exp z (-inf when the support is empty)
+ *   entropy     LSE - sum p z in nats; may be NULL; must be NULL for replay
+ *   shard_stats optional [n_shards][3][T]: per shard its local LSE, its local
+ *               target logit (z[y] if y lies in the shard, else 0) and its local
+ *               mean logit sum_{v in shard} softmax_local(z)_v z_v (0 for replay).
+ *               An empty shard reports (-inf, 0, 0). */
+typedef struct {
+  float* logp;
+  float* lse;
+  float* entropy;
+  float* shard_stats;
+} lp_outputs;
+
+/* Bytes of device scratch the operation needs for these sizes (0 for none).
+ * Returns 0 and is harmless for invalid arguments (the call itself reports them). */
+LP_API size_t lp_workspace_size(lp_op op, int64_t T, int64_t H, const lp_vocab_partition* part);
+
+/* Fused linear-logp forward (page "feat(rl-kernel): add CUDA linear logp provider
+ * integration", Changes): logp, LSE and optional entropy of softmax((X W^T + b)/tau)
+ * over the real vocabulary, computed by a tcgen05 GEMM whose epilogue folds each
+ * vocabulary tile into per-row running statistics; logits never reach memory.
+ *   X     bf16 [T, H], row-major, H % 8 == 0
+ *   W     host array [n_shards] of device pointers, shard k bf16 [V_k, H] row-major
+ *         (NULL allowed for an empty shard)
+ *   bias  NULL, or host array [n_shards] of device pointers to bf16 [V_k] (entries may be NULL)
+ *   y     int32 [T] global target ids in [0, vocab_real)
+ *   tau   temperature, finite and > 0 */
+LP_API lp_status lp_forward(const void* X, int64_t T, int64_t H,
+                     const void* const* W, const void* const* bias,
+                     const lp_vocab_partition* part, const int32_t* y, float tau,
+                     const lp_outputs* out, void* workspace, size_t ws_bytes,
+                     lp_stream_t stream);
+
+/* Logits-reuse forward (page "feat(rl-kernel): add CUDA linear logp provider
+ * integration", Changes / Megatron integration: reuse local logits instead of a
+ * second projection). logits[k] is shard k's UNSCALED bf16 logits (X W^T + b)
+ * [T, V_k] with row stride ld[k] elements (ld[k] >= V_k, ld[k] % 8 == 0); the
+ * temperature is applied once, here. Streams the logits once from HBM. */
+LP_API lp_status lp_forward_from_logits(const void* const* logits, const int64_t* ld, int64_t T,
+                                 const lp_vocab_partition* part, const int32_t* y, float tau,
+                                 const lp_outputs* out, void* workspace, size_t ws_bytes,
+                                 lp_stream_t stream);
+
+/* Compact top-p replay (page "Perf/cuda compact top p replay", Summary and
+ * Walkthrough "CUDA kernel and empty-shard handling"): per row, the up to 64 ids
+ * in replay_ids[t][0..63] (-1 = unused slot; duplicates allowed) are validated,
+ * sorted ascending and deduplicated; z_v = (x_t . W[v] + b[v]) / tau is scored
+ * for those ids only (a gather GEMV, no full-vocabulary projection), and LSE is
+ * taken over that set. logp = z[y] - LSE if y is in the set, else -inf.
+ * Arguments as lp_forward, plus replay_ids int32 [T, 64]; out->entropy must be NULL. */
+LP_API lp_status lp_top_p_replay(const void* X, int64_t T, int64_t H,
+                          const void* const* W, const void* const* bias,
+                          const lp_vocab_partition* part, const int32_t* replay_ids,
+                          const int32_t* y, float tau, const lp_outputs* out,
+                          void* workspace, size_t ws_bytes, lp_stream_t stream);
+
+/* The dense keep-mask route the compact replay replaces (page "Perf/cuda compact
+ * top p replay", Validation: dense-mask and compact-support results are bitwise
+ * equal). keep_mask[k] is uint8 [T, V_k] (nonzero = id kept, padded ids ignored).
+ * Same outputs as lp_top_p_replay and bitwise equal to it for the same sets. */
+LP_API lp_status lp_top_p_replay_dense_mask(const void* X, int64_t T, int64_t H,
+                                     const void* const* W, const void* const* bias,
+                                     const lp_vocab_partition* part,
+                                     const uint8_t* const* keep_mask, const int32_t* y,
+                                     float tau, const lp_outputs* out, void* workspace,
+                                     size_t ws_bytes, lp_stream_t stream);
+
+/* Backward of sum_t grad_logp[t] * logp[t] (the gradient the provider's autograd
+ * contract implies; page "feat(rl-kernel): add CUDA linear logp provider
+ * integration", Summary). With p = softmax(z) over the real ids and lse the
+ * merged LSE from lp_forward:
+ *   G[t,v] = grad_logp[t] * (1[v == y_t] - exp(z[t,v] - lse[t])) / tau   (0 on padded ids)
+ *   dX = sum_k G_k W_k (fp32 [T,H]),  dW_k = G_k^T X (fp32 [V_k,H]),  db_k = sum_t G_k (fp32 [V_k]).
+ * dX, dW[k] and db[k] are overwritten. db may be NULL (then no bias gradient);
+ * dW entries may be NULL only for empty shards. */
+LP_API lp_status lp_backward(const void* X, int64_t T, int64_t H,
+                      const void* const* W, const void* const* bias,
+                      const lp_vocab_partition* part, const int32_t* y, float tau,
+                      const float* lse, const float* grad_logp,
+                      float* dX, float* const* dW, float* const* db,
+                      void* workspace, size_t ws_bytes, lp_stream_t stream);
+
+/* Synchronises `stream`, returns the first device-side error recorded on the
+ * current device since the last call (LP_OK if none) and clears it. */
+LP_API lp_status lp_get_device_error(lp_stream_t stream);
+
+/* 1 if the current device can run this library (sm_100 family, e.g. GB300), else 0. */
+LP_API int lp_device_supported(void);
+
+/* Static, human-readable name of a status code. */
+LP_API const char* lp_status_string(lp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LP_H_ */

@@ -1,0 +1,335 @@
+"""Deterministic fused linear-logp for GB300 (sm_103a): Python binding of liblp.so.
+
+Every entry point of the C ABI (include/lp.h) has a function of the same name here.
+This module only marshals arguments: it checks that tensors live on the GPU with the
+expected dtype and layout, allocates outputs and workspace through PyTorch, takes
+the current CUDA stream and calls the library. All arithmetic runs in the library's
+CUDA kernels; there is no CPU path. If liblp.so has not been built, importing the
+functions works but the first call raises ImportError.
+
+    part = VocabPartition(vocab_real=151936, vocab_padded=151936, ranges=((0, 151936),))
+    out = lp_forward(X, [W], None, part, y, tau=0.7)      # out["logp"], out["lse"], out["entropy"]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from ._build import LIB as LIB_PATH
+
+LP_MAX_SHARDS = 8
+LP_REPLAY_SLOTS = 64
+
+LP_OK = 0
+STATUS_NAMES = {
+    0: "LP_OK",
+    1: "LP_ERR_INVALID_ARG",
+    2: "LP_ERR_ALIGNMENT",
+    3: "LP_ERR_UNSUPPORTED_DEVICE",
+    4: "LP_ERR_WORKSPACE_TOO_SMALL",
+    5: "LP_ERR_TARGET_OUT_OF_RANGE",
+    6: "LP_ERR_REPLAY_ID_OUT_OF_RANGE",
+    7: "LP_ERR_DEVICE_TIMEOUT",
+    8: "LP_ERR_CUDA",
+    9: "LP_ERR_REPLAY_TOO_MANY_IDS",
+}
+
+LP_OP_FORWARD = 0
+LP_OP_FORWARD_FROM_LOGITS = 1
+LP_OP_TOP_P_REPLAY = 2
+LP_OP_BACKWARD = 3
+LP_OP_TOP_P_REPLAY_DENSE_MASK = 4
+
+# every symbol include/lp.h declares
+EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_from_logits", "lp_top_p_replay",
+            "lp_top_p_replay_dense_mask", "lp_backward", "lp_get_device_error",
+            "lp_device_supported", "lp_status_string")
+
+
+class LPError(RuntimeError):
+    """A non-OK lp_status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+@dataclass(frozen=True)
+class VocabPartition:
+    """Tensor-parallel vocabulary partition: contiguous ascending global-id ranges
+    covering [0, vocab_padded); ids >= vocab_real are padding."""
+    vocab_real: int
+    vocab_padded: int
+    ranges: Tuple[Tuple[int, int], ...]
+
+    @property
+    def n_shards(self) -> int:
+        return len(self.ranges)
+
+
+class _ShardRange(ctypes.Structure):
+    _fields_ = [("vocab_start", ctypes.c_int64), ("vocab_end", ctypes.c_int64)]
+
+
+class _Partition(ctypes.Structure):
+    _fields_ = [("vocab_real", ctypes.c_int64), ("vocab_padded", ctypes.c_int64),
+                ("n_shards", ctypes.c_int32), ("shards", ctypes.POINTER(_ShardRange))]
+
+
+class _Outputs(ctypes.Structure):
+    _fields_ = [("logp", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("entropy", ctypes.c_void_p), ("shard_stats", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded liblp.so (raises ImportError if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"liblp.so is not built ({LIB_PATH}); run "
+                          "`python -m lm_head_linear_tcgen05_gb300._build` or __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    P = ctypes.POINTER
+    L.lp_workspace_size.argtypes = [ctypes.c_int, i64, i64, P(_Partition)]
+    L.lp_workspace_size.restype = sz
+    L.lp_forward.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, P(_Outputs), vp, sz, vp]
+    L.lp_forward_from_logits.argtypes = [P(vp), P(i64), i64, P(_Partition), vp, f32, P(_Outputs), vp, sz, vp]
+    L.lp_top_p_replay.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, vp, f32, P(_Outputs), vp, sz, vp]
+    L.lp_top_p_replay_dense_mask.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), P(vp), vp, f32,
+                                             P(_Outputs), vp, sz, vp]
+    L.lp_backward.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, vp, vp, vp, P(vp), P(vp),
+                              vp, sz, vp]
+    L.lp_get_device_error.argtypes = [vp]
+    L.lp_device_supported.argtypes = []
+    L.lp_status_string.argtypes = [ctypes.c_int]
+    L.lp_status_string.restype = ctypes.c_char_p
+    for name in ("lp_forward", "lp_forward_from_logits", "lp_top_p_replay", "lp_top_p_replay_dense_mask",
+                 "lp_backward", "lp_get_device_error", "lp_device_supported"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _c_partition(part) -> Tuple[_Partition, object]:
+    n = len(part.ranges)
+    arr = (_ShardRange * max(n, 1))(*[_ShardRange(int(s), int(e)) for s, e in part.ranges])
+    cp = _Partition(int(part.vocab_real), int(part.vocab_padded), n, ctypes.cast(arr, ctypes.POINTER(_ShardRange)))
+    return cp, arr
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _ptr_array(ts) -> ctypes.Array:
+    return (ctypes.c_void_p * max(len(ts), 1))(*[_ptr(t) for t in ts])
+
+
+def _check(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(dev) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _raise(st: int, where: str):
+    if st != LP_OK:
+        raise LPError(st, where)
+
+
+def lp_status_string(status: int) -> str:
+    return lib().lp_status_string(int(status)).decode()
+
+
+def lp_device_supported() -> bool:
+    return bool(lib().lp_device_supported())
+
+
+def lp_workspace_size(op: int, T: int, H: int, part) -> int:
+    cp, _keep = _c_partition(part)
+    return int(lib().lp_workspace_size(int(op), int(T), int(H), ctypes.byref(cp)))
+
+
+def lp_get_device_error(stream: Optional[int] = None) -> int:
+    """Synchronise the stream and return (and clear) the sticky device error code."""
+    s = _stream(torch.cuda.current_device()) if stream is None else stream
+    return int(lib().lp_get_device_error(s))
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def _outputs(T: int, n_shards: int, device, entropy: bool, shard_stats: bool):
+    o = {"logp": torch.empty(T, dtype=torch.float32, device=device),
+         "lse": torch.empty(T, dtype=torch.float32, device=device),
+         "entropy": torch.empty(T, dtype=torch.float32, device=device) if entropy else None,
+         "shard_stats": torch.empty((n_shards, 3, T), dtype=torch.float32, device=device) if shard_stats else None}
+    co = _Outputs(_ptr(o["logp"]), _ptr(o["lse"]), _ptr(o["entropy"]), _ptr(o["shard_stats"]))
+    return o, co
+
+
+def _shard_list(ts, n: int, name: str, dtype, ndim: int, allow_none: bool):
+    if ts is None:
+        return [None] * n
+    if len(ts) != n:
+        raise ValueError(f"{name} must have one entry per shard ({n})")
+    for k, t in enumerate(ts):
+        if t is None:
+            if not allow_none:
+                raise ValueError(f"{name}[{k}] is None")
+            continue
+        _check(t, f"{name}[{k}]", dtype, ndim)
+    return list(ts)
+
+
+# ------------------------------------------------------------------ entry points
+
+def lp_forward(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optional[Sequence[torch.Tensor]], part,
+               y: torch.Tensor, tau: float, entropy: bool = True, shard_stats: bool = False,
+               workspace: Optional[torch.Tensor] = None) -> dict:
+    """Fused linear-logp forward. X bf16 [T,H]; W[k] bf16 [V_k,H]; bias None or per-shard
+    bf16 [V_k]; y int32 [T]. Returns dict of fp32 tensors logp, lse, entropy, shard_stats."""
+    _check(X, "X", torch.bfloat16, 2)
+    _check(y, "y", torch.int32, 1)
+    n = len(part.ranges)
+    W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
+    bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
+    T, H = X.shape
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(X.device):
+        need = lp_workspace_size(LP_OP_FORWARD, T, H, part)
+        ws, wsb = _workspace(need, X.device, workspace)
+        o, co = _outputs(T, n, X.device, entropy, shard_stats)
+        st = lib().lp_forward(X.data_ptr(), T, H, _ptr_array(W), _ptr_array(bias) if bias is not None else None,
+                              ctypes.byref(cp), y.data_ptr(), float(tau), ctypes.byref(co), _ptr(ws), wsb,
+                              _stream(X.device))
+    _raise(st, "lp_forward")
+    return o
+
+
+def lp_forward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tensor, tau: float,
+                           entropy: bool = True, shard_stats: bool = False) -> dict:
+    """Logits-reuse forward from unscaled bf16 logits[k] [T, V_k] (row stride = stride(0))."""
+    _check(y, "y", torch.int32, 1)
+    n = len(part.ranges)
+    T = y.shape[0]
+    ld = (ctypes.c_int64 * max(n, 1))()
+    for k, L in enumerate(logits):
+        if L is None:
+            continue
+        if not (isinstance(L, torch.Tensor) and L.is_cuda and L.dtype == torch.bfloat16 and L.dim() == 2):
+            raise TypeError(f"logits[{k}] must be a 2-D bf16 CUDA tensor")
+        if L.stride(1) != 1 or L.shape[0] != T:
+            raise ValueError(f"logits[{k}] must be [T, V_k] with unit column stride")
+        ld[k] = L.stride(0)
+    if len(logits) != n:
+        raise ValueError("logits must have one entry per shard")
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(y.device):
+        o, co = _outputs(T, n, y.device, entropy, shard_stats)
+        st = lib().lp_forward_from_logits(_ptr_array(logits), ld, T, ctypes.byref(cp), y.data_ptr(), float(tau),
+                                          ctypes.byref(co), None, 0, _stream(y.device))
+    _raise(st, "lp_forward_from_logits")
+    return o
+
+
+def lp_top_p_replay(X: torch.Tensor, W, bias, part, replay_ids: torch.Tensor, y: torch.Tensor, tau: float,
+                    shard_stats: bool = False) -> dict:
+    """Compact top-p replay: replay_ids int32 [T, 64] (-1 = unused slot)."""
+    _check(X, "X", torch.bfloat16, 2)
+    _check(y, "y", torch.int32, 1)
+    _check(replay_ids, "replay_ids", torch.int32, 2)
+    if replay_ids.shape[1] != LP_REPLAY_SLOTS or replay_ids.shape[0] != X.shape[0]:
+        raise ValueError("replay_ids must be [T, 64]")
+    n = len(part.ranges)
+    W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
+    bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
+    T, H = X.shape
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(X.device):
+        o, co = _outputs(T, n, X.device, False, shard_stats)
+        st = lib().lp_top_p_replay(X.data_ptr(), T, H, _ptr_array(W), _ptr_array(bias) if bias is not None else None,
+                                   ctypes.byref(cp), replay_ids.data_ptr(), y.data_ptr(), float(tau),
+                                   ctypes.byref(co), None, 0, _stream(X.device))
+    _raise(st, "lp_top_p_replay")
+    return o
+
+
+def lp_top_p_replay_dense_mask(X: torch.Tensor, W, bias, part, keep_mask: Sequence[torch.Tensor], y: torch.Tensor,
+                               tau: float, shard_stats: bool = False,
+                               workspace: Optional[torch.Tensor] = None) -> dict:
+    """Dense keep-mask route: keep_mask[k] uint8 [T, V_k]; bitwise equal to lp_top_p_replay."""
+    _check(X, "X", torch.bfloat16, 2)
+    _check(y, "y", torch.int32, 1)
+    n = len(part.ranges)
+    W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
+    bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
+    keep_mask = _shard_list(keep_mask, n, "keep_mask", torch.uint8, 2, True)
+    T, H = X.shape
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(X.device):
+        need = lp_workspace_size(LP_OP_TOP_P_REPLAY_DENSE_MASK, T, H, part)
+        ws, wsb = _workspace(need, X.device, workspace)
+        o, co = _outputs(T, n, X.device, False, shard_stats)
+        st = lib().lp_top_p_replay_dense_mask(X.data_ptr(), T, H, _ptr_array(W),
+                                              _ptr_array(bias) if bias is not None else None, ctypes.byref(cp),
+                                              _ptr_array(keep_mask), y.data_ptr(), float(tau), ctypes.byref(co),
+                                              _ptr(ws), wsb, _stream(X.device))
+    _raise(st, "lp_top_p_replay_dense_mask")
+    return o
+
+
+def lp_backward(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse: torch.Tensor,
+                grad_logp: torch.Tensor, bias_grad: bool = True,
+                workspace: Optional[torch.Tensor] = None) -> dict:
+    """Backward of sum_t grad_logp[t] logp[t]: returns fp32 dX [T,H], dW (per shard [V_k,H]),
+    db (per shard [V_k], or None). `lse` is the merged LSE returned by lp_forward."""
+    _check(X, "X", torch.bfloat16, 2)
+    _check(y, "y", torch.int32, 1)
+    _check(lse, "lse", torch.float32, 1)
+    _check(grad_logp, "grad_logp", torch.float32, 1)
+    n = len(part.ranges)
+    W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
+    bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
+    T, H = X.shape
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(X.device):
+        need = lp_workspace_size(LP_OP_BACKWARD, T, H, part)
+        ws, wsb = _workspace(need, X.device, workspace)
+        dX = torch.empty((T, H), dtype=torch.float32, device=X.device)
+        dW = [torch.empty((e - s, H), dtype=torch.float32, device=X.device) if e > s else None
+              for s, e in part.ranges]
+        db = [torch.empty(e - s, dtype=torch.float32, device=X.device) if e > s else None
+              for s, e in part.ranges] if bias_grad else None
+        st = lib().lp_backward(X.data_ptr(), T, H, _ptr_array(W), _ptr_array(bias) if bias is not None else None,
+                               ctypes.byref(cp), y.data_ptr(), float(tau), lse.data_ptr(), grad_logp.data_ptr(),
+                               dX.data_ptr(), _ptr_array(dW), _ptr_array(db) if db is not None else None,
+                               _ptr(ws), wsb, _stream(X.device))
+    _raise(st, "lp_backward")
+    return {"dX": dX, "dW": dW, "db": db}

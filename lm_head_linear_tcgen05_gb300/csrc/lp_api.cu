@@ -1,0 +1,448 @@
+// lp_api.cu - the C ABI of liblp.so: argument validation, per-device set-up, tensor
+// maps, workspace carving and kernel dispatch. Declarations and the contract of every
+// entry point are in include/lp.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "lp_internal.h"
+
+namespace lp {
+
+// Sticky per-device error word: the first device-detected error since the last
+// lp_get_device_error(). Kernels receive its device address as a parameter.
+__device__ unsigned int g_error_word;
+
+__global__ void probe_kernel() {}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool init = false;
+  bool supported = false;
+  int num_sms = 0;
+  unsigned int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Resolves, once per device (with that device current), whether this library's
+// sm_103a code can run there, the SM count and the device address of the error word.
+lp_status device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return LP_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.init) {
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, probe_kernel) != cudaSuccess) {
+      cudaGetLastError();
+      st.supported = false;
+    } else {
+      int sms = 0;
+      void* err = nullptr;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaGetSymbolAddress(&err, g_error_word) != cudaSuccess) {
+        cudaGetLastError();
+        return LP_ERR_CUDA;
+      }
+      st.num_sms = sms;
+      st.err = static_cast<unsigned int*>(err);
+      st.supported = true;
+    }
+    st.init = true;
+  }
+  if (!st.supported) return LP_ERR_UNSUPPORTED_DEVICE;
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      cudaGetLastError();
+      return LP_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = &st;
+  return LP_OK;
+}
+
+}  // namespace
+
+// bf16 row-major matrix [rows, inner] with row stride ld elements, boxes of
+// 64 (inner) x box_rows, 128-byte swizzle, out-of-bounds elements read as zero.
+bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
+                    uint32_t box_rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+lp_status check_partition(const lp_vocab_partition* part, Shards* sh) {
+  if (part == nullptr || part->shards == nullptr) return LP_ERR_INVALID_ARG;
+  const int n = part->n_shards;
+  if (n < 1 || n > LP_MAX_SHARDS) return LP_ERR_INVALID_ARG;
+  if (part->vocab_real < 1 || part->vocab_real > part->vocab_padded || part->vocab_padded > INT32_MAX)
+    return LP_ERR_INVALID_ARG;
+  int64_t expect = 0;
+  for (int k = 0; k < n; ++k) {
+    const int64_t s = part->shards[k].vocab_start, e = part->shards[k].vocab_end;
+    if (s != expect || e < s) return LP_ERR_INVALID_ARG;
+    expect = e;
+    sh->start[k] = s;
+    sh->end[k] = e;
+    sh->width[k] = e - s;
+    const int64_t r = (e < part->vocab_real ? e : part->vocab_real) - s;
+    sh->real[k] = r > 0 ? r : 0;
+  }
+  if (expect != part->vocab_padded) return LP_ERR_INVALID_ARG;
+  sh->n = n;
+  sh->vocab_real = part->vocab_real;
+  sh->vocab_padded = part->vocab_padded;
+  return LP_OK;
+}
+
+bool valid_rows(int64_t T) { return T >= 1 && T <= (int64_t(1) << 30); }
+bool valid_hidden(int64_t H) { return H >= 8 && H <= 65536 && H % 8 == 0; }
+bool valid_tau(float tau) { return std::isfinite(tau) && tau > 0.f; }
+
+size_t forward_ws_bytes(int64_t T, const Shards& sh) {
+  int64_t nb = 0;
+  for (int k = 0; k < sh.n; ++k) nb += (sh.real[k] + kFwdBlockN - 1) / kFwdBlockN;
+  const size_t per = align_up(size_t(nb) * size_t(T) * sizeof(float), 256);
+  return 3 * per + align_up(size_t(T) * sizeof(float), 256);
+}
+
+}  // namespace lp
+
+using namespace lp;
+
+extern "C" {
+
+const char* lp_status_string(lp_status s) {
+  switch (s) {
+    case LP_OK: return "LP_OK";
+    case LP_ERR_INVALID_ARG: return "LP_ERR_INVALID_ARG: invalid argument";
+    case LP_ERR_ALIGNMENT: return "LP_ERR_ALIGNMENT: a pointer or row stride is not 16-byte aligned";
+    case LP_ERR_UNSUPPORTED_DEVICE: return "LP_ERR_UNSUPPORTED_DEVICE: no sm_103 device is current";
+    case LP_ERR_WORKSPACE_TOO_SMALL: return "LP_ERR_WORKSPACE_TOO_SMALL: workspace smaller than lp_workspace_size()";
+    case LP_ERR_TARGET_OUT_OF_RANGE: return "LP_ERR_TARGET_OUT_OF_RANGE: a target id is outside [0, vocab_real)";
+    case LP_ERR_REPLAY_ID_OUT_OF_RANGE: return "LP_ERR_REPLAY_ID_OUT_OF_RANGE: a replay id is outside [0, vocab_real)";
+    case LP_ERR_DEVICE_TIMEOUT: return "LP_ERR_DEVICE_TIMEOUT: a pipeline wait exceeded its time limit";
+    case LP_ERR_CUDA: return "LP_ERR_CUDA: a CUDA runtime call failed";
+    case LP_ERR_REPLAY_TOO_MANY_IDS: return "LP_ERR_REPLAY_TOO_MANY_IDS: a keep-mask row keeps more than 64 ids";
+  }
+  return "unknown lp_status";
+}
+
+int lp_device_supported(void) {
+  DeviceState* st = nullptr;
+  return device_state(&st) == LP_OK ? 1 : 0;
+}
+
+size_t lp_workspace_size(lp_op op, int64_t T, int64_t H, const lp_vocab_partition* part) {
+  Shards sh;
+  if (!valid_rows(T) || check_partition(part, &sh) != LP_OK) return 0;
+  switch (op) {
+    case LP_OP_FORWARD: return forward_ws_bytes(T, sh);
+    case LP_OP_FORWARD_FROM_LOGITS: return 0;
+    case LP_OP_TOP_P_REPLAY: return 0;
+    case LP_OP_TOP_P_REPLAY_DENSE_MASK: return align_up(size_t(T) * LP_REPLAY_SLOTS * sizeof(int32_t), 256);
+    case LP_OP_BACKWARD: return valid_hidden(H) ? backward_ws_bytes(T, H, sh) : 0;
+  }
+  return 0;
+}
+
+lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, const void* const* bias,
+                     const lp_vocab_partition* part, const int32_t* y, float tau, const lp_outputs* out,
+                     void* workspace, size_t ws_bytes, lp_stream_t stream) {
+  Shards sh;
+  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (X == nullptr || W == nullptr || y == nullptr || out == nullptr || out->logp == nullptr ||
+      out->lse == nullptr || !valid_rows(T) || !valid_hidden(H) || !valid_tau(tau))
+    return LP_ERR_INVALID_ARG;
+  for (int k = 0; k < sh.n; ++k)
+    if (sh.real[k] > 0 && W[k] == nullptr) return LP_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(workspace)) return LP_ERR_ALIGNMENT;
+  for (int k = 0; k < sh.n; ++k)
+    if (sh.real[k] > 0 && !aligned16(W[k])) return LP_ERR_ALIGNMENT;
+  const size_t need = forward_ws_bytes(T, sh);
+  if (workspace == nullptr || ws_bytes < need) return LP_ERR_WORKSPACE_TOO_SMALL;
+
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_bf16_2d(&p.maps[0], X, uint64_t(H), uint64_t(T), uint64_t(H), kFwdBlockM)) return LP_ERR_CUDA;
+  int nb = 0;
+  for (int k = 0; k < sh.n; ++k) {
+    if (sh.real[k] > 0 &&
+        !encode_bf16_2d(&p.maps[1 + k], W[k], uint64_t(H), uint64_t(sh.width[k]), uint64_t(H), kFwdBlockN))
+      return LP_ERR_CUDA;
+    p.bias[k] = bias != nullptr ? static_cast<const __nv_bfloat16*>(bias[k]) : nullptr;
+    p.shard_start[k] = sh.start[k];
+    p.shard_width[k] = int32_t(sh.real[k]);
+    p.nb_start[k] = nb;
+    nb += int((sh.real[k] + kFwdBlockN - 1) / kFwdBlockN);
+  }
+  p.nb_start[sh.n] = nb;
+  p.keep_maps = 1u;  // X is re-read by every vocabulary block: keep it in L2
+  p.n_shards = sh.n;
+  p.T = int32_t(T);
+  p.num_m_blocks = int32_t((T + kFwdBlockM - 1) / kFwdBlockM);
+  p.num_k_blocks = int32_t((H + kFwdBlockK - 1) / kFwdBlockK);
+  p.total_tiles = nb * p.num_m_blocks;
+  p.err = dev->err;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.y = y;
+  p.vocab_real = sh.vocab_real;
+  p.scale_log2 = float(1.4426950408889634 / double(tau));
+  p.inv_tau = float(1.0 / double(tau));
+  const size_t per = align_up(size_t(nb) * size_t(T) * sizeof(float), 256);
+  char* ws = static_cast<char*>(workspace);
+  p.ws_m = reinterpret_cast<float*>(ws);
+  p.ws_s = reinterpret_cast<float*>(ws + per);
+  p.ws_a = reinterpret_cast<float*>(ws + 2 * per);
+  p.ws_t = reinterpret_cast<float*>(ws + 3 * per);
+
+  MergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.ws_m = p.ws_m;
+  mp.ws_s = p.ws_s;
+  mp.ws_a = p.ws_a;
+  mp.ws_t = p.ws_t;
+  mp.y = y;
+  mp.logp = out->logp;
+  mp.lse = out->lse;
+  mp.entropy = out->entropy;
+  mp.shard_stats = out->shard_stats;
+  mp.err = dev->err;
+  mp.vocab_real = sh.vocab_real;
+  for (int k = 0; k < sh.n; ++k) {
+    mp.shard_start[k] = sh.start[k];
+    mp.shard_end[k] = sh.end[k];
+    mp.nb_start[k] = p.nb_start[k];
+  }
+  mp.nb_start[sh.n] = nb;
+  mp.n_shards = sh.n;
+  mp.T = int32_t(T);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_fused_forward(p, dev->num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
+  if (launch_merge(mp, s) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
+}
+
+lp_status lp_forward_from_logits(const void* const* logits, const int64_t* ld, int64_t T,
+                                 const lp_vocab_partition* part, const int32_t* y, float tau,
+                                 const lp_outputs* out, void* workspace, size_t ws_bytes, lp_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  Shards sh;
+  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (logits == nullptr || ld == nullptr || y == nullptr || out == nullptr || out->logp == nullptr ||
+      out->lse == nullptr || !valid_rows(T) || !valid_tau(tau))
+    return LP_ERR_INVALID_ARG;
+  for (int k = 0; k < sh.n; ++k) {
+    if (sh.real[k] == 0) continue;
+    if (logits[k] == nullptr || ld[k] < sh.width[k]) return LP_ERR_INVALID_ARG;
+    if (!aligned16(logits[k]) || ld[k] % 8 != 0) return LP_ERR_ALIGNMENT;
+  }
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+
+  StreamParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int k = 0; k < sh.n; ++k) {
+    p.logits[k] = static_cast<const __nv_bfloat16*>(logits[k]);
+    p.ld[k] = ld[k];
+    p.shard_start[k] = sh.start[k];
+    p.shard_width[k] = sh.real[k];
+    p.shard_end[k] = sh.end[k];
+  }
+  p.y = y;
+  p.logp = out->logp;
+  p.lse = out->lse;
+  p.entropy = out->entropy;
+  p.shard_stats = out->shard_stats;
+  p.err = dev->err;
+  p.vocab_real = sh.vocab_real;
+  p.n_shards = sh.n;
+  p.T = int32_t(T);
+  p.scale_log2 = float(1.4426950408889634 / double(tau));
+  p.inv_tau = float(1.0 / double(tau));
+  if (launch_stream_logits(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
+}
+
+static lp_status replay_common(const void* X, int64_t T, int64_t H, const void* const* W, const void* const* bias,
+                               const lp_vocab_partition* part, const int32_t* y, float tau, const lp_outputs* out,
+                               Shards* sh, ReplayParams* p, DeviceState** dev) {
+  if (check_partition(part, sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (X == nullptr || W == nullptr || y == nullptr || out == nullptr || out->logp == nullptr ||
+      out->lse == nullptr || out->entropy != nullptr || !valid_rows(T) || !valid_hidden(H) || !valid_tau(tau))
+    return LP_ERR_INVALID_ARG;
+  for (int k = 0; k < sh->n; ++k) {
+    if (sh->real[k] == 0) continue;
+    if (W[k] == nullptr) return LP_ERR_INVALID_ARG;
+    if (!aligned16(W[k])) return LP_ERR_ALIGNMENT;
+  }
+  if (!aligned16(X)) return LP_ERR_ALIGNMENT;
+  lp_status st = device_state(dev);
+  if (st != LP_OK) return st;
+  std::memset(p, 0, sizeof(*p));
+  p->X = static_cast<const __nv_bfloat16*>(X);
+  for (int k = 0; k < sh->n; ++k) {
+    p->W[k] = static_cast<const __nv_bfloat16*>(W[k]);
+    p->bias[k] = bias != nullptr ? static_cast<const __nv_bfloat16*>(bias[k]) : nullptr;
+    p->shard_start[k] = sh->start[k];
+    p->shard_end[k] = sh->end[k];
+  }
+  p->y = y;
+  p->logp = out->logp;
+  p->lse = out->lse;
+  p->shard_stats = out->shard_stats;
+  p->err = (*dev)->err;
+  p->vocab_real = sh->vocab_real;
+  p->n_shards = sh->n;
+  p->T = int32_t(T);
+  p->H = int32_t(H);
+  p->inv_tau = float(1.0 / double(tau));
+  return LP_OK;
+}
+
+lp_status lp_top_p_replay(const void* X, int64_t T, int64_t H, const void* const* W, const void* const* bias,
+                          const lp_vocab_partition* part, const int32_t* replay_ids, const int32_t* y, float tau,
+                          const lp_outputs* out, void* workspace, size_t ws_bytes, lp_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  if (replay_ids == nullptr) return LP_ERR_INVALID_ARG;
+  Shards sh;
+  ReplayParams p;
+  DeviceState* dev = nullptr;
+  lp_status st = replay_common(X, T, H, W, bias, part, y, tau, out, &sh, &p, &dev);
+  if (st != LP_OK) return st;
+  p.ids = replay_ids;
+  if (launch_replay(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
+}
+
+lp_status lp_top_p_replay_dense_mask(const void* X, int64_t T, int64_t H, const void* const* W,
+                                     const void* const* bias, const lp_vocab_partition* part,
+                                     const uint8_t* const* keep_mask, const int32_t* y, float tau,
+                                     const lp_outputs* out, void* workspace, size_t ws_bytes, lp_stream_t stream) {
+  if (keep_mask == nullptr) return LP_ERR_INVALID_ARG;
+  Shards sh;
+  ReplayParams p;
+  DeviceState* dev = nullptr;
+  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  for (int k = 0; k < sh.n; ++k)
+    if (sh.real[k] > 0 && keep_mask[k] == nullptr) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T)) return LP_ERR_INVALID_ARG;
+  const size_t need = align_up(size_t(T) * LP_REPLAY_SLOTS * sizeof(int32_t), 256);
+  lp_status st = replay_common(X, T, H, W, bias, part, y, tau, out, &sh, &p, &dev);
+  if (st != LP_OK) return st;
+  if (workspace == nullptr || ws_bytes < need) return LP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return LP_ERR_ALIGNMENT;
+  MaskParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  for (int k = 0; k < sh.n; ++k) {
+    mp.mask[k] = keep_mask[k];
+    mp.shard_start[k] = sh.start[k];
+    mp.shard_width[k] = sh.width[k];
+  }
+  mp.ids_out = static_cast<int32_t*>(workspace);
+  mp.err = dev->err;
+  mp.vocab_real = sh.vocab_real;
+  mp.n_shards = sh.n;
+  mp.T = int32_t(T);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_mask_compact(mp, s) != cudaSuccess) return LP_ERR_CUDA;
+  p.ids = mp.ids_out;
+  if (launch_replay(p, s) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
+}
+
+lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W, const void* const* bias,
+                      const lp_vocab_partition* part, const int32_t* y, float tau, const float* lse,
+                      const float* grad_logp, float* dX, float* const* dW, float* const* db, void* workspace,
+                      size_t ws_bytes, lp_stream_t stream) {
+  Shards sh;
+  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (X == nullptr || W == nullptr || y == nullptr || lse == nullptr || grad_logp == nullptr || dX == nullptr ||
+      dW == nullptr || !valid_rows(T) || !valid_hidden(H) || !valid_tau(tau))
+    return LP_ERR_INVALID_ARG;
+  for (int k = 0; k < sh.n; ++k) {
+    if (sh.width[k] == 0) continue;
+    if ((sh.real[k] > 0 && W[k] == nullptr) || dW[k] == nullptr || (db != nullptr && db[k] == nullptr))
+      return LP_ERR_INVALID_ARG;
+    if ((sh.real[k] > 0 && !aligned16(W[k])) || !aligned16(dW[k])) return LP_ERR_ALIGNMENT;
+  }
+  if (!aligned16(X) || !aligned16(dX) || !aligned16(workspace)) return LP_ERR_ALIGNMENT;
+  const size_t need = backward_ws_bytes(T, H, sh);
+  if (workspace == nullptr || ws_bytes < need) return LP_ERR_WORKSPACE_TOO_SMALL;
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+  BackwardArgs a;
+  a.X = X;
+  a.T = T;
+  a.H = H;
+  a.y = y;
+  a.tau = tau;
+  a.lse = lse;
+  a.grad = grad_logp;
+  a.dX = dX;
+  for (int k = 0; k < sh.n; ++k) {
+    a.W[k] = W[k];
+    a.bias[k] = bias != nullptr ? bias[k] : nullptr;
+    a.dW[k] = dW[k];
+    a.db[k] = db != nullptr ? db[k] : nullptr;
+  }
+  a.workspace = workspace;
+  a.err = dev->err;
+  a.num_sms = dev->num_sms;
+  return run_backward(a, sh, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_get_device_error(lp_stream_t stream) {
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int word = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LP_ERR_CUDA;
+  if (cudaMemcpyAsync(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return LP_ERR_CUDA;
+  if (cudaMemsetAsync(dev->err, 0, sizeof(word), s) != cudaSuccess) return LP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LP_ERR_CUDA;
+  return static_cast<lp_status>(word);
+}
+
+}  // extern "C"

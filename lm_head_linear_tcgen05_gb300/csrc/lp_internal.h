@@ -1,0 +1,161 @@
+// lp_internal.h - declarations shared by the translation units of liblp.so
+// (kernel parameter blocks, tile constants and the launchers lp_api.cu calls).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lp.h"
+
+namespace lp {
+
+// Tile of the tcgen05 GEMM pipeline: 128 rows x 256 columns, K walked in 64s.
+constexpr int kFwdBlockM = 128;
+constexpr int kFwdBlockN = 256;
+constexpr int kFwdBlockK = 64;
+
+// Validated vocabulary partition (host side).
+struct Shards {
+  int n;
+  int64_t vocab_real, vocab_padded;
+  int64_t start[LP_MAX_SHARDS], end[LP_MAX_SHARDS];
+  int64_t width[LP_MAX_SHARDS];  // vocab_end - vocab_start
+  int64_t real[LP_MAX_SHARDS];   // ids of the shard below vocab_real
+};
+
+// ------------------------------------------------------------- fused forward
+// Tensor-map slots of the GEMM kernels: maps[0] is the row operand (X, or G / G^T
+// in the backward), maps[1 + k] the operand of shard k.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+
+struct FwdParams {
+  CUtensorMap maps[LP_MAX_SHARDS + 1];  // [0] X [T, H]; [1 + k] W_k [V_k, H]; 128B swizzle
+  uint32_t keep_maps;                   // maps loaded with an L2 evict-last hint
+  int32_t total_tiles;
+  unsigned int* err;
+  uint64_t wait_limit_ns;
+  const __nv_bfloat16* bias[LP_MAX_SHARDS];
+  const int32_t* y;
+  float* ws_m;                          // [nb_total][T]
+  float* ws_s;                          // [nb_total][T]
+  float* ws_a;                          // [nb_total][T]
+  float* ws_t;                          // [T] target logit z[y], written by the tile holding y
+  int64_t vocab_real;
+  int64_t shard_start[LP_MAX_SHARDS];
+  int32_t shard_width[LP_MAX_SHARDS];   // real (unpadded) width of each shard
+  int32_t nb_start[LP_MAX_SHARDS + 1];  // first global vocabulary block of each shard
+  int32_t n_shards;
+  int32_t T;
+  int32_t num_m_blocks;
+  int32_t num_k_blocks;
+  float scale_log2;                     // log2(e) / tau
+  float inv_tau;                        // 1 / tau
+};
+
+// Merge of per-tile (or per-chunk) statistics, one warp per row.
+struct MergeParams {
+  const float* ws_m;
+  const float* ws_s;
+  const float* ws_a;
+  const float* ws_t;
+  const int32_t* y;
+  float* logp;
+  float* lse;
+  float* entropy;
+  float* shard_stats;
+  unsigned int* err;
+  int64_t vocab_real;
+  int64_t shard_start[LP_MAX_SHARDS];
+  int64_t shard_end[LP_MAX_SHARDS];
+  int32_t nb_start[LP_MAX_SHARDS + 1];
+  int32_t n_shards;
+  int32_t T;
+};
+
+// Logits-reuse streaming kernel, one CTA per row.
+struct StreamParams {
+  const __nv_bfloat16* logits[LP_MAX_SHARDS];
+  int64_t ld[LP_MAX_SHARDS];
+  int64_t shard_start[LP_MAX_SHARDS];
+  int64_t shard_width[LP_MAX_SHARDS];   // real (unpadded) columns of each shard
+  int64_t shard_end[LP_MAX_SHARDS];
+  const int32_t* y;
+  float* logp;
+  float* lse;
+  float* entropy;
+  float* shard_stats;
+  unsigned int* err;
+  int64_t vocab_real;
+  int32_t n_shards;
+  int32_t T;
+  float scale_log2;
+  float inv_tau;
+};
+
+// Compact top-p replay, one CTA per row.
+struct ReplayParams {
+  const __nv_bfloat16* X;
+  const __nv_bfloat16* W[LP_MAX_SHARDS];
+  const __nv_bfloat16* bias[LP_MAX_SHARDS];
+  const int32_t* ids;                   // [T][64]
+  const int32_t* y;
+  float* logp;
+  float* lse;
+  float* shard_stats;
+  unsigned int* err;
+  int64_t vocab_real;
+  int64_t shard_start[LP_MAX_SHARDS];
+  int64_t shard_end[LP_MAX_SHARDS];
+  int32_t n_shards;
+  int32_t T;
+  int32_t H;
+  float inv_tau;
+};
+
+// Dense keep-mask compaction into canonical replay slots.
+struct MaskParams {
+  const uint8_t* mask[LP_MAX_SHARDS];
+  int64_t shard_start[LP_MAX_SHARDS];
+  int64_t shard_width[LP_MAX_SHARDS];
+  int32_t* ids_out;                     // [T][64]
+  unsigned int* err;
+  int64_t vocab_real;
+  int32_t n_shards;
+  int32_t T;
+};
+
+// Backward: everything lp_backward validated, handed to the backward translation unit.
+struct BackwardArgs {
+  const void* X;
+  int64_t T, H;
+  const int32_t* y;
+  float tau;
+  const float* lse;
+  const float* grad;
+  float* dX;
+  const void* W[LP_MAX_SHARDS];
+  const void* bias[LP_MAX_SHARDS];
+  float* dW[LP_MAX_SHARDS];
+  float* db[LP_MAX_SHARDS];
+  void* workspace;
+  unsigned int* err;
+  int num_sms;
+};
+
+size_t backward_ws_bytes(int64_t T, int64_t H, const Shards& sh);
+lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s);
+
+// bf16 row-major [rows, inner] (row stride ld elements) as a TMA map with boxes of
+// 64 x box_rows elements, 128-byte swizzle and zero fill out of bounds.
+bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
+                    uint32_t box_rows);
+
+cudaError_t launch_fused_forward(const FwdParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+cudaError_t launch_stream_logits(const StreamParams& p, cudaStream_t s);
+cudaError_t launch_replay(const ReplayParams& p, cudaStream_t s);
+cudaError_t launch_mask_compact(const MaskParams& p, cudaStream_t s);
+
+}  // namespace lp

@@ -1,0 +1,164 @@
+// lp_stream.cu - logits-reuse path: LSE, target logp and entropy from precomputed
+// local logits, streamed once from HBM.
+//
+// Page "feat(rl-kernel): add CUDA linear logp provider integration", Changes /
+// Megatron integration: strict LM-head local logits are reused when available,
+// avoiding a second projection. Page "Perf/cuda compact top p replay", Summary:
+// temperature scaling happens exactly once for reused logits - the logits given
+// here are unscaled and 1/tau is applied in this kernel only.
+//
+// One CTA (512 threads) per row. Each thread streams 16-byte vectors (8 bf16) of
+// the row with four loads in flight, keeping an online base-2 statistic; the
+// threads are combined by a fixed shuffle tree per warp and then warp by warp in
+// ascending order, shard after shard in ascending order. The work split depends
+// only on the shard width, so a row's result never depends on T.
+#include <cuda_bf16.h>
+
+#include "lp_device.cuh"
+
+namespace lp {
+
+namespace {
+
+constexpr int kStreamThreads = 512;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Per-thread online statistic over raw (unscaled) logits x: the running maximum is
+// tracked on x, m = max(x) * c2 and d = x * c2 - m, so u = x * c2 is never rounded
+// separately from the subtraction. -inf logits (entries a caller masked out) add
+// nothing; a thread that saw only -inf stays empty.
+struct RawStat {
+  float xmax;  // running max of x (-inf while empty)
+  float m;     // xmax * c2
+  float s, a;
+};
+
+__device__ __forceinline__ void raw_rescale(RawStat& st, float new_xmax, float c2) {
+  const float nm = __fmul_rn(new_xmax, c2);
+  if (st.xmax == -INFINITY) {
+    st.s = 0.f;
+    st.a = 0.f;
+  } else {
+    const float d = __fsub_rn(st.m, nm);
+    const float e = hw_ex2(d);
+    st.a = __fmul_rn(e, __fmaf_rn(d, st.s, st.a));
+    st.s = __fmul_rn(st.s, e);
+  }
+  st.xmax = new_xmax;
+  st.m = nm;
+}
+
+__device__ __forceinline__ void raw_push8(RawStat& st, const uint4 v, float c2) {
+  float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  const float vmax = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+  if (vmax > st.xmax) raw_rescale(st, vmax, c2);
+  const float nm = -st.m;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    // clamping at -256 (2^-256 flushes to 0) keeps -inf (masked) logits from
+    // producing 0 * -inf in the entropy sum
+    const float d = fmaxf(__fmaf_rn(x[j], c2, nm), -256.f);
+    const float e = hw_ex2(d);
+    st.s = __fadd_rn(st.s, e);
+    st.a = __fmaf_rn(e, d, st.a);
+  }
+}
+
+__device__ __forceinline__ void raw_push1(RawStat& st, float x, float c2) {
+  if (x > st.xmax) raw_rescale(st, x, c2);
+  const float d = fmaxf(__fmaf_rn(x, c2, -st.m), -256.f);
+  const float e = hw_ex2(d);
+  st.s = __fadd_rn(st.s, e);
+  st.a = __fmaf_rn(e, d, st.a);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kStreamThreads) stream_logits_kernel(const __grid_constant__ StreamParams p) {
+  __shared__ Stat red[kStreamWarps];
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const float c2 = p.scale_log2;
+  const int yv = __ldg(p.y + row);
+  const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
+  const size_t T = size_t(p.T);
+
+  Stat tot = stat_empty();  // meaningful in thread 0 only
+  float t_val = 0.f;
+
+  for (int k = 0; k < p.n_shards; ++k) {
+    const int64_t width = p.shard_width[k];
+    RawStat st{-INFINITY, -INFINITY, 0.f, 0.f};
+    if (width > 0) {
+      const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
+      const uint4* Lv = reinterpret_cast<const uint4*>(L);
+      const int64_t nvec = width >> 3;
+      int64_t v = tid;
+      for (; v + (kUnroll - 1) * kStreamThreads < nvec; v += kUnroll * kStreamThreads) {
+        uint4 q[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) q[u] = ld_stream(Lv + v + u * kStreamThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) raw_push8(st, q[u], c2);
+      }
+      for (; v < nvec; v += kStreamThreads) raw_push8(st, ld_stream(Lv + v), c2);
+      // ragged tail (width % 8 elements) by the first threads, in ascending order
+      const int64_t tail0 = nvec << 3;
+      if (tail0 + tid < width) raw_push1(st, __bfloat162float(L[tail0 + tid]), c2);
+    }
+    Stat loc{st.m, st.s, st.a};
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const Stat o{__shfl_down_sync(0xffffffffu, loc.m, off), __shfl_down_sync(0xffffffffu, loc.s, off),
+                   __shfl_down_sync(0xffffffffu, loc.a, off)};
+      if (lane < off) stat_merge(loc, o);
+    }
+    if (lane == 0) red[warp] = loc;
+    __syncthreads();
+    if (tid == 0) {
+      Stat sh = red[0];
+      for (int w = 1; w < kStreamWarps; ++w) stat_merge(sh, red[w]);
+      const bool own = y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k];
+      float tk = 0.f;
+      if (own) {
+        const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
+        tk = __fmul_rn(__bfloat162float(L[yv - p.shard_start[k]]), p.inv_tau);
+        t_val = tk;
+      }
+      if (p.shard_stats != nullptr) {
+        float* ss = p.shard_stats + size_t(k) * 3 * T;
+        ss[row] = stat_lse(sh);
+        ss[T + row] = tk;
+        ss[2 * T + row] = stat_mean(sh);
+      }
+      stat_merge(tot, sh);
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const float lse = stat_lse(tot);
+    p.lse[row] = lse;
+    if (p.entropy != nullptr) p.entropy[row] = stat_entropy(tot);
+    if (!y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
+    p.logp[row] = (y_ok && tot.m != -INFINITY) ? __fsub_rn(t_val, lse) : -INFINITY;
+  }
+}
+
+cudaError_t launch_stream_logits(const StreamParams& p, cudaStream_t s) {
+  stream_logits_kernel<<<p.T, kStreamThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace lp

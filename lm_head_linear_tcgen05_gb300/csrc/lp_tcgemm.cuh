@@ -1,0 +1,220 @@
+// lp_tcgemm.cuh - persistent warp-specialised bf16 GEMM pipeline on tcgen05/TMEM.
+//
+// C_tile[128 x 256] = sum_k A[rows, k] * B[cols, k]  (both operands K-major bf16,
+// fp32 accumulation in tensor memory), followed by an epilogue supplied by the
+// caller that reads the accumulator straight out of TMEM. The kernel is persistent
+// (one CTA per SM, tiles handed out round-robin) and warp specialised:
+//
+//   warp 0      TMA producer: A and B boxes of 64 (K) x 128 / 256 rows, 128-byte
+//               swizzle, into a kStages-deep shared-memory ring (mbarrier full/empty);
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
+//               issues tcgen05.mma kind::f16 (M=128, N=256, K=16) from one thread,
+//               committing each stage back to the producer and each finished tile
+//               to the epilogue;
+//   warps 2..5  epilogue: warp w may read TMEM lanes 32*(w%4)..+31, so each thread
+//               owns one row of the tile; the callback runs while the MMA warp
+//               fills the other accumulator.
+//
+// Every mbarrier wait is bounded in time (see lp_device.cuh): a wait that runs past
+// the limit records LP_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag and every
+// role leaves its loop; the producer then waits (bounded) for its copies in flight,
+// the MMA warp for its MMAs, and TMEM is freed before the CTA exits.
+//
+// An epilogue type E provides
+//   struct E::Params           with members `CUtensorMap maps[kGemmMaps]`,
+//                              `uint32_t keep_maps` (bit i: map i is small and
+//                              reused, loaded with an L2 evict-last hint),
+//                              `int total_tiles`, `unsigned int* err`,
+//                              `uint64_t wait_limit_ns`;
+//   static TileJob E::job(const Params&, int tile);
+//   static void E::run(const Params&, int tile, uint32_t tmem_row_base, int quarter, int lane);
+// `tmem_row_base` addresses column 0 of the tile's accumulator at this warp's first
+// lane; column c of this thread's row is at tmem_row_base + c.
+#pragma once
+
+#include "lp_device.cuh"
+
+namespace lp {
+
+constexpr int kGemmBlockM = kFwdBlockM;
+constexpr int kGemmBlockN = kFwdBlockN;
+constexpr int kGemmBlockK = kFwdBlockK;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int kGemmStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr int kGemmTmemCols = 512;
+constexpr int kGemmMaps = LP_MAX_SHARDS + 1;
+
+constexpr uint32_t kGemmStageA = kGemmBlockM * kGemmBlockK * 2;  // 16 KB
+constexpr uint32_t kGemmStageB = kGemmBlockN * kGemmBlockK * 2;  // 32 KB
+constexpr uint32_t kGemmStageBytes = kGemmStageA + kGemmStageB;
+
+// What one tile reads: box rows a_y.. of map a_map and b_y.. of map b_map, for k
+// blocks kb0 .. kb0 + nkb - 1 (coordinates in elements; x = k * 64).
+struct TileJob {
+  int a_map, b_map;
+  int a_y, b_y;
+  int kb0, nkb;
+};
+
+struct GemmSync {
+  uint64_t full[kGemmStages];
+  uint64_t empty[kGemmStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kGemmSmemBytes = 1024 + size_t(kGemmStages) * kGemmStageBytes + sizeof(GemmSync);
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) break;
+  }
+}
+
+template <class E>
+__global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ typename E::Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kGemmStages * kGemmStageA;
+  GemmSync* sync = reinterpret_cast<GemmSync*>(smem + kGemmStages * kGemmStageBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(&sync->full[s], 1);
+      mbar_init(&sync->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sync->tfull[b], 1);
+      mbar_init(&sync->tempty[b], 4);
+    }
+    mbar_init(&sync->done, 1);
+    sync->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sync->tmem_base, kGemmTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sync->tmem_base;
+  volatile int* abort = &sync->abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // --------------------------------------------------------- TMA producer
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_norm = l2_policy_evict_normal();
+      uint32_t stage = 0, phase = 0;
+      uint32_t armed = 0, armed_phase = 0;  // stages with a copy issued, and its phase
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+        const TileJob j = E::job(p, tile);
+        for (int kb = 0; kb < j.nkb; ++kb) {
+          if (!mbar_wait(&sync->empty[stage], phase ^ 1u, abort, p.wait_limit_ns, p.err)) {
+            ok = false;
+            break;
+          }
+          const int x = (j.kb0 + kb) * kGemmBlockK;
+          mbar_arrive_expect_tx(&sync->full[stage], kGemmStageBytes);
+          tma_load_2d(sA + stage * kGemmStageA, &p.maps[j.a_map], &sync->full[stage], x, j.a_y,
+                      ((p.keep_maps >> j.a_map) & 1u) ? pol_keep : pol_norm);
+          tma_load_2d(sB + stage * kGemmStageB, &p.maps[j.b_map], &sync->full[stage], x, j.b_y,
+                      ((p.keep_maps >> j.b_map) & 1u) ? pol_keep : pol_norm);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kGemmStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kGemmStages; ++s)
+          if (armed & (1u << s)) drain_wait(&sync->full[s], (armed_phase >> s) & 1u, p.wait_limit_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBlockM, kGemmBlockN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+        const TileJob j = E::job(p, tile);
+        if (!mbar_wait(&sync->tempty[acc], acc_phase ^ 1u, abort, p.wait_limit_ns, p.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * kGemmBlockN;
+        for (int kb = 0; kb < j.nkb; ++kb) {
+          if (!mbar_wait(&sync->full[stage], phase, abort, p.wait_limit_ns, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = sw128_kmajor_desc(smem_u32(sA + stage * kGemmStageA));
+          const uint64_t b_desc = sw128_kmajor_desc(smem_u32(sB + stage * kGemmStageB));
+#pragma unroll
+          for (int k = 0; k < kGemmBlockK / 16; ++k)
+            umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit(&sync->empty[stage]);
+          if (++stage == kGemmStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&sync->tfull[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit(&sync->done);
+      drain_wait(&sync->done, 0, p.wait_limit_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+      // every lane waits; the warp proceeds only if all saw the accumulator ready
+      if (!__all_sync(0xffffffffu, mbar_wait(&sync->tfull[acc], acc_phase, abort, p.wait_limit_ns, p.err)))
+        break;
+      tc_fence_after();
+      E::run(p, tile, tmem + (uint32_t(q * 32) << 16) + acc * kGemmBlockN, q, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sync->tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kGemmTmemCols);
+  }
+}
+
+template <class E>
+cudaError_t launch_tc_gemm(const typename E::Params& p, int num_sms, cudaStream_t s) {
+  static_assert(kGemmSmemBytes <= 232448, "shared memory budget");
+  cudaError_t e =
+      cudaFuncSetAttribute(tc_gemm_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemmSmemBytes));
+  if (e != cudaSuccess) return e;
+  int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
+  if (grid < 1) return cudaSuccess;
+  tc_gemm_kernel<E><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace lp

@@ -176,3 +176,53 @@ def upstream_grad(T: int, seed: int = 0) -> np.ndarray:
     """Per-row upstream gradient of the loss with respect to logp, g ~ N(0,1), float32 [T]."""
     rng = np.random.Generator(np.random.PCG64(seed + 7919))
     return rng.standard_normal(T, dtype=np.float32)
+
+
+# ------------------------------------------------------------------ on-device draws
+# Same distributions as above, drawn with a seeded torch generator directly on the
+# GPU. Used for the large timing inputs of the benchmark, where drawing gigabytes
+# on the host would dominate the run; parity tests use the numpy generators above.
+
+def device_forward_inputs(T: int, H: int, part: Partition, tau: float, device, seed: int = 0,
+                          w_std: float = 0.02, bias_std: Optional[float] = None):
+    """(X bf16 [T,H], [W_k bf16 [V_k,H]], bias list or None, y int32 [T]) on `device`."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    X = torch.randn((T, H), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    W = []
+    for s, e in part.ranges:
+        w = torch.empty((e - s, H), device=device, dtype=torch.bfloat16)
+        for r0 in range(0, e - s, 16384):
+            r1 = min(e - s, r0 + 16384)
+            w[r0:r1] = (torch.randn((r1 - r0, H), generator=g, device=device) * w_std).to(torch.bfloat16)
+        W.append(w)
+    bias = None
+    if bias_std is not None:
+        bias = [(torch.randn(e - s, generator=g, device=device) * bias_std).to(torch.bfloat16)
+                for s, e in part.ranges]
+    y = torch.randint(0, part.vocab_real, (T,), generator=g, device=device, dtype=torch.int64).to(torch.int32)
+    return X, W, bias, y
+
+
+def device_logits(T: int, part: Partition, device, seed: int = 0, std: float = 3.0,
+                  peak_frac: float = 0.01, peak_value: float = 8.0):
+    """Per-shard unscaled bf16 logits [T, V_k] on `device` (peaked rows as in logits_inputs)
+    and targets y int32 [T]."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    V = part.vocab_padded
+    full = torch.empty((T, V), device=device, dtype=torch.bfloat16)
+    for r0 in range(0, T, 1024):
+        r1 = min(T, r0 + 1024)
+        full[r0:r1] = (torch.randn((r1 - r0, V), generator=g, device=device) * std).to(torch.bfloat16)
+    n_peak = int(round(peak_frac * part.vocab_real))
+    if n_peak:
+        for r0 in range(0, T, 1024):
+            r1 = min(T, r0 + 1024)
+            keys = torch.rand((r1 - r0, part.vocab_real), generator=g, device=device)
+            cols = keys.topk(n_peak, dim=1).indices          # uniform without replacement
+            full[r0:r1].scatter_(1, cols, torch.full_like(cols, 0, dtype=torch.bfloat16) + peak_value)
+    y = torch.randint(0, part.vocab_real, (T,), generator=g, device=device, dtype=torch.int64).to(torch.int32)
+    return [full[:, s:e] for s, e in part.ranges], y

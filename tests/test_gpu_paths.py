@@ -1,0 +1,210 @@
+"""GPU parity of the logits-reuse, compact top-p replay (and its dense keep-mask route)
+and backward paths against the fp64 oracle, at sizes spanning several tiles with
+ragged tails, padded ids and empty shards."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from lp_util import (TOL_ENT, TOL_GRAD_REL, TOL_LOGP, TOL_LSE, dev_bf16, dev_f32, dev_i32, dev_inputs, max_abs,
+                     part_of, rel_fro)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lp():
+    from lm_head_linear_tcgen05_gb300 import _build
+    _build.build()
+    import lm_head_linear_tcgen05_gb300 as mod
+    import torch
+    assert mod.lp_device_supported()
+    torch.cuda.set_device(0)
+    return mod
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+# ----------------------------------------------------------------- logits reuse
+
+@pytest.mark.parametrize("T,bounds,real", [
+    (37, [0, 1000], 1000),
+    (64, [0, 4099, 4099, 9000, 12301], 12290),     # ragged widths, empty shard, padding
+    (5, [0, 7], 7),                                  # narrower than one vector
+])
+def test_logits_reuse_parity(lp, T, bounds, real):
+    part = synth.ranges_partition(real, bounds[-1], bounds)
+    L, y, tau = synth.logits_inputs(T, part, 0.7, seed=T)
+    import torch
+    # give every shard a padded row stride (multiple of 8) to exercise ld
+    Ld = []
+    for a in L:
+        w = a.shape[1]
+        if w == 0:
+            Ld.append(None)
+            continue
+        ld = (w + 7) // 8 * 8 + 8
+        buf = torch.zeros((T, ld), dtype=torch.bfloat16, device="cuda")
+        buf[:, :w] = dev_bf16(a)
+        Ld.append(buf[:, :w])
+    out = lp.lp_forward_from_logits(Ld, part_of(part), dev_i32(y), tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.forward_from_logits(L, part, y, tau)
+    assert max_abs(_np(out["logp"]), ref.logp) <= TOL_LOGP
+    assert max_abs(_np(out["lse"]), ref.lse) <= TOL_LSE
+    assert max_abs(_np(out["entropy"]), ref.entropy) <= TOL_ENT
+    ss = _np(out["shard_stats"])
+    for k, s in enumerate(ref.shards):
+        assert max_abs(ss[k, 0], s.lse) <= TOL_LSE
+        assert max_abs(ss[k, 1], s.t) <= TOL_LOGP
+        assert max_abs(ss[k, 2], s.mu) <= TOL_ENT
+
+
+def test_logits_reuse_bitwise_and_batch_invariant(lp):
+    import torch
+    part = synth.even_partition(20000, 2)
+    L, y, tau = synth.logits_inputs(96, part, 0.7, seed=3)
+    Ld = [dev_bf16(a) for a in L]
+    yd = dev_i32(y)
+    a = lp.lp_forward_from_logits(Ld, part_of(part), yd, tau)
+    b = lp.lp_forward_from_logits(Ld, part_of(part), yd, tau)
+    c = lp.lp_forward_from_logits([x[40:].contiguous() for x in Ld], part_of(part), yd[40:].contiguous(), tau)
+    for k in ("logp", "lse", "entropy"):
+        assert torch.equal(a[k], b[k])
+        assert torch.equal(a[k][40:], c[k])
+
+
+# ----------------------------------------------------------------------- replay
+
+def _mask_from_ids(ids, part):
+    masks = [np.zeros((ids.shape[0], e - s), np.uint8) for s, e in part.ranges]
+    for t in range(ids.shape[0]):
+        for v in ids[t]:
+            if v < 0:
+                continue
+            for k, (s, e) in enumerate(part.ranges):
+                if s <= v < e:
+                    masks[k][t, v - s] = 1
+    return masks
+
+
+@pytest.mark.parametrize("T,H,bounds,real,bias", [
+    (200, 256, [0, 2500, 5000, 7500, 10000], 10000, None),
+    (77, 136, [0, 3000, 3000, 8000, 8192], 8100, 0.2),     # empty shard, padding, H % 64 != 0
+])
+def test_replay_parity_and_dense_mask_bitwise(lp, T, H, bounds, real, bias):
+    import torch
+    part = synth.ranges_partition(real, bounds[-1], bounds)
+    inp = synth.forward_inputs(T, H, part, tau=0.7, seed=11, w_std=0.05, bias_std=bias)
+    ids, y = synth.replay_ids(T, part, seed=12)
+    X, W, b, _ = dev_inputs(inp)
+    P = part_of(part)
+    out = lp.lp_top_p_replay(X, W, b, P, dev_i32(ids), dev_i32(y), inp.tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.top_p_replay(inp.X, inp.W, inp.bias, part, ids, y, inp.tau)
+    assert max_abs(_np(out["logp"]), ref.logp) <= TOL_LOGP
+    assert max_abs(_np(out["lse"]), ref.lse) <= TOL_LSE
+    ss = _np(out["shard_stats"])
+    for k in range(part.n_shards):
+        assert max_abs(ss[k, 0], ref.shard_lse[k]) <= TOL_LSE
+        assert max_abs(ss[k, 1], ref.shard_t[k]) <= TOL_LOGP
+    # the dense keep-mask route gives the same bits
+    masks = [dev_i32(m).to(torch.uint8) if m.shape[1] else None for m in _mask_from_ids(ids, part)]
+    dm = lp.lp_top_p_replay_dense_mask(X, W, b, P, masks, dev_i32(y), inp.tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    for k in ("logp", "lse", "shard_stats"):
+        assert torch.equal(dm[k], out[k]), k
+    # slot order and duplicates do not change a bit
+    rng = np.random.default_rng(0)
+    ids2 = ids.copy()
+    for t in range(T):
+        live = ids2[t][ids2[t] >= 0]
+        extra = rng.choice(live, size=min(3, 64 - live.size))
+        row = np.concatenate([live, extra, np.full(64 - live.size - extra.size, -1)])
+        ids2[t] = rng.permutation(row)
+    o2 = lp.lp_top_p_replay(X, W, b, P, dev_i32(ids2), dev_i32(y), inp.tau, shard_stats=True)
+    for k in ("logp", "lse", "shard_stats"):
+        assert torch.equal(o2[k], out[k]), k
+    # batch invariance
+    o3 = lp.lp_top_p_replay(X[10:].contiguous(), W, b, P, dev_i32(ids[10:]), dev_i32(y[10:]), inp.tau)
+    assert torch.equal(o3["logp"], out["logp"][10:]) and torch.equal(o3["lse"], out["lse"][10:])
+
+
+def test_replay_whole_vocab_matches_dense_forward(lp):
+    part = synth.ranges_partition(60, 64, [0, 16, 32, 48, 64])
+    inp = synth.forward_inputs(9, 64, part, tau=0.7, seed=4, w_std=0.3, bias_std=0.2)
+    ids = np.full((9, 64), -1, np.int32)
+    for t in range(9):
+        ids[t, :60] = np.random.default_rng(t).permutation(60)
+    X, W, b, y = dev_inputs(inp)
+    rep = lp.lp_top_p_replay(X, W, b, part_of(part), dev_i32(ids), y, inp.tau)
+    fwd = lp.lp_forward(X, W, b, part_of(part), y, inp.tau)
+    assert max_abs(_np(rep["lse"]), _np(fwd["lse"])) <= TOL_LSE
+    assert max_abs(_np(rep["logp"]), _np(fwd["logp"])) <= TOL_LOGP
+
+
+def test_replay_errors_and_empty_rows(lp):
+    part = synth.even_partition(1000, 2)
+    inp = synth.forward_inputs(4, 64, part, tau=0.7, seed=9)
+    X, W, b, _ = dev_inputs(inp)
+    ids = np.full((4, 64), -1, np.int32)
+    ids[0, :3] = [5, 600, 5]
+    ids[1, 0] = 1000                     # out of range: device error, row fails closed
+    # row 2: no ids at all; row 3: target not in the set
+    ids[3, :2] = [7, 8]
+    y = np.array([600, 3, 4, 9], np.int32)
+    out = lp.lp_top_p_replay(X, W, b, part_of(part), dev_i32(ids), dev_i32(y), inp.tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 6
+    lg, ls = _np(out["logp"]), _np(out["lse"])
+    assert np.isfinite(lg[0]) and np.isfinite(ls[0])
+    assert np.isneginf(lg[1]) and np.isneginf(ls[1])
+    assert np.isneginf(lg[2]) and np.isneginf(ls[2])
+    assert np.isneginf(lg[3]) and np.isfinite(ls[3])
+    ss = _np(out["shard_stats"])
+    assert not np.any(np.isnan(ss))
+    assert np.isneginf(ss[1, 0, 3]) and ss[1, 1, 3] == 0.0      # row 3 has no id in shard 1
+
+
+# --------------------------------------------------------------------- backward
+
+@pytest.mark.parametrize("T,H,bounds,real,bias", [
+    (64, 256, [0, 1000], 1000, None),
+    (200, 192, [0, 700, 700, 1500, 2048], 2000, 0.3),    # empty shard, padding, ragged rows
+    (130, 520, [0, 300, 640], 600, 0.1),                 # H % 256 != 0, shard widths not multiples of 64
+])
+def test_backward_parity(lp, T, H, bounds, real, bias):
+    part = synth.ranges_partition(real, bounds[-1], bounds)
+    inp = synth.forward_inputs(T, H, part, tau=0.7, seed=T, w_std=0.05, bias_std=bias)
+    g = synth.upstream_grad(T, seed=T)
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    fwd = lp.lp_forward(X, W, b, P, y, inp.tau)
+    bw = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], dev_f32(g))
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g)
+    assert rel_fro(_np(bw["dX"]), ref.dX) <= TOL_GRAD_REL
+    for k, (s, e) in enumerate(part.ranges):
+        if e == s:
+            continue
+        assert rel_fro(_np(bw["dW"][k]), ref.dW[k]) <= TOL_GRAD_REL, k
+        assert rel_fro(_np(bw["db"][k]), ref.db[k]) <= TOL_GRAD_REL, k
+        # padded ids get exactly zero gradient
+        pad = slice(max(0, real - s), e - s)
+        assert np.all(_np(bw["dW"][k])[pad] == 0) and np.all(_np(bw["db"][k])[pad] == 0)
+
+
+def test_backward_bitwise_repeatable(lp):
+    import torch
+    part = synth.ranges_partition(3000, 3072, [0, 1500, 3072])
+    inp = synth.forward_inputs(300, 256, part, tau=0.7, seed=2, bias_std=0.1)
+    g = dev_f32(synth.upstream_grad(300, seed=2))
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    fwd = lp.lp_forward(X, W, b, P, y, inp.tau)
+    a = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], g)
+    c = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], g)
+    assert torch.equal(a["dX"], c["dX"])
+    for k in range(2):
+        assert torch.equal(a["dW"][k], c["dW"][k]) and torch.equal(a["db"][k], c["db"][k])
