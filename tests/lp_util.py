@@ -35,7 +35,7 @@ def max_abs(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
-    d = np.where(both_inf, 0.0, np.abs(a - b))
+    d = np.abs(np.where(both_inf, 0.0, a) - np.where(both_inf, 0.0, b))
     return float(np.max(d)) if d.size else 0.0
 
 

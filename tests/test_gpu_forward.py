@@ -88,8 +88,9 @@ def test_one_dominant_logit(lp):
     T, H, tau = 8, 64, 1.0
     inp = synth.forward_inputs(T, H, part, tau=tau, seed=2)
     inp.W = [np.zeros_like(w) for w in inp.W]
+    inp.y[:] = 3001                       # the bias is shared by all rows: one hot id
     hot = np.zeros(4096, np.float32)
-    hot[inp.y] = 100.0
+    hot[3001] = 100.0
     inp.bias = [synth.bf16_bits(hot[:2048]), synth.bf16_bits(hot[2048:])]
     out = _run(lp, inp)
     assert np.all(np.abs(_np(out["logp"])) <= 1e-5)
