@@ -50,6 +50,7 @@ extern "C" {
 
 #define LP_MAX_SHARDS 8     /* shards per call */
 #define LP_REPLAY_SLOTS 64  /* replay id slots per row */
+#define LP_NOALLOC_SCRATCH_BYTES (32u << 20) /* scratch of lp_forward_noalloc, per device */
 
 #if defined(__GNUC__)
 #define LP_API __attribute__((visibility("default")))
@@ -179,6 +180,31 @@ LP_API lp_status lp_backward(const void* X, int64_t T, int64_t H,
                       const float* lse, const float* grad_logp,
                       float* dX, float* const* dW, float* const* db,
                       void* workspace, size_t ws_bytes, lp_stream_t stream);
+
+/* Fused forward that allocates nothing. The paper has no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory at all - a plugin
+ * inside an engine whose memory manager owns every device byte, a runtime with a
+ * memory budget fixed at start-up, a host language without a CUDA allocator - and so
+ * cannot pass lp_forward a workspace.
+ *
+ * Same arguments, outputs and results as lp_forward, minus the workspace: the
+ * scratch is one device array of LP_NOALLOC_SCRATCH_BYTES inside this library,
+ * which every GPU that loads the library keeps until the process exits. Inputs and
+ * outputs are still the caller's device memory. The call allocates nothing (no
+ * cudaMalloc, no allocating library routine) and frees nothing.
+ *  - Limit: lp_workspace_size(LP_OP_FORWARD, T, H, part) must not exceed
+ *    LP_NOALLOC_SCRATCH_BYTES (32 MiB: e.g. T <= 4705 rows at V = 151936 in one
+ *    shard); larger problems return LP_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *  - The first call on each device looks up that device's address of the array
+ *    (with the device current); make that first call before any stream capture.
+ *  - Every call shares the one array and it keeps the previous call's contents.
+ *    Nothing in it needs to start at zero (each call writes every slot it reads),
+ *    but calls whose kernels overlap on the GPU - on different streams, or from
+ *    different threads - race on it and give wrong results. */
+LP_API lp_status lp_forward_noalloc(const void* X, int64_t T, int64_t H,
+                                    const void* const* W, const void* const* bias,
+                                    const lp_vocab_partition* part, const int32_t* y, float tau,
+                                    const lp_outputs* out, lp_stream_t stream);
 
 /* Synchronises `stream`, returns the first device-side error recorded on the
  * current device since the last call (LP_OK if none) and clears it. */

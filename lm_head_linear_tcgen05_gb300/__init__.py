@@ -23,6 +23,7 @@ from ._build import LIB as LIB_PATH
 
 LP_MAX_SHARDS = 8
 LP_REPLAY_SLOTS = 64
+LP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 LP_OK = 0
 STATUS_NAMES = {
@@ -45,7 +46,7 @@ LP_OP_BACKWARD = 3
 LP_OP_TOP_P_REPLAY_DENSE_MASK = 4
 
 # every symbol include/lp.h declares
-EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_from_logits", "lp_top_p_replay",
+EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
             "lp_top_p_replay_dense_mask", "lp_backward", "lp_get_device_error",
             "lp_device_supported", "lp_status_string")
 
@@ -102,6 +103,7 @@ def lib() -> ctypes.CDLL:
     L.lp_workspace_size.argtypes = [ctypes.c_int, i64, i64, P(_Partition)]
     L.lp_workspace_size.restype = sz
     L.lp_forward.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, P(_Outputs), vp, sz, vp]
+    L.lp_forward_noalloc.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, P(_Outputs), vp]
     L.lp_forward_from_logits.argtypes = [P(vp), P(i64), i64, P(_Partition), vp, f32, P(_Outputs), vp, sz, vp]
     L.lp_top_p_replay.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, vp, f32, P(_Outputs), vp, sz, vp]
     L.lp_top_p_replay_dense_mask.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), P(vp), vp, f32,
@@ -112,7 +114,7 @@ def lib() -> ctypes.CDLL:
     L.lp_device_supported.argtypes = []
     L.lp_status_string.argtypes = [ctypes.c_int]
     L.lp_status_string.restype = ctypes.c_char_p
-    for name in ("lp_forward", "lp_forward_from_logits", "lp_top_p_replay", "lp_top_p_replay_dense_mask",
+    for name in ("lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay", "lp_top_p_replay_dense_mask",
                  "lp_backward", "lp_get_device_error", "lp_device_supported"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -230,6 +232,27 @@ def lp_forward(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optional[Sequen
                               ctypes.byref(cp), y.data_ptr(), float(tau), ctypes.byref(co), _ptr(ws), wsb,
                               _stream(X.device))
     _raise(st, "lp_forward")
+    return o
+
+
+def lp_forward_noalloc(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optional[Sequence[torch.Tensor]], part,
+                       y: torch.Tensor, tau: float, entropy: bool = True, shard_stats: bool = False) -> dict:
+    """lp_forward without a workspace: the library uses its own fixed device scratch
+    (LP_NOALLOC_SCRATCH_BYTES per GPU), for callers that cannot allocate device memory.
+    Only the outputs are allocated here, as the caller's buffers."""
+    _check(X, "X", torch.bfloat16, 2)
+    _check(y, "y", torch.int32, 1)
+    n = len(part.ranges)
+    W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
+    bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
+    T, H = X.shape
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(X.device):
+        o, co = _outputs(T, n, X.device, entropy, shard_stats)
+        st = lib().lp_forward_noalloc(X.data_ptr(), T, H, _ptr_array(W),
+                                      _ptr_array(bias) if bias is not None else None, ctypes.byref(cp),
+                                      y.data_ptr(), float(tau), ctypes.byref(co), _stream(X.device))
+    _raise(st, "lp_forward_noalloc")
     return o
 
 
