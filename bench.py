@@ -135,6 +135,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def reduce_max_ms(ms: float, dist, device) -> float:
+    """Slowest rank's time: the only collective of the multi-GPU run (no data exchange)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(rows_per_rank: int, world: int, ms_max: float) -> float:
+    """Rows processed by all ranks per second of the slowest rank (weak scaling)."""
+    return world * rows_per_rank / (ms_max * 1e-3)
+
+
 def time_steps(fn, steps, warmup, stream):
     """Average ms per step over `steps` calls of fn(), CUDA events on `stream`."""
     import torch
@@ -171,6 +186,7 @@ def run_ours(args, rank, world, dist):
     peaks, peak_src = load_peaks()
 
     # ---- headline: fused forward, T=4096, H=4096, V=151936, tau=0.7, no bias
+    T_FWD, V = args.rows, args.vocab
     part = synth.even_partition(V, 1)
     P = lp.VocabPartition(part.vocab_real, part.vocab_padded, part.ranges)
     X, W, _, y = synth.device_forward_inputs(T_FWD, H, part, TAU, dev, seed=0)
@@ -182,13 +198,10 @@ def run_ours(args, rank, world, dist):
         ms = time_steps(step, args.steps, args.warmup, stream)
     if lp.lp_get_device_error() != 0:
         raise RuntimeError("device error during the timed forward")
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max_ms(ms, dist, dev)
     flops = 2.0 * T_FWD * H * V
     tflops = flops / (ms * 1e-3) / 1e12
-    value = world * T_FWD / (ms * 1e-3)
+    value = whole_job_rate(T_FWD, world, ms)
 
     # ---- end to end through the public API: pinned host X, y in; logp, lse, entropy out
     hX = torch.empty((T_FWD, H), dtype=torch.bfloat16, pin_memory=True)
@@ -207,10 +220,7 @@ def run_ours(args, rank, world, dist):
         h_out[2].copy_(o["entropy"], non_blocking=True)
 
     ms_e2e = time_steps(e2e_step, args.steps, args.warmup, stream)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = reduce_max_ms(ms_e2e, dist, dev)
     del hX
     paths = {}
     if not args.headline_only:
@@ -223,13 +233,13 @@ def run_ours(args, rank, world, dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "Qwen3-8B-shaped LM-head fused forward, T=4096 rows, H=4096, V=151936, "
+        "config": {"workload": f"Qwen3-8B-shaped LM-head fused forward, T={T_FWD} rows, H={H}, V={V}, "
                                "tau=0.7, no bias, logp+LSE+entropy",
                    "T": T_FWD, "H": H, "V": V, "tau": TAU, "shards": 1,
                    "l2": "inputs larger than L2 (W 1.245 GB > 129 MB); no flush",
                    "parallelism": f"replicas x{world}"},
         "clocks": clk.summary(),
-        "e2e": {"value": world * T_FWD / (ms_e2e * 1e-3), "unit": UNIT,
+        "e2e": {"value": whole_job_rate(T_FWD, world, ms_e2e), "unit": UNIT,
                 "h2d_bytes_per_step": T_FWD * H * 2 + T_FWD * 4, "d2h_bytes_per_step": 3 * T_FWD * 4,
                 "ms_per_step": ms_e2e},
         "gpu_launches": 2 * args.steps,
@@ -370,6 +380,8 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="time only the fused forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per reference step")
+    ap.add_argument("--rows", type=int, default=T_FWD, help="headline rows T (profiling of smaller cases)")
+    ap.add_argument("--vocab", type=int, default=V, help="headline vocabulary V (profiling of smaller cases)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -210,6 +210,13 @@ LP_API lp_status lp_forward_noalloc(const void* X, int64_t T, int64_t H,
  * current device since the last call (LP_OK if none) and clears it. */
 LP_API lp_status lp_get_device_error(lp_stream_t stream);
 
+/* Self-test of the bounded pipeline waits every kernel uses (failure detection): one
+ * CTA waits on an mbarrier that nothing ever arrives on, with a limit of `limit_ns`
+ * nanoseconds (1 us .. 2 s); the wait gives up, records LP_ERR_DEVICE_TIMEOUT in the
+ * device error word and the kernel exits cleanly, leaving the context usable. Read the
+ * result with lp_get_device_error(). Nothing hangs and nothing faults. */
+LP_API lp_status lp_selftest_wait_timeout(uint64_t limit_ns, lp_stream_t stream);
+
 /* 1 if the current device can run this library (sm_100 family, e.g. GB300), else 0. */
 LP_API int lp_device_supported(void);
 

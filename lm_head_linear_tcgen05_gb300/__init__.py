@@ -48,7 +48,7 @@ LP_OP_TOP_P_REPLAY_DENSE_MASK = 4
 # every symbol include/lp.h declares
 EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
             "lp_top_p_replay_dense_mask", "lp_backward", "lp_get_device_error",
-            "lp_device_supported", "lp_status_string")
+            "lp_selftest_wait_timeout", "lp_device_supported", "lp_status_string")
 
 
 class LPError(RuntimeError):
@@ -111,11 +111,12 @@ def lib() -> ctypes.CDLL:
     L.lp_backward.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, vp, vp, vp, P(vp), P(vp),
                               vp, sz, vp]
     L.lp_get_device_error.argtypes = [vp]
+    L.lp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     L.lp_device_supported.argtypes = []
     L.lp_status_string.argtypes = [ctypes.c_int]
     L.lp_status_string.restype = ctypes.c_char_p
     for name in ("lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay", "lp_top_p_replay_dense_mask",
-                 "lp_backward", "lp_get_device_error", "lp_device_supported"):
+                 "lp_backward", "lp_get_device_error", "lp_selftest_wait_timeout", "lp_device_supported"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -177,6 +178,12 @@ def lp_get_device_error(stream: Optional[int] = None) -> int:
     """Synchronise the stream and return (and clear) the sticky device error code."""
     s = _stream(torch.cuda.current_device()) if stream is None else stream
     return int(lib().lp_get_device_error(s))
+
+
+def lp_selftest_wait_timeout(limit_ns: int, stream: Optional[int] = None) -> None:
+    """Launch the bounded-wait self-test; lp_get_device_error() then reports 7."""
+    s = _stream(torch.cuda.current_device()) if stream is None else stream
+    _raise(lib().lp_selftest_wait_timeout(int(limit_ns), s), "lp_selftest_wait_timeout")
 
 
 def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "lp_device.cuh"
 #include "lp_internal.h"
 
 namespace lp {
@@ -18,6 +19,21 @@ namespace lp {
 __device__ unsigned int g_error_word;
 
 __global__ void probe_kernel() {}
+
+// One warp waits on an mbarrier that nothing arrives on; the bounded wait must give
+// up after limit_ns, record LP_ERR_DEVICE_TIMEOUT and return.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, unsigned int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort, limit_ns, err);
+  __syncthreads();
+}
 
 namespace {
 
@@ -202,8 +218,8 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
   if (!encode_bf16_2d(&p.maps[0], X, uint64_t(H), uint64_t(T), uint64_t(H), kFwdBlockM)) return LP_ERR_CUDA;
   int nb = 0;
   for (int k = 0; k < sh.n; ++k) {
-    if (sh.real[k] > 0 &&
-        !encode_bf16_2d(&p.maps[1 + k], W[k], uint64_t(H), uint64_t(sh.width[k]), uint64_t(H), kFwdBlockN))
+    if (sh.real[k] > 0 && !encode_bf16_2d(&p.maps[1 + k], W[k], uint64_t(H), uint64_t(sh.width[k]), uint64_t(H),
+                                          kFwdBlockN / kFwdClusterM))
       return LP_ERR_CUDA;
     p.bias[k] = bias != nullptr ? static_cast<const __nv_bfloat16*>(bias[k]) : nullptr;
     p.shard_start[k] = sh.start[k];
@@ -215,7 +231,8 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
   p.keep_maps = 1u;  // X is re-read by every vocabulary block: keep it in L2
   p.n_shards = sh.n;
   p.T = int32_t(T);
-  p.num_m_blocks = int32_t((T + kFwdBlockM - 1) / kFwdBlockM);
+  const int64_t mblocks = (T + kFwdBlockM - 1) / kFwdBlockM;  // row blocks, counted in whole clusters
+  p.num_m_blocks = int32_t((mblocks + kFwdClusterM - 1) / kFwdClusterM * kFwdClusterM);
   p.num_k_blocks = int32_t((H + kFwdBlockK - 1) / kFwdBlockK);
   p.total_tiles = nb * p.num_m_blocks;
   p.err = dev->err;
@@ -430,6 +447,15 @@ lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W,
   a.err = dev->err;
   a.num_sms = dev->num_sms;
   return run_backward(a, sh, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_selftest_wait_timeout(uint64_t limit_ns, lp_stream_t stream) {
+  if (limit_ns < 1000ull || limit_ns > 2000000000ull) return LP_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+  wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, dev->err);
+  return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
 lp_status lp_get_device_error(lp_stream_t stream) {

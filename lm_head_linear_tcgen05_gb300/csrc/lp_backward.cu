@@ -167,6 +167,7 @@ struct GradParams {
 
 struct GradEpi {
   using Params = GradParams;
+  static constexpr int kClusterM = kFwdClusterM;
 
   struct Coord {
     int shard, nb_local, mb;
@@ -294,6 +295,7 @@ struct StoreParams {
 
 struct StoreEpi {
   using Params = StoreParams;
+  static constexpr int kClusterM = 1;
 
   struct Coord {
     int shard, mb, nb, s;
@@ -401,8 +403,8 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     if (!encode_bf16_2d(&p.maps[0], a.X, uint64_t(H), uint64_t(T), uint64_t(H), kFwdBlockM)) return LP_ERR_CUDA;
     int nb = 0;
     for (int k = 0; k < sh.n; ++k) {
-      if (sh.real[k] > 0 &&
-          !encode_bf16_2d(&p.maps[1 + k], a.W[k], uint64_t(H), uint64_t(sh.width[k]), uint64_t(H), kFwdBlockN))
+      if (sh.real[k] > 0 && !encode_bf16_2d(&p.maps[1 + k], a.W[k], uint64_t(H), uint64_t(sh.width[k]),
+                                            uint64_t(H), kFwdBlockN / kFwdClusterM))
         return LP_ERR_CUDA;
       p.bias[k] = static_cast<const __nv_bfloat16*>(a.bias[k]);
       p.coff[k] = L.coff[k];
@@ -416,7 +418,8 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.keep_maps = 1u;
     p.n_shards = sh.n;
     p.T = int32_t(T);
-    p.num_m_blocks = int32_t((T + kFwdBlockM - 1) / kFwdBlockM);
+    const int64_t mblocks = (T + kFwdBlockM - 1) / kFwdBlockM;
+    p.num_m_blocks = int32_t((mblocks + kFwdClusterM - 1) / kFwdClusterM * kFwdClusterM);
     p.num_k_blocks = int32_t((H + kFwdBlockK - 1) / kFwdBlockK);
     p.total_tiles = nb * p.num_m_blocks;
     p.err = a.err;

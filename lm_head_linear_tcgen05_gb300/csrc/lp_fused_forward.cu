@@ -103,6 +103,7 @@ __device__ __forceinline__ TileCoord fwd_coord(const FwdParams& p, int tile) {
 
 struct LogpEpi {
   using Params = FwdParams;
+  static constexpr int kClusterM = kFwdClusterM;
 
   static __device__ __forceinline__ TileJob job(const Params& p, int tile) {
     const TileCoord c = fwd_coord(p, tile);

@@ -15,6 +15,10 @@ namespace lp {
 constexpr int kFwdBlockM = 128;
 constexpr int kFwdBlockN = 256;
 constexpr int kFwdBlockK = 64;
+// CTAs per cluster along M in the projection GEMMs (forward and the backward's G):
+// the two row blocks of one vocabulary block share its W box through TMA multicast,
+// so row blocks are counted in pairs and W maps have boxes of kFwdBlockN / 2 rows.
+constexpr int kFwdClusterM = 2;
 
 // Validated vocabulary partition (host side).
 struct Shards {

@@ -7,11 +7,14 @@
 // temperature scaling happens exactly once for reused logits - the logits given
 // here are unscaled and 1/tau is applied in this kernel only.
 //
-// One CTA (512 threads) per row. Each thread streams 16-byte vectors (8 bf16) of
-// the row with four loads in flight, keeping an online base-2 statistic; the
-// threads are combined by a fixed shuffle tree per warp and then warp by warp in
-// ascending order, shard after shard in ascending order. The work split depends
-// only on the shard width, so a row's result never depends on T.
+// One CTA (256 threads) per row, four CTAs per SM. Thread 0 streams the row through
+// a 3-stage ring of 16 KB shared-memory chunks with 1-D bulk copies (cp.async.bulk,
+// completion on mbarriers, L2 evict-first), so up to 192 KB per SM are in flight
+// without holding registers. Each thread folds the 16-byte vectors j = tid, tid+256,
+// ... of every chunk into an online base-2 statistic; the threads are combined by a
+// fixed shuffle tree per warp and then warp by warp in ascending order, shard after
+// shard in ascending order. The work split depends only on the shard width, so a
+// row's result never depends on T.
 #include <cuda_bf16.h>
 
 #include "lp_device.cuh"
@@ -20,17 +23,10 @@ namespace lp {
 
 namespace {
 
-constexpr int kStreamThreads = 512;
+constexpr int kStreamThreads = 256;
 constexpr int kStreamWarps = kStreamThreads / 32;
-constexpr int kUnroll = 4;
-
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+constexpr int kChunkVecs = 1024;  // 16 KB of logits per stage
+constexpr int kStages = 3;        // 48 KB of copies in flight per row, four rows per SM
 
 // Per-thread online statistic over raw (unscaled) logits x: the running maximum is
 // tracked on x, m = max(x) * c2 and d = x * c2 - m, so u = x * c2 is never rounded
@@ -84,8 +80,11 @@ __device__ __forceinline__ void raw_push1(RawStat& st, float x, float c2) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kStreamThreads) stream_logits_kernel(const __grid_constant__ StreamParams p) {
+__global__ void __launch_bounds__(kStreamThreads, 4) stream_logits_kernel(const __grid_constant__ StreamParams p) {
+  extern __shared__ uint4 sbuf[];  // kStages x kChunkVecs vectors of 8 bf16
+  __shared__ uint64_t full[kStages];
   __shared__ Stat red[kStreamWarps];
+  __shared__ int abort_flag;
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -94,30 +93,61 @@ __global__ void __launch_bounds__(kStreamThreads) stream_logits_kernel(const __g
   const int yv = __ldg(p.y + row);
   const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
   const size_t T = size_t(p.T);
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const uint64_t pol = l2_policy_evict_first();
 
   Stat tot = stat_empty();  // meaningful in thread 0 only
   float t_val = 0.f;
+  uint32_t g0 = 0;          // chunks of this row consumed so far (all shards): fixes stage and parity
+  bool ok = true;
 
-  for (int k = 0; k < p.n_shards; ++k) {
+  for (int k = 0; k < p.n_shards && ok; ++k) {
     const int64_t width = p.shard_width[k];
+    const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
+    const uint4* src = reinterpret_cast<const uint4*>(L);
+    const int64_t nvec = width > 0 ? (width >> 3) : 0;
+    const int nchunks = int((nvec + kChunkVecs - 1) / kChunkVecs);
     RawStat st{-INFINITY, -INFINITY, 0.f, 0.f};
-    if (width > 0) {
-      const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
-      const uint4* Lv = reinterpret_cast<const uint4*>(L);
-      const int64_t nvec = width >> 3;
-      int64_t v = tid;
-      for (; v + (kUnroll - 1) * kStreamThreads < nvec; v += kUnroll * kStreamThreads) {
-        uint4 q[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) q[u] = ld_stream(Lv + v + u * kStreamThreads);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) raw_push8(st, q[u], c2);
+    // thread 0 streams the row through the stage ring; the other threads consume
+    auto issue = [&](int c) {
+      const int64_t v0 = int64_t(c) * kChunkVecs;
+      const int64_t nv = nvec - v0 < kChunkVecs ? nvec - v0 : kChunkVecs;
+      const uint32_t s = (g0 + c) % kStages;
+      mbar_arrive_expect_tx(&full[s], uint32_t(nv) * 16u);
+      bulk_load(sbuf + size_t(s) * kChunkVecs, src + v0, uint32_t(nv) * 16u, &full[s], pol);
+    };
+    if (tid == 0)
+      for (int c = 0; c < nchunks && c < kStages; ++c) issue(c);
+    for (int c = 0; c < nchunks; ++c) {
+      const uint32_t g = g0 + c;
+      const uint32_t s = g % kStages;
+      const bool got = mbar_wait(&full[s], (g / kStages) & 1u, &abort_flag, kDefaultWaitLimitNs, p.err);
+      if (!__syncthreads_and(got)) {
+        ok = false;
+        if (tid == 0)  // let the copies already issued land before the CTA exits
+          for (int d = c; d < nchunks && d < c + kStages; ++d)
+            drain_wait(&full[(g0 + d) % kStages], ((g0 + d) / kStages) & 1u, kDefaultWaitLimitNs);
+        break;
       }
-      for (; v < nvec; v += kStreamThreads) raw_push8(st, ld_stream(Lv + v), c2);
-      // ragged tail (width % 8 elements) by the first threads, in ascending order
-      const int64_t tail0 = nvec << 3;
-      if (tail0 + tid < width) raw_push1(st, __bfloat162float(L[tail0 + tid]), c2);
+      const int64_t v0 = int64_t(c) * kChunkVecs;
+      const int nv = int(nvec - v0 < kChunkVecs ? nvec - v0 : kChunkVecs);
+      const uint4* chunk = sbuf + size_t(s) * kChunkVecs;
+#pragma unroll 4
+      for (int j = tid; j < nv; j += kStreamThreads) raw_push8(st, chunk[j], c2);
+      __syncthreads();  // stage s fully read
+      if (tid == 0 && c + kStages < nchunks) issue(c + kStages);
     }
+    g0 += uint32_t(nchunks);
+    if (!ok) break;
+    // ragged tail (width % 8 elements) by the first threads, in ascending order
+    const int64_t tail0 = nvec << 3;
+    if (width > 0 && tail0 + tid < width) raw_push1(st, __bfloat162float(L[tail0 + tid]), c2);
+
     Stat loc{st.m, st.s, st.a};
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
@@ -133,7 +163,6 @@ __global__ void __launch_bounds__(kStreamThreads) stream_logits_kernel(const __g
       const bool own = y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k];
       float tk = 0.f;
       if (own) {
-        const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
         tk = __fmul_rn(__bfloat162float(L[yv - p.shard_start[k]]), p.inv_tau);
         t_val = tk;
       }
@@ -149,6 +178,12 @@ __global__ void __launch_bounds__(kStreamThreads) stream_logits_kernel(const __g
   }
   if (tid == 0) {
     const float lse = stat_lse(tot);
+    if (!ok) {
+      p.lse[row] = -INFINITY;
+      p.logp[row] = -INFINITY;
+      if (p.entropy != nullptr) p.entropy[row] = 0.f;
+      return;
+    }
     p.lse[row] = lse;
     if (p.entropy != nullptr) p.entropy[row] = stat_entropy(tot);
     if (!y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
@@ -157,7 +192,10 @@ __global__ void __launch_bounds__(kStreamThreads) stream_logits_kernel(const __g
 }
 
 cudaError_t launch_stream_logits(const StreamParams& p, cudaStream_t s) {
-  stream_logits_kernel<<<p.T, kStreamThreads, 0, s>>>(p);
+  const int smem = kStages * kChunkVecs * int(sizeof(uint4));
+  cudaError_t e = cudaFuncSetAttribute(stream_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  stream_logits_kernel<<<p.T, kStreamThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -5,8 +5,8 @@
 // caller that reads the accumulator straight out of TMEM. The kernel is persistent
 // (one CTA per SM, tiles handed out round-robin) and warp specialised:
 //
-//   warp 0      TMA producer: A and B boxes of 64 (K) x 128 / 256 rows, 128-byte
-//               swizzle, into a kStages-deep shared-memory ring (mbarrier full/empty);
+//   warp 0      TMA producer: A and B boxes (64 K-elements wide, 128-byte swizzle)
+//               into a kGemmStages-deep shared-memory ring (mbarrier full/empty);
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
 //               issues tcgen05.mma kind::f16 (M=128, N=256, K=16) from one thread,
 //               committing each stage back to the producer and each finished tile
@@ -15,21 +15,30 @@
 //               owns one row of the tile; the callback runs while the MMA warp
 //               fills the other accumulator.
 //
+// With kClusterM = 2 the CTAs run in clusters of two that take the two row blocks of
+// the same column block (tiles 2j and 2j+1): each CTA fetches half of the shared B
+// box (128 of its 256 rows) and multicasts it into both CTAs' shared memory, so every
+// SM pulls 32 KB instead of 48 KB per K step through L2. A stage may then be refilled
+// only when both CTAs' MMAs are done with it: each MMA commit arrives on the empty
+// barrier of both CTAs (count 2).
+//
 // Every mbarrier wait is bounded in time (see lp_device.cuh): a wait that runs past
 // the limit records LP_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag and every
 // role leaves its loop; the producer then waits (bounded) for its copies in flight,
 // the MMA warp for its MMAs, and TMEM is freed before the CTA exits.
 //
 // An epilogue type E provides
+//   static constexpr int kClusterM;       1, or 2 for the multicast pairing above
 //   struct E::Params           with members `CUtensorMap maps[kGemmMaps]`,
 //                              `uint32_t keep_maps` (bit i: map i is small and
 //                              reused, loaded with an L2 evict-last hint),
-//                              `int total_tiles`, `unsigned int* err`,
-//                              `uint64_t wait_limit_ns`;
+//                              `int total_tiles` (a multiple of kClusterM),
+//                              `unsigned int* err`, `uint64_t wait_limit_ns`;
 //   static TileJob E::job(const Params&, int tile);
 //   static void E::run(const Params&, int tile, uint32_t tmem_row_base, int quarter, int lane);
 // `tmem_row_base` addresses column 0 of the tile's accumulator at this warp's first
-// lane; column c of this thread's row is at tmem_row_base + c.
+// lane; column c of this thread's row is at tmem_row_base + c. With kClusterM = 2 the
+// B maps must have boxes of 128 rows (each CTA loads half of the 256-row tile).
 #pragma once
 
 #include "lp_device.cuh"
@@ -49,7 +58,7 @@ constexpr uint32_t kGemmStageB = kGemmBlockN * kGemmBlockK * 2;  // 32 KB
 constexpr uint32_t kGemmStageBytes = kGemmStageA + kGemmStageB;
 
 // What one tile reads: box rows a_y.. of map a_map and b_y.. of map b_map, for k
-// blocks kb0 .. kb0 + nkb - 1 (coordinates in elements; x = k * 64).
+// blocks kb0 .. kb0 + nkb - 1 (coordinates in elements; x = k * 64); nkb >= 1.
 struct TileJob {
   int a_map, b_map;
   int a_y, b_y;
@@ -68,15 +77,10 @@ struct GemmSync {
 
 constexpr size_t kGemmSmemBytes = 1024 + size_t(kGemmStages) * kGemmStageBytes + sizeof(GemmSync);
 
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_test(bar, parity)) {
-    if (global_timer_ns() - t0 > limit_ns) break;
-  }
-}
-
 template <class E>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ typename E::Params p) {
+  constexpr int kCM = E::kClusterM;
+  static_assert(kCM == 1 || kCM == 2, "cluster of one or two CTAs along M");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -85,11 +89,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kCM == 2 ? cluster_ctarank() : 0u;
+  const int cluster_id = int(blockIdx.x) / kCM;
+  const int num_clusters = int(gridDim.x) / kCM;
+  const int cluster_tiles = p.total_tiles / kCM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
       mbar_init(&sync->full[s], 1);
-      mbar_init(&sync->empty[s], 1);
+      mbar_init(&sync->empty[s], kCM);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sync->tfull[b], 1);
@@ -104,7 +112,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kCM == 2)
+    cluster_sync();  // the peer's barriers are initialised before anything targets them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sync->tmem_base;
   volatile int* abort = &sync->abort;
@@ -117,8 +128,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, armed_phase = 0;  // stages with a copy issued, and its phase
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-        const TileJob j = E::job(p, tile);
+      for (int ct = cluster_id; ok && ct < cluster_tiles; ct += num_clusters) {
+        const TileJob j = E::job(p, ct * kCM + int(rank));
+        const uint64_t pa = ((p.keep_maps >> j.a_map) & 1u) ? pol_keep : pol_norm;
+        const uint64_t pb = ((p.keep_maps >> j.b_map) & 1u) ? pol_keep : pol_norm;
         for (int kb = 0; kb < j.nkb; ++kb) {
           if (!mbar_wait(&sync->empty[stage], phase ^ 1u, abort, p.wait_limit_ns, p.err)) {
             ok = false;
@@ -126,10 +139,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           }
           const int x = (j.kb0 + kb) * kGemmBlockK;
           mbar_arrive_expect_tx(&sync->full[stage], kGemmStageBytes);
-          tma_load_2d(sA + stage * kGemmStageA, &p.maps[j.a_map], &sync->full[stage], x, j.a_y,
-                      ((p.keep_maps >> j.a_map) & 1u) ? pol_keep : pol_norm);
-          tma_load_2d(sB + stage * kGemmStageB, &p.maps[j.b_map], &sync->full[stage], x, j.b_y,
-                      ((p.keep_maps >> j.b_map) & 1u) ? pol_keep : pol_norm);
+          tma_load_2d(sA + stage * kGemmStageA, &p.maps[j.a_map], &sync->full[stage], x, j.a_y, pa);
+          if constexpr (kCM == 2) {
+            constexpr uint32_t half = kGemmStageB / 2;
+            tma_load_2d_multicast(sB + stage * kGemmStageB + rank * half, &p.maps[j.b_map], &sync->full[stage], x,
+                                  j.b_y + int(rank) * (kGemmBlockN / 2), uint16_t(0x3), pb);
+          } else {
+            tma_load_2d(sB + stage * kGemmStageB, &p.maps[j.b_map], &sync->full[stage], x, j.b_y, pb);
+          }
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kGemmStages) {
@@ -149,8 +166,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       constexpr uint32_t idesc = idesc_bf16_f32(kGemmBlockM, kGemmBlockN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-        const TileJob j = E::job(p, tile);
+      for (int ct = cluster_id; ok && ct < cluster_tiles; ct += num_clusters) {
+        const TileJob j = E::job(p, ct * kCM + int(rank));
         if (!mbar_wait(&sync->tempty[acc], acc_phase ^ 1u, abort, p.wait_limit_ns, p.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * kGemmBlockN;
@@ -165,7 +182,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 #pragma unroll
           for (int k = 0; k < kGemmBlockK / 16; ++k)
             umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          umma_commit(&sync->empty[stage]);
+          if constexpr (kCM == 2)
+            umma_commit_multicast(&sync->empty[stage], uint16_t(0x3));
+          else
+            umma_commit(&sync->empty[stage]);
           if (++stage == kGemmStages) {
             stage = 0;
             phase ^= 1u;
@@ -183,12 +203,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    for (int ct = cluster_id; ct < cluster_tiles; ct += num_clusters) {
       // every lane waits; the warp proceeds only if all saw the accumulator ready
       if (!__all_sync(0xffffffffu, mbar_wait(&sync->tfull[acc], acc_phase, abort, p.wait_limit_ns, p.err)))
         break;
       tc_fence_after();
-      E::run(p, tile, tmem + (uint32_t(q * 32) << 16) + acc * kGemmBlockN, q, lane);
+      E::run(p, ct * kCM + int(rank), tmem + (uint32_t(q * 32) << 16) + acc * kGemmBlockN, q, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sync->tempty[acc]);
@@ -198,23 +218,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kCM == 2)
+    cluster_sync();  // neither CTA leaves while its peer may still signal or write into it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kGemmTmemCols);
   }
 }
 
+// Launches one CTA per SM (rounded to whole clusters) over p.total_tiles tiles.
 template <class E>
 cudaError_t launch_tc_gemm(const typename E::Params& p, int num_sms, cudaStream_t s) {
   static_assert(kGemmSmemBytes <= 232448, "shared memory budget");
+  constexpr int kCM = E::kClusterM;
   cudaError_t e =
       cudaFuncSetAttribute(tc_gemm_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemmSmemBytes));
   if (e != cudaSuccess) return e;
-  int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
-  if (grid < 1) return cudaSuccess;
-  tc_gemm_kernel<E><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  if (p.total_tiles < kCM) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.stream = s;
+  int clusters = num_sms / kCM;
+  if (kCM > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(kCM * clusters, 1, 1);
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, tc_gemm_kernel<E>, &cfg) == cudaSuccess && active > 0 &&
+        active < clusters)
+      clusters = active;
+    cudaGetLastError();
+  }
+  const int cluster_tiles = p.total_tiles / kCM;
+  if (clusters > cluster_tiles) clusters = cluster_tiles;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(kCM * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<E>, p);
 }
 
 }  // namespace lp

@@ -346,21 +346,25 @@ def backward_sampled(X_bits, W_bits, b_bits, part, y, tau, g, dx_rows, dw_rows):
     g = np.asarray(g, dtype=np.float64)
     T = X_bits.shape[0]
     Xd = bf16_to_f64(X_bits)
-    # LSE of every row, streaming over W chunks (online max / sum in float64)
-    M = np.full(T, -np.inf)
-    S = np.zeros(T)
+    # LSE of the rows needed: every row when dW/db samples are asked for (a column
+    # of G spans all rows), else only the dX rows. Streamed over W chunks with an
+    # online max / sum in float64.
+    need = np.arange(T) if any(len(r) for r in dw_rows) else np.asarray(dx_rows)
+    M = np.full(need.size, -np.inf)
+    S = np.zeros(need.size)
     for k, (vs, ve) in enumerate(part.ranges):
         hi = min(ve, part.vocab_real)
         for c0 in range(0, max(hi - vs, 0), _W_CHUNK_ROWS):
             c1 = min(hi - vs, c0 + _W_CHUNK_ROWS)
-            a = Xd @ bf16_to_f64(W_bits[k][c0:c1]).T
+            a = Xd[need] @ bf16_to_f64(W_bits[k][c0:c1]).T
             if b_bits is not None:
                 a = a + bf16_to_f64(b_bits[k][c0:c1])[None, :]
             z = a / tau
             Mn = np.maximum(M, z.max(axis=1))
             S = S * np.exp(M - Mn) + np.exp(z - Mn[:, None]).sum(axis=1)
             M = Mn
-    lse = M + np.log(S)
+    lse = np.full(T, np.nan)
+    lse[need] = M + np.log(S)
     # dX on the sampled rows: G_row = g (onehot - p)/tau, dX = G_row W
     dx_rows = np.asarray(dx_rows)
     H = X_bits.shape[1]
@@ -382,6 +386,10 @@ def backward_sampled(X_bits, W_bits, b_bits, part, y, tau, g, dx_rows, dw_rows):
     dW, db = [], []
     for k, (vs, ve) in enumerate(part.ranges):
         rk = np.asarray(dw_rows[k], dtype=np.int64)
+        if rk.size == 0:
+            dW.append(np.zeros((0, H)))
+            db.append(np.zeros(0))
+            continue
         Wr = bf16_to_f64(W_bits[k][rk])
         a = Xd @ Wr.T
         if b_bits is not None:

@@ -358,3 +358,14 @@ def test_backward_sampled_matches_full():
     for k in range(2):
         np.testing.assert_allclose(dW[k], full.dW[k][dw_rows[k]], atol=1e-12)
         np.testing.assert_allclose(db[k], full.db[k][dw_rows[k]], atol=1e-12)
+
+
+def test_backward_sampled_dx_only_matches_full():
+    part = synth.ranges_partition(200, 208, [0, 104, 208])
+    inp = synth.forward_inputs(9, 16, part, tau=0.7, seed=8, w_std=0.3, bias_std=0.1)
+    g = synth.upstream_grad(9, seed=8)
+    full = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g)
+    dX, dW, db = oracle.backward_sampled(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g, [1, 7], [[], []])
+    np.testing.assert_allclose(dX, full.dX[[1, 7]], atol=1e-12)
+    assert dW[0].shape == (0, 16) and db[1].shape == (0,)
+
