@@ -53,21 +53,30 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_hash() -> str:
-    """Hash of the kernel sources: a stored ncu traffic figure is valid only for this hash."""
+# device sources each timed kernel is compiled from
+KERNEL_SOURCES = {
+    "fused_forward": ("lp_fused_forward.cu", "lp_tcgemm.cuh", "lp_device.cuh"),
+    "stream_logits": ("lp_stream.cu", "lp_device.cuh"),
+    "replay": ("lp_replay.cu", "lp_device.cuh"),
+}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of a kernel's sources: a stored ncu traffic figure is valid only for this hash."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def stored_traffic(kernel: str):
+    """DRAM bytes per launch from profiles/traffic.json, or None if the kernel changed since."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
         e = d.get(kernel)
-        if e and e.get("source_hash") == source_hash():
+        if e and e.get("source_hash") == source_hash(kernel):
             return float(e["bytes_per_launch"])
     except Exception:
         pass
