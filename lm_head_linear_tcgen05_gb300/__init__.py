@@ -19,7 +19,11 @@ from typing import Optional, Sequence, Tuple
 
 import torch
 
-from ._build import LIB as LIB_PATH
+from ._build import LIB as _BUILT_LIB
+
+# The in-tree build by default; LP_LIBRARY points the binding at another build of the
+# same C ABI (for example one installed elsewhere).
+LIB_PATH = os.environ.get("LP_LIBRARY", _BUILT_LIB)
 
 LP_MAX_SHARDS = 8
 LP_REPLAY_SLOTS = 64

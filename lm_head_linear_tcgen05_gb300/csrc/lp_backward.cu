@@ -8,19 +8,20 @@
 //     dX = sum_k G_k W_k,   dW_k = G_k^T X,   db_k = sum_t G_k.
 //
 // Steps (all in the caller's workspace; nothing is allocated):
-//   1. X^T and W^T (bf16) by tiled transposes, so that every GEMM below has both
-//      operands K-major and runs on the same tcgen05 pipeline as the forward;
-//   2. the G kernel: the forward's projection X W_k^T recomputed tile by tile on the
-//      tensor core; its epilogue forms G from the accumulator and the saved LSE and
-//      writes it in bf16 twice, as G [T, Vc] and G^T [Vc, Tp];
-//   3. dW_k = G_k^T X: tcgen05 GEMM, A = G^T rows of shard k, B = X^T, K = T;
-//   4. dX = G W: tcgen05 GEMM, A = G, B = W^T, K = every shard's columns in
-//      ascending order, split into a fixed number of K ranges (a function of the
-//      vocabulary only) whose fp32 partials are then summed in ascending order;
-//   5. db_k: sums of the rows of G^T, each in a fixed order.
-// Column layout of G and W^T: shard k occupies columns [coff_k, coff_k + real_k) with
-// coff_k a multiple of 64 and zero columns up to coff_{k+1}, so K blocks never read
-// another shard's data and padded ids contribute exactly zero.
+//   1. the G kernel: the forward's projection X W_k^T recomputed tile by tile on the
+//      tensor core (2-CTA clusters, W tile multicast); its epilogue forms G from the
+//      accumulator and the saved LSE and writes it once, bf16 [T, Vc];
+//   2. dW_k^T = X^T G_k: tcgen05 GEMM with both operands read MN-major straight from
+//      X [T, H] and G [T, Vc] (K = T), 2-CTA clusters sharing the G tile; the
+//      epilogue stores each accumulator row h as column h of dW_k;
+//   3. dX = G W: tcgen05 GEMM, A = G (K-major), B = W_k read MN-major from each
+//      shard's own weight (K = every shard's columns in ascending order), split into
+//      a fixed number of K ranges (a function of the vocabulary only) whose fp32
+//      partials are then summed in ascending order;
+//   4. db_k: column sums of G over fixed 128-row chunks, then over the chunks in order.
+// Column layout of G: shard k occupies columns [coff_k, coff_k + real_k) with coff_k a
+// multiple of 64 and zero columns up to coff_{k+1}, so K blocks never straddle shards
+// and padded ids contribute exactly zero.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -32,19 +33,20 @@ namespace lp {
 namespace {
 
 constexpr int kSplitChunkCols = 32768;  // dX splits K into Vc / 32768 ranges (1..8)
+constexpr int kDbRows = 128;            // rows per db partial sum
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct BwdLayout {
-  int64_t Tp, Vc;
+  int64_t Vc;
   int64_t coff[LP_MAX_SHARDS + 1];
   int split;
-  size_t off_xt, off_wt, off_g, off_gt, off_part, total;
+  int64_t db_chunks;
+  size_t off_g, off_part, off_db, total;
 };
 
 BwdLayout bwd_layout(int64_t T, int64_t H, const Shards& sh) {
   BwdLayout L;
-  L.Tp = (T + 7) / 8 * 8;
   int64_t c = 0;
   for (int k = 0; k < sh.n; ++k) {
     L.coff[k] = c;
@@ -54,43 +56,19 @@ BwdLayout bwd_layout(int64_t T, int64_t H, const Shards& sh) {
   L.Vc = c;
   int split = int(c / kSplitChunkCols);
   L.split = split < 1 ? 1 : (split > 8 ? 8 : split);
+  L.db_chunks = (T + kDbRows - 1) / kDbRows;
   size_t off = 0;
-  L.off_xt = off;
-  off += align_up(size_t(H) * size_t(L.Tp) * 2, 256);
-  L.off_wt = off;
-  off += align_up(size_t(H) * size_t(L.Vc) * 2, 256);
   L.off_g = off;
   off += align_up(size_t(T) * size_t(L.Vc) * 2, 256);
-  L.off_gt = off;
-  off += align_up(size_t(L.Vc) * size_t(L.Tp) * 2, 256);
   L.off_part = off;
   if (L.split > 1) off += align_up(size_t(L.split) * size_t(T) * size_t(H) * 4, 256);
+  L.off_db = off;
+  off += align_up(size_t(L.db_chunks) * size_t(L.Vc) * 4, 256);
   L.total = off;
   return L;
 }
 
 __device__ __forceinline__ float f32(uint32_t r) { return __uint_as_float(r); }
-
-// out[c][col0 + r] = in[r][c] for r < rows, c < cols (bf16, 32 x 32 tiles through
-// shared memory); out[c][col0 + r] = 0 for rows <= r < rows_pad.
-__global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restrict__ in, int64_t ld_in, int64_t rows,
-                                                         int64_t rows_pad, int64_t cols, uint16_t* __restrict__ out,
-                                                         int64_t ld_out, int64_t col0) {
-  __shared__ uint16_t tile[32][33];
-  const int64_t r0 = int64_t(blockIdx.y) * 32;
-  const int64_t c0 = int64_t(blockIdx.x) * 32;
-  const int tx = threadIdx.x & 31;
-  const int ty = threadIdx.x >> 5;  // 0..7
-  for (int i = ty; i < 32; i += 8) {
-    const int64_t r = r0 + i, c = c0 + tx;
-    tile[i][tx] = (r < rows && c < cols) ? in[r * ld_in + c] : uint16_t(0);
-  }
-  __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int64_t c = c0 + i, r = r0 + tx;
-    if (c < cols && r < rows_pad) out[c * ld_out + col0 + r] = tile[tx][i];
-  }
-}
 
 // fp32 dX = sum_s part[s] in ascending s (vectors of 4)
 __global__ void __launch_bounds__(256) reduce_split_kernel(const float4* __restrict__ part, int split, size_t n4,
@@ -108,32 +86,37 @@ __global__ void __launch_bounds__(256) reduce_split_kernel(const float4* __restr
   out[i] = acc;
 }
 
-// db[v] = sum_t G^T[row0 + v][t], one warp per v: lane l adds the 8-element vectors
-// l, l+32, ... in order, then a fixed shuffle tree.
-__global__ void __launch_bounds__(256) bias_grad_kernel(const uint16_t* __restrict__ gt, int64_t ld, int64_t row0,
-                                                         int64_t rows, int64_t T, float* __restrict__ db) {
-  const int64_t v = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (v >= rows) return;
-  const uint4* row = reinterpret_cast<const uint4*>(gt + (row0 + v) * ld);
-  const int64_t nvec = (T + 7) / 8;
-  float acc = 0.f;
-  for (int64_t i = lane; i < nvec; i += 32) {
-    const uint4 q = row[i];
+// part[c][v] = sum over rows t in [128 c, 128 c + 128) of G[t][v], rows in order;
+// each thread owns 8 consecutive columns (one 16-byte vector per row).
+__global__ void __launch_bounds__(256) db_partial_kernel(const uint16_t* __restrict__ G, int64_t Vc, int64_t T,
+                                                          float* __restrict__ part) {
+  const int64_t v8 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+  if (v8 >= Vc) return;
+  const int64_t c = blockIdx.y;
+  const int64_t t0 = c * kDbRows;
+  const int64_t t1 = t0 + kDbRows < T ? t0 + kDbRows : T;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int64_t t = t0; t < t1; ++t) {
+    const uint4 q = *reinterpret_cast<const uint4*>(G + t * Vc + v8);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int64_t t = i * 8 + j;
-      const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
-      if (t < T) acc = __fadd_rn(acc, x);
-    }
+    for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]));
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const float o = __shfl_down_sync(0xffffffffu, acc, off);
-    if (lane < off) acc = __fadd_rn(acc, o);
-  }
-  if (lane == 0) db[v] = acc;
+  float4* o = reinterpret_cast<float4*>(part + c * Vc + v8);
+  o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+// db[v] = sum_c part[c][col0 + v] in ascending c for v < real; 0 for real <= v < width.
+__global__ void __launch_bounds__(256) db_reduce_kernel(const float* __restrict__ part, int64_t Vc, int64_t chunks,
+                                                         int64_t col0, int64_t real, int64_t width,
+                                                         float* __restrict__ db) {
+  const int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (v >= width) return;
+  float acc = 0.f;
+  if (v < real)
+    for (int64_t c = 0; c < chunks; ++c) acc = __fadd_rn(acc, part[c * Vc + col0 + v]);
+  db[v] = acc;
 }
 
 }  // namespace
@@ -149,9 +132,8 @@ struct GradParams {
   const int32_t* y;
   const float* lse;
   const float* grad;
-  uint16_t* G;   // [T][Vc]
-  uint16_t* Gt;  // [Vc][Tp]
-  int64_t Vc, Tp;
+  uint16_t* G;  // [T][Vc]
+  int64_t Vc;
   int64_t coff[LP_MAX_SHARDS + 1];
   int64_t shard_start[LP_MAX_SHARDS];
   int32_t real[LP_MAX_SHARDS];
@@ -165,7 +147,7 @@ struct GradParams {
   float inv_tau;
 };
 
-struct GradEpi {
+struct GradEpi : GemmEpiBase {
   using Params = GradParams;
   static constexpr int kClusterM = kFwdClusterM;
 
@@ -226,9 +208,9 @@ struct GradEpi {
       if (ch * 32 >= wlim) break;
       float bl = 0.f;
       if (bias != nullptr && ch * 32 + lane < valid) bl = __bfloat162float(bias[n0 + ch * 32 + lane]);
-      uint32_t r[32];
       uint32_t packed[16];
       if (ch * 32 < valid) {
+        uint32_t r[32];
         tmem_ld32(tbase + ch * 32, r);
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
@@ -254,70 +236,50 @@ struct GradEpi {
         dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         dst[2] = make_uint4(packed[8], packed[9], packed[10], packed[11]);
         dst[3] = make_uint4(packed[12], packed[13], packed[14], packed[15]);
-        // G^T: column (col_base + ch*32 + j), row `row`; lanes write consecutive rows
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (ch * 32 + j < valid) {
-            const uint16_t h = uint16_t((j & 1) ? (packed[j >> 1] >> 16) : (packed[j >> 1] & 0xFFFFu));
-            p.Gt[size_t(col_base + ch * 32 + j) * size_t(p.Tp) + size_t(row)] = h;
-          }
-        }
       }
     }
   }
 };
 
-// --------------------------------------------------------- fp32 GEMM store
-// mode 0 (dW): tile = (row block of one shard's G^T rows, column block of H),
-//              column blocks fastest; K = T.
-// mode 1 (dX): tile = (row block of T, column block of H, K range s), row blocks
-//              fastest, then column blocks, then s; partial s goes to part[s].
-struct StoreParams {
-  CUtensorMap maps[kGemmMaps];  // [0] A, [1] B
+// ------------------------------------------------------------------- dW
+// Tile = (vocabulary block of one shard, row block of H), row blocks fastest. The
+// accumulator holds dW_k^T: TMEM lane = h, column = vocabulary id, so each thread
+// stores its row h into column h of 256 rows of dW_k (a warp writes 128 contiguous
+// bytes of one dW row per store).
+struct DwParams {
+  CUtensorMap maps[kGemmMaps];  // [0] X [T, H] (MN-major boxes 64 h x 64 t); [1] G [T, Vc] (64 v x 64 t)
   uint32_t keep_maps;
   int32_t total_tiles;
   unsigned int* err;
   uint64_t wait_limit_ns;
-  int32_t mode;
-  int32_t num_m, num_n;
-  int32_t nkb_total, kb_per_split;
-  int64_t H;
-  // mode 0
   float* dW[LP_MAX_SHARDS];
-  int32_t mb_start[LP_MAX_SHARDS + 1];
   int64_t coff[LP_MAX_SHARDS];
-  int64_t real[LP_MAX_SHARDS];
+  int32_t real[LP_MAX_SHARDS];
+  int32_t nb_start[LP_MAX_SHARDS + 1];
   int32_t n_shards;
-  // mode 1
-  float* out;     // dX (split == 1) or partials [split][T][H]
-  int64_t T;
+  int32_t num_m_blocks;  // row blocks of H, counted in whole clusters
+  int32_t nkb;           // K blocks over T
+  int64_t H;
 };
 
-struct StoreEpi {
-  using Params = StoreParams;
-  static constexpr int kClusterM = 1;
+struct DwEpi : GemmEpiBase {
+  using Params = DwParams;
+  static constexpr int kClusterM = kFwdClusterM;
+  static constexpr bool kAMN = true;
+  static constexpr bool kBMN = true;
 
   struct Coord {
-    int shard, mb, nb, s;
+    int shard, nb_local, mb;
   };
 
   static __device__ __forceinline__ Coord coord(const Params& p, int tile) {
     Coord c;
-    if (p.mode == 0) {
-      c.nb = tile % p.num_n;
-      const int mbg = tile / p.num_n;
-      int k = 0;
-      while (k + 1 < p.n_shards && mbg >= p.mb_start[k + 1]) ++k;
-      c.shard = k;
-      c.mb = mbg - p.mb_start[k];
-      c.s = 0;
-    } else {
-      c.mb = tile % p.num_m;
-      const int rest = tile / p.num_m;
-      c.nb = rest % p.num_n;
-      c.s = rest / p.num_n;
-      c.shard = 0;
-    }
+    c.mb = tile % p.num_m_blocks;
+    const int nbg = tile / p.num_m_blocks;
+    int k = 0;
+    while (k + 1 < p.n_shards && nbg >= p.nb_start[k + 1]) ++k;
+    c.shard = k;
+    c.nb_local = nbg - p.nb_start[k];
     return c;
   }
 
@@ -325,33 +287,102 @@ struct StoreEpi {
     const Coord c = coord(p, tile);
     TileJob j;
     j.a_map = 0;
+    j.a_y = c.mb * kGemmBlockM;
     j.b_map = 1;
-    j.b_y = c.nb * kGemmBlockN;
-    if (p.mode == 0) {
-      j.a_y = int(p.coff[c.shard]) + c.mb * kGemmBlockM;
-      j.kb0 = 0;
-      j.nkb = p.nkb_total;
-    } else {
-      j.a_y = c.mb * kGemmBlockM;
-      j.kb0 = c.s * p.kb_per_split;
-      const int left = p.nkb_total - j.kb0;
-      j.nkb = left < p.kb_per_split ? left : p.kb_per_split;
-    }
+    j.b_y = int(p.coff[c.shard]) + c.nb_local * kGemmBlockN;
+    j.kb0 = 0;
+    j.nkb = p.nkb;
     return j;
   }
 
   static __device__ __forceinline__ void run(const Params& p, int tile, uint32_t tbase, int q, int lane) {
     const Coord c = coord(p, tile);
-    const int64_t rloc = int64_t(c.mb) * kGemmBlockM + q * 32 + lane;
-    float* dst;
-    bool ok;
-    if (p.mode == 0) {
-      ok = rloc < p.real[c.shard];
-      dst = p.dW[c.shard] + size_t(ok ? rloc : 0) * size_t(p.H);
-    } else {
-      ok = rloc < p.T;
-      dst = p.out + size_t(c.s) * size_t(p.T) * size_t(p.H) + size_t(ok ? rloc : 0) * size_t(p.H);
+    const int64_t h = int64_t(c.mb) * kGemmBlockM + q * 32 + lane;
+    const int64_t v0 = int64_t(c.nb_local) * kGemmBlockN;
+    const int64_t left = p.real[c.shard] - v0;
+    const int valid = int(left < kGemmBlockN ? left : kGemmBlockN);
+    const bool ok = h < p.H;
+    float* base = p.dW[c.shard] + size_t(v0) * size_t(p.H) + size_t(ok ? h : 0);
+#pragma unroll 1
+    for (int ch = 0; ch < kGemmBlockN / 32; ++ch) {
+      if (ch * 32 >= valid) break;
+      uint32_t r[32];
+      tmem_ld32(tbase + ch * 32, r);
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (ch * 32 + j < valid) base[size_t(ch * 32 + j) * size_t(p.H)] = f32(r[j]);
+      }
     }
+  }
+};
+
+// ------------------------------------------------------------------- dX
+// Tile = (row block of T, column block of H, K range s), row blocks fastest, then
+// column blocks, then s. A = G (K-major, K = global column), B = W_k read MN-major from
+// the shard holding each K block; partial s goes to out + s*T*H.
+struct DxParams {
+  CUtensorMap maps[kGemmMaps];  // [0] G [T, Vc] (boxes 64 v x 128 t); [1 + k] W_k [real_k, H] (64 h x 64 v)
+  uint32_t keep_maps;
+  int32_t total_tiles;
+  unsigned int* err;
+  uint64_t wait_limit_ns;
+  float* out;
+  int64_t coff[LP_MAX_SHARDS + 1];
+  int32_t n_shards;
+  int32_t num_m_blocks;  // row blocks of T, counted in whole clusters
+  int32_t num_n;
+  int32_t nkb_total;
+  int32_t kb_per_split;
+  int64_t T, H;
+};
+
+struct DxEpi : GemmEpiBase {
+  using Params = DxParams;
+  static constexpr int kClusterM = kFwdClusterM;
+  static constexpr bool kBMN = true;
+
+  struct Coord {
+    int mb, nb, s;
+  };
+
+  static __device__ __forceinline__ Coord coord(const Params& p, int tile) {
+    Coord c;
+    c.mb = tile % p.num_m_blocks;
+    const int rest = tile / p.num_m_blocks;
+    c.nb = rest % p.num_n;
+    c.s = rest / p.num_n;
+    return c;
+  }
+
+  static __device__ __forceinline__ TileJob job(const Params& p, int tile) {
+    const Coord c = coord(p, tile);
+    TileJob j;
+    j.a_map = 0;
+    j.a_y = c.mb * kGemmBlockM;
+    j.b_map = 1;
+    j.b_y = c.nb * kGemmBlockN;
+    j.kb0 = c.s * p.kb_per_split;
+    const int left = p.nkb_total - j.kb0;
+    j.nkb = left < p.kb_per_split ? left : p.kb_per_split;
+    return j;
+  }
+
+  // the W map and local row of global K block kb0 + kb: the shard whose columns hold it
+  static __device__ __forceinline__ void b_k(const void* pp, const TileJob& j, int kb, int& map, int& k) {
+    const Params& p = *static_cast<const Params*>(pp);
+    const int64_t col = int64_t(j.kb0 + kb) * kFwdBlockK;
+    int s = 0;
+    while (s + 1 < p.n_shards && col >= p.coff[s + 1]) ++s;
+    map = 1 + s;
+    k = int(col - p.coff[s]);
+  }
+
+  static __device__ __forceinline__ void run(const Params& p, int tile, uint32_t tbase, int q, int lane) {
+    const Coord c = coord(p, tile);
+    const int64_t row = int64_t(c.mb) * kGemmBlockM + q * 32 + lane;
+    const bool ok = row < p.T;
+    float* dst = p.out + size_t(c.s) * size_t(p.T) * size_t(p.H) + size_t(ok ? row : 0) * size_t(p.H);
     const int64_t c0 = int64_t(c.nb) * kGemmBlockN;
     const int64_t cols = p.H - c0 < kGemmBlockN ? p.H - c0 : kGemmBlockN;
 #pragma unroll 1
@@ -363,40 +394,37 @@ struct StoreEpi {
         float4* d4 = reinterpret_cast<float4*>(dst + c0 + ch * 32);
 #pragma unroll
         for (int v = 0; v < 8; ++v)
-          if (ch * 32 + v * 4 < cols) d4[v] = make_float4(f32(r[4 * v]), f32(r[4 * v + 1]), f32(r[4 * v + 2]), f32(r[4 * v + 3]));
+          if (ch * 32 + v * 4 < cols)
+            d4[v] = make_float4(f32(r[4 * v]), f32(r[4 * v + 1]), f32(r[4 * v + 2]), f32(r[4 * v + 3]));
       }
     }
   }
 };
+
+namespace {
+
+// bf16 [rows, inner] with row stride ld as MN-major atoms: boxes of 64 (inner) x 64 rows
+bool encode_mn_atoms(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t ld) {
+  return encode_bf16_2d(m, base, inner, rows, ld, 64);
+}
+
+int32_t pad_to_cluster(int64_t blocks) {
+  return int32_t((blocks + kFwdClusterM - 1) / kFwdClusterM * kFwdClusterM);
+}
+
+}  // namespace
 
 size_t backward_ws_bytes(int64_t T, int64_t H, const Shards& sh) { return bwd_layout(T, H, sh).total; }
 
 lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) {
   const BwdLayout L = bwd_layout(a.T, a.H, sh);
   char* ws = static_cast<char*>(a.workspace);
-  uint16_t* Xt = reinterpret_cast<uint16_t*>(ws + L.off_xt);
-  uint16_t* Wt = reinterpret_cast<uint16_t*>(ws + L.off_wt);
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.off_g);
-  uint16_t* Gt = reinterpret_cast<uint16_t*>(ws + L.off_gt);
   float* part = reinterpret_cast<float*>(ws + L.off_part);
+  float* dbp = reinterpret_cast<float*>(ws + L.off_db);
   const int64_t T = a.T, H = a.H;
 
-  // 1. transposes
-  {
-    dim3 grid(unsigned((H + 31) / 32), unsigned((T + 31) / 32));
-    transpose_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(a.X), H, T, T, H, Xt, L.Tp, 0);
-    if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
-    for (int k = 0; k < sh.n; ++k) {
-      const int64_t rp = L.coff[k + 1] - L.coff[k];
-      if (rp == 0) continue;
-      dim3 g2(unsigned((H + 31) / 32), unsigned((rp + 31) / 32));
-      transpose_kernel<<<g2, 256, 0, s>>>(static_cast<const uint16_t*>(a.W[k]), H, sh.real[k], rp, H, Wt, L.Vc,
-                                           L.coff[k]);
-      if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
-    }
-  }
-
-  // 2. G and G^T
+  // 1. G
   {
     GradParams p;
     std::memset(&p, 0, sizeof(p));
@@ -418,8 +446,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.keep_maps = 1u;
     p.n_shards = sh.n;
     p.T = int32_t(T);
-    const int64_t mblocks = (T + kFwdBlockM - 1) / kFwdBlockM;
-    p.num_m_blocks = int32_t((mblocks + kFwdClusterM - 1) / kFwdClusterM * kFwdClusterM);
+    p.num_m_blocks = pad_to_cluster((T + kFwdBlockM - 1) / kFwdBlockM);
     p.num_k_blocks = int32_t((H + kFwdBlockK - 1) / kFwdBlockK);
     p.total_tiles = nb * p.num_m_blocks;
     p.err = a.err;
@@ -428,41 +455,38 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.lse = a.lse;
     p.grad = a.grad;
     p.G = G;
-    p.Gt = Gt;
     p.Vc = L.Vc;
-    p.Tp = L.Tp;
     p.vocab_real = sh.vocab_real;
     p.scale_log2 = float(1.4426950408889634 / double(a.tau));
     p.inv_tau = float(1.0 / double(a.tau));
     if (launch_tc_gemm<GradEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
   }
 
-  // 3. dW_k = G_k^T X  (and zero rows of padded ids)
+  // 2. dW_k (and zero rows of padded ids)
   {
-    StoreParams p;
+    DwParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!encode_bf16_2d(&p.maps[0], Gt, uint64_t(T), uint64_t(L.Vc), uint64_t(L.Tp), kFwdBlockM) ||
-        !encode_bf16_2d(&p.maps[1], Xt, uint64_t(T), uint64_t(H), uint64_t(L.Tp), kFwdBlockN))
+    if (!encode_mn_atoms(&p.maps[0], a.X, uint64_t(H), uint64_t(T), uint64_t(H)) ||
+        !encode_mn_atoms(&p.maps[1], G, uint64_t(L.Vc), uint64_t(T), uint64_t(L.Vc)))
       return LP_ERR_CUDA;
-    p.keep_maps = 2u;  // X^T is reused by every row block
-    p.mode = 0;
-    p.num_n = int32_t((H + kFwdBlockN - 1) / kFwdBlockN);
-    p.nkb_total = int32_t((T + kFwdBlockK - 1) / kFwdBlockK);
-    p.H = H;
-    int mb = 0;
+    p.keep_maps = 1u;  // X is re-read by every vocabulary block
+    int nb = 0;
     for (int k = 0; k < sh.n; ++k) {
       p.dW[k] = a.dW[k];
-      p.mb_start[k] = mb;
       p.coff[k] = L.coff[k];
-      p.real[k] = sh.real[k];
-      mb += int((sh.real[k] + kFwdBlockM - 1) / kFwdBlockM);
+      p.real[k] = int32_t(sh.real[k]);
+      p.nb_start[k] = nb;
+      nb += int((sh.real[k] + kFwdBlockN - 1) / kFwdBlockN);
     }
-    p.mb_start[sh.n] = mb;
+    p.nb_start[sh.n] = nb;
     p.n_shards = sh.n;
-    p.total_tiles = mb * p.num_n;
+    p.num_m_blocks = pad_to_cluster((H + kFwdBlockM - 1) / kFwdBlockM);
+    p.nkb = int32_t((T + kFwdBlockK - 1) / kFwdBlockK);
+    p.H = H;
+    p.total_tiles = nb * p.num_m_blocks;
     p.err = a.err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
-    if (launch_tc_gemm<StoreEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
+    if (launch_tc_gemm<DwEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
     for (int k = 0; k < sh.n; ++k) {
       const int64_t pad = sh.width[k] - sh.real[k];
       if (pad > 0 && cudaMemsetAsync(a.dW[k] + sh.real[k] * H, 0, size_t(pad) * size_t(H) * 4, s) != cudaSuccess)
@@ -470,27 +494,29 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     }
   }
 
-  // 4. dX = G W
+  // 3. dX = G W
   {
-    StoreParams p;
+    DxParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!encode_bf16_2d(&p.maps[0], G, uint64_t(L.Vc), uint64_t(T), uint64_t(L.Vc), kFwdBlockM) ||
-        !encode_bf16_2d(&p.maps[1], Wt, uint64_t(L.Vc), uint64_t(H), uint64_t(L.Vc), kFwdBlockN))
-      return LP_ERR_CUDA;
+    if (!encode_bf16_2d(&p.maps[0], G, uint64_t(L.Vc), uint64_t(T), uint64_t(L.Vc), kFwdBlockM)) return LP_ERR_CUDA;
+    for (int k = 0; k < sh.n; ++k)
+      if (sh.real[k] > 0 && !encode_mn_atoms(&p.maps[1 + k], a.W[k], uint64_t(H), uint64_t(sh.real[k]), uint64_t(H)))
+        return LP_ERR_CUDA;
+    for (int k = 0; k <= sh.n; ++k) p.coff[k] = L.coff[k];
     p.keep_maps = 0u;
-    p.mode = 1;
-    p.num_m = int32_t((T + kFwdBlockM - 1) / kFwdBlockM);
+    p.n_shards = sh.n;
+    p.num_m_blocks = pad_to_cluster((T + kFwdBlockM - 1) / kFwdBlockM);
     p.num_n = int32_t((H + kFwdBlockN - 1) / kFwdBlockN);
     p.nkb_total = int32_t(L.Vc / kFwdBlockK);
     p.kb_per_split = (p.nkb_total + L.split - 1) / L.split;
     const int splits = (p.nkb_total + p.kb_per_split - 1) / p.kb_per_split;
-    p.H = H;
     p.T = T;
+    p.H = H;
     p.out = splits > 1 ? part : a.dX;
-    p.total_tiles = p.num_m * p.num_n * splits;
+    p.total_tiles = p.num_m_blocks * p.num_n * splits;
     p.err = a.err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
-    if (launch_tc_gemm<StoreEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
+    if (launch_tc_gemm<DxEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
     if (splits > 1) {
       const size_t n4 = size_t(T) * size_t(H) / 4;
       reduce_split_kernel<<<unsigned((n4 + 255) / 256), 256, 0, s>>>(reinterpret_cast<const float4*>(part), splits,
@@ -499,16 +525,21 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     }
   }
 
-  // 5. db
-  for (int k = 0; k < sh.n; ++k) {
-    if (a.db[k] == nullptr) continue;
-    if (sh.real[k] > 0) {
-      const unsigned blocks = unsigned((sh.real[k] * 32 + 255) / 256);
-      bias_grad_kernel<<<blocks, 256, 0, s>>>(Gt, L.Tp, L.coff[k], sh.real[k], T, a.db[k]);
+  // 4. db
+  bool any_db = false;
+  for (int k = 0; k < sh.n; ++k) any_db = any_db || (a.db[k] != nullptr && sh.width[k] > 0);
+  if (any_db) {
+    dim3 grid(unsigned((L.Vc / 8 + 255) / 256), unsigned(L.db_chunks));
+    if (L.Vc > 0) {
+      db_partial_kernel<<<grid, 256, 0, s>>>(G, L.Vc, T, dbp);
       if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
     }
-    const int64_t pad = sh.width[k] - sh.real[k];
-    if (pad > 0 && cudaMemsetAsync(a.db[k] + sh.real[k], 0, size_t(pad) * 4, s) != cudaSuccess) return LP_ERR_CUDA;
+    for (int k = 0; k < sh.n; ++k) {
+      if (a.db[k] == nullptr || sh.width[k] == 0) continue;
+      db_reduce_kernel<<<unsigned((sh.width[k] + 255) / 256), 256, 0, s>>>(dbp, L.Vc, L.db_chunks, L.coff[k],
+                                                                           sh.real[k], sh.width[k], a.db[k]);
+      if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
+    }
   }
   return LP_OK;
 }

@@ -248,11 +248,29 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Descriptor of an MN-major bf16 operand in the 128-byte swizzled layout TMA writes
+// for boxes of 64 MN-elements x 64 K-rows: each K row is 128 bytes (64 consecutive
+// MN elements), 8 K rows form a 1024-byte swizzle atom, consecutive 8-row K groups
+// are 1024 bytes apart (stride byte offset) and consecutive 64-element MN atoms are
+// `mn_atom_bytes` apart (leading byte offset). Advancing along K by 16 rows adds
+// 2048 bytes (128 in the encoded address).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t mn_atom_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(mn_atom_bytes >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits [4,6) = 1),
-// A and B bf16 (bits [7,10) = 1, [10,13) = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits [17,23), M >> 4 in bits [24,29).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+// A and B bf16 (bits [7,10) = 1, [10,13) = 1), A / B major-ness in bits 15 / 16
+// (0 = K-major, 1 = MN-major), N >> 3 in bits [17,23), M >> 4 in bits [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false,
+                                                      bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
 }
 
 // 32 TMEM lanes x 32 consecutive 32-bit columns: thread i of the warp receives

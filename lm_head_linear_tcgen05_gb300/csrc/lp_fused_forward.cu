@@ -101,7 +101,7 @@ __device__ __forceinline__ TileCoord fwd_coord(const FwdParams& p, int tile) {
 
 }  // namespace
 
-struct LogpEpi {
+struct LogpEpi : GemmEpiBase {
   using Params = FwdParams;
   static constexpr int kClusterM = kFwdClusterM;
 

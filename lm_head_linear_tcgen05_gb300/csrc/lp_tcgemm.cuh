@@ -27,8 +27,10 @@
 // role leaves its loop; the producer then waits (bounded) for its copies in flight,
 // the MMA warp for its MMAs, and TMEM is freed before the CTA exits.
 //
-// An epilogue type E provides
+// An epilogue type E derives from GemmEpiBase and provides
 //   static constexpr int kClusterM;       1, or 2 for the multicast pairing above
+//   kAMN / kBMN                           operand major-ness (default K-major)
+//   a_k / b_k                             per-k-block map and K coordinate (default above)
 //   struct E::Params           with members `CUtensorMap maps[kGemmMaps]`,
 //                              `uint32_t keep_maps` (bit i: map i is small and
 //                              reused, loaded with an L2 evict-last hint),
@@ -37,8 +39,9 @@
 //   static TileJob E::job(const Params&, int tile);
 //   static void E::run(const Params&, int tile, uint32_t tmem_row_base, int quarter, int lane);
 // `tmem_row_base` addresses column 0 of the tile's accumulator at this warp's first
-// lane; column c of this thread's row is at tmem_row_base + c. With kClusterM = 2 the
-// B maps must have boxes of 128 rows (each CTA loads half of the 256-row tile).
+// lane; column c of this thread's row is at tmem_row_base + c. Boxes: K-major A 64 x 128,
+// K-major B 64 x 256 (64 x 128 with kClusterM = 2: each CTA loads half), MN-major
+// operands 64 x 64 atoms (with kClusterM = 2 each CTA loads half of B's atoms).
 #pragma once
 
 #include "lp_device.cuh"
@@ -57,12 +60,30 @@ constexpr uint32_t kGemmStageA = kGemmBlockM * kGemmBlockK * 2;  // 16 KB
 constexpr uint32_t kGemmStageB = kGemmBlockN * kGemmBlockK * 2;  // 32 KB
 constexpr uint32_t kGemmStageBytes = kGemmStageA + kGemmStageB;
 
-// What one tile reads: box rows a_y.. of map a_map and b_y.. of map b_map, for k
-// blocks kb0 .. kb0 + nkb - 1 (coordinates in elements; x = k * 64); nkb >= 1.
+constexpr uint32_t kMNAtomBytes = 64 * kGemmBlockK * 2;  // 64 MN elements x 64 K rows: 8 KB
+
+// What one tile reads: rows (MN indices) a_y.. of map a_map and b_y.. of map b_map,
+// for k blocks kb0 .. kb0 + nkb - 1; nkb >= 1. A K-major operand is one box at
+// (x = k, y = row); an MN-major one is a row of 64-wide atoms at (x = mn, y = k).
 struct TileJob {
   int a_map, b_map;
   int a_y, b_y;
   int kb0, nkb;
+};
+
+// Default K coordinates: the tile's own maps, k = (kb0 + kb) * 64. An epilogue type
+// overrides a_k / b_k when an operand's K range spans several maps (shards).
+struct GemmEpiBase {
+  static constexpr bool kAMN = false;  // A operand MN-major
+  static constexpr bool kBMN = false;  // B operand MN-major
+  static __device__ __forceinline__ void a_k(const void*, const TileJob& j, int kb, int& map, int& k) {
+    map = j.a_map;
+    k = (j.kb0 + kb) * kFwdBlockK;
+  }
+  static __device__ __forceinline__ void b_k(const void*, const TileJob& j, int kb, int& map, int& k) {
+    map = j.b_map;
+    k = (j.kb0 + kb) * kFwdBlockK;
+  }
 };
 
 struct GemmSync {
@@ -137,15 +158,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             ok = false;
             break;
           }
-          const int x = (j.kb0 + kb) * kGemmBlockK;
+          int am, ak, bm, bk;
+          E::a_k(&p, j, kb, am, ak);
+          E::b_k(&p, j, kb, bm, bk);
           mbar_arrive_expect_tx(&sync->full[stage], kGemmStageBytes);
-          tma_load_2d(sA + stage * kGemmStageA, &p.maps[j.a_map], &sync->full[stage], x, j.a_y, pa);
-          if constexpr (kCM == 2) {
-            constexpr uint32_t half = kGemmStageB / 2;
-            tma_load_2d_multicast(sB + stage * kGemmStageB + rank * half, &p.maps[j.b_map], &sync->full[stage], x,
-                                  j.b_y + int(rank) * (kGemmBlockN / 2), uint16_t(0x3), pb);
+          uint8_t* dA = sA + stage * kGemmStageA;
+          uint8_t* dB = sB + stage * kGemmStageB;
+          if constexpr (!E::kAMN) {
+            tma_load_2d(dA, &p.maps[am], &sync->full[stage], ak, j.a_y, pa);
+          } else {  // MN-major: 64-element atoms of 64 K rows each
+#pragma unroll
+            for (int i = 0; i < kGemmBlockM / 64; ++i)
+              tma_load_2d(dA + i * kMNAtomBytes, &p.maps[am], &sync->full[stage], j.a_y + 64 * i, ak, pa);
+          }
+          if constexpr (!E::kBMN) {
+            if constexpr (kCM == 2)
+              tma_load_2d_multicast(dB + rank * (kGemmStageB / 2), &p.maps[bm], &sync->full[stage], bk,
+                                    j.b_y + int(rank) * (kGemmBlockN / 2), uint16_t(0x3), pb);
+            else
+              tma_load_2d(dB, &p.maps[bm], &sync->full[stage], bk, j.b_y, pb);
           } else {
-            tma_load_2d(sB + stage * kGemmStageB, &p.maps[j.b_map], &sync->full[stage], x, j.b_y, pb);
+            constexpr int kAtoms = kGemmBlockN / 64;
+#pragma unroll
+            for (int i = 0; i < kAtoms / kCM; ++i) {
+              const int a = int(rank) * (kAtoms / kCM) + i;
+              if constexpr (kCM == 2)
+                tma_load_2d_multicast(dB + a * kMNAtomBytes, &p.maps[bm], &sync->full[stage], j.b_y + 64 * a, bk,
+                                      uint16_t(0x3), pb);
+              else
+                tma_load_2d(dB + a * kMNAtomBytes, &p.maps[bm], &sync->full[stage], j.b_y + 64 * a, bk, pb);
+            }
           }
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -163,7 +205,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBlockM, kGemmBlockN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBlockM, kGemmBlockN, E::kAMN, E::kBMN);
+      // per 16-deep K step: +32 bytes inside a K-major row, +2048 bytes (16 rows) in MN-major
+      constexpr uint32_t a_step = E::kAMN ? 128u : 2u;
+      constexpr uint32_t b_step = E::kBMN ? 128u : 2u;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int ct = cluster_id; ok && ct < cluster_tiles; ct += num_clusters) {
@@ -177,11 +222,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             break;
           }
           tc_fence_after();
-          const uint64_t a_desc = sw128_kmajor_desc(smem_u32(sA + stage * kGemmStageA));
-          const uint64_t b_desc = sw128_kmajor_desc(smem_u32(sB + stage * kGemmStageB));
+          const uint32_t aa = smem_u32(sA + stage * kGemmStageA);
+          const uint32_t ba = smem_u32(sB + stage * kGemmStageB);
+          const uint64_t a_desc = E::kAMN ? sw128_mnmajor_desc(aa, kMNAtomBytes) : sw128_kmajor_desc(aa);
+          const uint64_t b_desc = E::kBMN ? sw128_mnmajor_desc(ba, kMNAtomBytes) : sw128_kmajor_desc(ba);
 #pragma unroll
           for (int k = 0; k < kGemmBlockK / 16; ++k)
-            umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc, (kb | k) != 0 ? 1u : 0u);
           if constexpr (kCM == 2)
             umma_commit_multicast(&sync->empty[stage], uint16_t(0x3));
           else

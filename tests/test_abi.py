@@ -68,7 +68,8 @@ def test_workspace_sizes(lp):
     nb = 149 + 149 + 149 + 148
     T = 4096
     assert lp.lp_workspace_size(lp.LP_OP_FORWARD, T, 4096, p4) == 3 * nb * T * 4 + T * 4
-    assert lp.lp_workspace_size(lp.LP_OP_BACKWARD, T, 4096, p4) > 3 * 151936 * 4096 * 2
+    # backward: G in bf16 [T, V] plus dX partials and db partials
+    assert lp.lp_workspace_size(lp.LP_OP_BACKWARD, T, 4096, p4) > T * 151936 * 2
     # invalid partitions size to 0
     assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 64, 256, _part(lp, 1000, 1000, [0, 500, 900])) == 0
     assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 0, 256, p) == 0
