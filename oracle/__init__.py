@@ -32,8 +32,11 @@ Readings where the pages are silent (each one is also listed in the design notes
   once, here.
 * Replay ids are 64 int32 slots per row, -1 marks an unused slot; the set R is
   the sorted distinct ids; LSE is taken over R only; logp = -inf if y is not in R.
-* Backward is the gradient of sum_t g_t * logp_t (no entropy term):
-  G[t,v] = g_t (1[v = y_t] - p_tv) / tau, dX = G W, dW = G^T X, db = sum_t G.
+* Backward is the gradient of sum_t g_t * logp_t, plus sum_t h_t * entropy_t when an
+  entropy gradient h is given: G[t,v] = (g_t (1[v = y_t] - p_tv) - h_t p_tv (z_tv -
+  mu_t)) / tau with mu_t = sum_v p_tv z_tv; dX = G W, dW = G^T X, db = sum_t G.
+* The logits-gather replay scores the replay set from reused unscaled logits
+  (z_v = L[t, v] / tau) instead of x . W[v]; everything else as the replay.
 
 Pins (tests/test_oracle.py, CPU only): closed forms (W = 0, constant bias,
 two-level logits, one dominant logit), torch.log_softmax in float64 on random
@@ -285,6 +288,45 @@ def top_p_replay(X_bits, W_bits, b_bits, part, ids, y, tau: float, rows=None) ->
     return ReplayResult(logp, lse, sh_lse, sh_t)
 
 
+def top_p_replay_from_logits(L_bits, part, ids, y, tau: float, rows=None) -> ReplayResult:
+    """Compact top-p replay scored from reused local logits: z_v = L_k[t, v - vs_k] / tau
+    for v in the row's sorted distinct set R (temperature once, here); LSE over R;
+    logp = z_y - LSE_R if y in R else -inf; per-shard local LSE and target logit with
+    the empty-shard convention. Same set rules as ``top_p_replay``."""
+    rows = np.arange(np.asarray(ids).shape[0]) if rows is None else np.asarray(rows)
+    K = part.n_shards
+    T = rows.shape[0]
+    logp = np.full(T, -np.inf)
+    lse = np.full(T, -np.inf)
+    sh_lse = np.full((K, T), -np.inf)
+    sh_t = np.zeros((K, T))
+    starts = np.array([r[0] for r in part.ranges])
+    for i, r in enumerate(rows):
+        R = replay_set(ids[r], part.vocab_real)
+        if R.size == 0:
+            continue
+        zs = np.empty(R.size)
+        for j, v in enumerate(R):
+            k = int(np.searchsorted(starts, v, side="right") - 1)
+            zs[j] = float(bf16_to_f64(L_bits[k][r, v - part.ranges[k][0]: v - part.ranges[k][0] + 1])[0]) / tau
+        M = zs.max()
+        lse[i] = M + np.log(np.exp(zs - M).sum())
+        yi = int(y[r])
+        hit = np.nonzero(R == yi)[0]
+        if hit.size:
+            logp[i] = zs[hit[0]] - lse[i]
+        for k, (vs, ve) in enumerate(part.ranges):
+            m = (R >= vs) & (R < ve)
+            if not m.any():
+                continue
+            zk = zs[m]
+            Mk = zk.max()
+            sh_lse[k, i] = Mk + np.log(np.exp(zk - Mk).sum())
+            if vs <= yi < ve and hit.size:
+                sh_t[k, i] = zs[hit[0]]
+    return ReplayResult(logp, lse, sh_lse, sh_t)
+
+
 # ------------------------------------------------------------------------ backward
 
 @dataclass
@@ -295,11 +337,14 @@ class BackwardResult:
     dw_rows: List[np.ndarray]      # local row indices of each shard that dW/db cover
 
 
-def backward_f64(Xd, Wd, bd, ranges, vocab_real, y, tau, g, dw_rows=None) -> BackwardResult:
-    """Gradient of sum_t g_t logp_t with respect to X, W_k and b_k (float64 inputs).
+def backward_f64(Xd, Wd, bd, ranges, vocab_real, y, tau, g, dw_rows=None, h=None) -> BackwardResult:
+    """Gradient of sum_t g_t logp_t (+ sum_t h_t entropy_t when h is given) with respect
+    to X, W_k and b_k (float64 inputs).
 
-    p = softmax(z) over the real ids; G[t,v] = g_t (1[v = y_t] - p_tv) / tau on real
-    ids and 0 on padded ids; dX = sum_k G_k W_k; dW_k = G_k^T X; db_k = sum_t G_k.
+    p = softmax(z) over the real ids, mu_t = sum_v p_tv z_tv;
+    G[t,v] = (g_t (1[v = y_t] - p_tv) - h_t p_tv (z_tv - mu_t)) / tau on real ids and 0
+    on padded ids (d entropy / d z_v = -p_v (z_v - mu)); dX = sum_k G_k W_k;
+    dW_k = G_k^T X; db_k = sum_t G_k.
     """
     y = np.asarray(y, dtype=np.int64)
     z = logits_f64(Xd, Wd, bd, ranges, vocab_real, tau)
@@ -310,6 +355,9 @@ def backward_f64(Xd, Wd, bd, ranges, vocab_real, y, tau, g, dw_rows=None) -> Bac
     onehot = np.zeros_like(p)
     onehot[np.arange(T), y] = 1.0
     G = np.asarray(g, dtype=np.float64)[:, None] * (onehot - p) / tau   # [T, vocab_real]
+    if h is not None:
+        mu = (p * z).sum(axis=1, keepdims=True)
+        G -= np.asarray(h, dtype=np.float64)[:, None] * p * (z - mu) / tau
     H = Xd.shape[1]
     dX = np.zeros((T, H))
     dW, db, rows_out = [], [], []
@@ -327,12 +375,13 @@ def backward_f64(Xd, Wd, bd, ranges, vocab_real, y, tau, g, dw_rows=None) -> Bac
     return BackwardResult(dX, dW, db, rows_out)
 
 
-def backward(X_bits, W_bits, b_bits, part, y, tau, g, dw_rows=None) -> BackwardResult:
-    """``backward_f64`` on bf16 inputs. ``dw_rows[k]`` (local indices) limits dW/db to a sample."""
+def backward(X_bits, W_bits, b_bits, part, y, tau, g, dw_rows=None, h=None) -> BackwardResult:
+    """``backward_f64`` on bf16 inputs. ``dw_rows[k]`` (local indices) limits dW/db to a
+    sample; ``h`` is the optional upstream gradient of the entropy."""
     Xd = bf16_to_f64(X_bits)
     Wd = [bf16_to_f64(w) for w in W_bits]
     bd = None if b_bits is None else [bf16_to_f64(b) for b in b_bits]
-    return backward_f64(Xd, Wd, bd, part.ranges, part.vocab_real, y, tau, g, dw_rows)
+    return backward_f64(Xd, Wd, bd, part.ranges, part.vocab_real, y, tau, g, dw_rows, h)
 
 
 def backward_sampled(X_bits, W_bits, b_bits, part, y, tau, g, dx_rows, dw_rows):

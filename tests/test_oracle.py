@@ -369,3 +369,101 @@ def test_backward_sampled_dx_only_matches_full():
     np.testing.assert_allclose(dX, full.dX[[1, 7]], atol=1e-12)
     assert dW[0].shape == (0, 16) and db[1].shape == (0,)
 
+
+
+# ------------------------------------------------------- logits-gather replay
+
+def _exact_logits_case(seed):
+    """X, W with small-integer entries so that X W^T is exact in bf16: the unscaled
+    logits a projection would produce can then be stored losslessly."""
+    rng = np.random.default_rng(seed)
+    part = synth.ranges_partition(50, 64, [0, 20, 20, 64])
+    T, H = 6, 8
+    Xf = rng.integers(-2, 3, size=(T, H)).astype(np.float32)
+    Wf = rng.integers(-2, 3, size=(64, H)).astype(np.float32)
+    X = synth.bf16_bits(Xf)
+    W = [synth.bf16_bits(Wf[s:e]) for s, e in part.ranges]
+    L = [synth.bf16_bits((Xf @ Wf[s:e].T).astype(np.float32)) for s, e in part.ranges]
+    return part, X, W, L
+
+
+def test_logits_gather_replay_equals_projection_replay_on_exact_logits():
+    part, X, W, L = _exact_logits_case(0)
+    ids, y = synth.replay_ids(6, part, seed=1, max_ids=30)
+    a = oracle.top_p_replay(X, W, None, part, ids, y, 0.7)
+    b = oracle.top_p_replay_from_logits(L, part, ids, y, 0.7)
+    np.testing.assert_allclose(b.lse, a.lse, atol=1e-12)
+    np.testing.assert_allclose(b.logp, a.logp, atol=1e-12)
+    np.testing.assert_allclose(b.shard_lse, a.shard_lse, atol=1e-12)
+    np.testing.assert_allclose(b.shard_t, a.shard_t, atol=1e-12)
+
+
+def test_logits_gather_replay_whole_vocab_equals_logits_forward_and_brute_force():
+    part = synth.ranges_partition(40, 48, [0, 16, 32, 48])
+    L, y, tau = synth.logits_inputs(3, part, 0.7, seed=5, peak_frac=0.1)
+    ids = np.full((3, 64), -1, np.int32)
+    for t in range(3):
+        ids[t, :40] = np.random.default_rng(t).permutation(40)
+    r = oracle.top_p_replay_from_logits(L, part, ids, y, tau)
+    f = oracle.forward_from_logits(L, part, y, tau)
+    np.testing.assert_allclose(r.lse, f.lse, atol=1e-12)
+    np.testing.assert_allclose(r.logp, f.logp, atol=1e-12)
+    # brute force on row 0 over a 3-id set, temperature once
+    ids1 = np.full((1, 64), -1, np.int32)
+    ids1[0, :4] = [7, 33, 7, 20]
+    r1 = oracle.top_p_replay_from_logits([x[:1] for x in L], part, ids1, np.array([33]), tau)
+    zs = [_dec(L[0][0][7]) / tau, _dec(L[1][0][4]) / tau, _dec(L[2][0][1]) / tau]
+    lse = math.log(math.fsum(math.exp(z) for z in zs))
+    assert abs(r1.lse[0] - lse) < 1e-12 and abs(r1.logp[0] - (zs[2] - lse)) < 1e-12
+
+
+# ------------------------------------------------------------ entropy gradient
+
+def test_entropy_gradient_central_finite_differences():
+    part = synth.ranges_partition(20, 24, [0, 10, 24])
+    rng = np.random.default_rng(12)
+    T, H, tau = 3, 5, 0.7
+    Xd = rng.standard_normal((T, H))
+    Wd = [rng.standard_normal((e - s, H)) * 0.5 for s, e in part.ranges]
+    bd = [rng.standard_normal(e - s) * 0.5 for s, e in part.ranges]
+    y = np.array([2, 19, 11])
+    g = rng.standard_normal(T)
+    hh = rng.standard_normal(T)
+    r = oracle.backward_f64(Xd, Wd, bd, part.ranges, 20, y, tau, g, h=hh)
+
+    def loss():
+        z = oracle.logits_f64(Xd, Wd, bd, part.ranges, 20, tau)
+        M = z.max(axis=1, keepdims=True)
+        lse = (M + np.log(np.exp(z - M).sum(axis=1, keepdims=True)))[:, 0]
+        p = np.exp(z - lse[:, None])
+        ent = -(p * (z - lse[:, None])).sum(axis=1)
+        return float(np.dot(g, z[np.arange(T), y] - lse) + np.dot(hh, ent))
+
+    eps = 1e-6
+
+    def fd(arr, idx):
+        old = arr[idx]
+        arr[idx] = old + eps
+        lp_ = loss()
+        arr[idx] = old - eps
+        lm_ = loss()
+        arr[idx] = old
+        return (lp_ - lm_) / (2 * eps)
+
+    np.testing.assert_allclose(r.dX, [[fd(Xd, (t, j)) for j in range(H)] for t in range(T)], rtol=1e-6, atol=1e-8)
+    for k in range(2):
+        Vk = Wd[k].shape[0]
+        np.testing.assert_allclose(r.dW[k], [[fd(Wd[k], (v, j)) for j in range(H)] for v in range(Vk)],
+                                   rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(r.db[k], [fd(bd[k], (v,)) for v in range(Vk)], rtol=1e-6, atol=1e-8)
+
+
+def test_entropy_gradient_of_uniform_logits_vanishes():
+    # z constant => p uniform, z - mu = 0: the entropy term adds nothing
+    part = synth.even_partition(30, 1)
+    X = np.zeros((2, 4), np.uint16)
+    W = [np.zeros((30, 4), np.uint16)]
+    g = np.array([0.5, -1.0])
+    a = oracle.backward(X, W, None, part, np.array([1, 2]), 0.7, g)
+    b = oracle.backward(X, W, None, part, np.array([1, 2]), 0.7, g, h=np.array([3.0, 7.0]))
+    np.testing.assert_allclose(b.db[0], a.db[0], atol=1e-15)
