@@ -155,6 +155,17 @@ LP_API lp_status lp_top_p_replay(const void* X, int64_t T, int64_t H,
                           const int32_t* y, float tau, const lp_outputs* out,
                           void* workspace, size_t ws_bytes, lp_stream_t stream);
 
+/* Compact top-p replay scored from reused local logits (page "Perf/cuda compact top p
+ * replay", Walkthrough: the replay data travels with the local logits through the
+ * tensor-parallel helper). Same id-set rules and outputs as lp_top_p_replay, but z_v
+ * = logits[k][t, v - vocab_start_k] / tau: logits[k] is shard k's UNSCALED bf16 logits
+ * [T, V_k] with row stride ld[k] elements (ld[k] >= V_k); temperature is applied once,
+ * here. Reads only the logits of the replay ids. out->entropy must be NULL. */
+LP_API lp_status lp_top_p_replay_from_logits(const void* const* logits, const int64_t* ld, int64_t T,
+                                             const lp_vocab_partition* part, const int32_t* replay_ids,
+                                             const int32_t* y, float tau, const lp_outputs* out,
+                                             void* workspace, size_t ws_bytes, lp_stream_t stream);
+
 /* The dense keep-mask route the compact replay replaces (page "Perf/cuda compact
  * top p replay", Validation: dense-mask and compact-support results are bitwise
  * equal). keep_mask[k] is uint8 [T, V_k] (nonzero = id kept, padded ids ignored).
@@ -166,18 +177,23 @@ LP_API lp_status lp_top_p_replay_dense_mask(const void* X, int64_t T, int64_t H,
                                      float tau, const lp_outputs* out, void* workspace,
                                      size_t ws_bytes, lp_stream_t stream);
 
-/* Backward of sum_t grad_logp[t] * logp[t] (the gradient the provider's autograd
- * contract implies; page "feat(rl-kernel): add CUDA linear logp provider
- * integration", Summary). With p = softmax(z) over the real ids and lse the
- * merged LSE from lp_forward:
- *   G[t,v] = grad_logp[t] * (1[v == y_t] - exp(z[t,v] - lse[t])) / tau   (0 on padded ids)
+/* Backward of sum_t grad_logp[t] * logp[t] (+ sum_t grad_entropy[t] * entropy[t]),
+ * the gradient the provider's autograd contract implies (page "feat(rl-kernel): add
+ * CUDA linear logp provider integration", Summary: logp and optional entropy with
+ * gradients attached). With p = softmax(z) over the real ids, lse and entropy the
+ * merged outputs of lp_forward and mu = lse - entropy (= sum_v p_v z_v):
+ *   G[t,v] = (grad_logp[t] (1[v == y_t] - p_tv) - grad_entropy[t] p_tv (z_tv - mu_t)) / tau
+ *            (0 on padded ids)
  *   dX = sum_k G_k W_k (fp32 [T,H]),  dW_k = G_k^T X (fp32 [V_k,H]),  db_k = sum_t G_k (fp32 [V_k]).
+ * entropy and grad_entropy are both NULL (logp term only) or both given. Rows whose
+ * lse or grad_logp is not finite, or whose target is invalid, get no gradient.
  * dX, dW[k] and db[k] are overwritten. db may be NULL (then no bias gradient);
  * dW entries may be NULL only for empty shards. */
 LP_API lp_status lp_backward(const void* X, int64_t T, int64_t H,
                       const void* const* W, const void* const* bias,
                       const lp_vocab_partition* part, const int32_t* y, float tau,
                       const float* lse, const float* grad_logp,
+                      const float* entropy, const float* grad_entropy,
                       float* dX, float* const* dW, float* const* db,
                       void* workspace, size_t ws_bytes, lp_stream_t stream);
 

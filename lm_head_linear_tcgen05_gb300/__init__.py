@@ -51,7 +51,7 @@ LP_OP_TOP_P_REPLAY_DENSE_MASK = 4
 
 # every symbol include/lp.h declares
 EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
-            "lp_top_p_replay_dense_mask", "lp_backward", "lp_get_device_error",
+            "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward", "lp_get_device_error",
             "lp_selftest_wait_timeout", "lp_device_supported", "lp_status_string")
 
 
@@ -110,16 +110,19 @@ def lib() -> ctypes.CDLL:
     L.lp_forward_noalloc.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, P(_Outputs), vp]
     L.lp_forward_from_logits.argtypes = [P(vp), P(i64), i64, P(_Partition), vp, f32, P(_Outputs), vp, sz, vp]
     L.lp_top_p_replay.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, vp, f32, P(_Outputs), vp, sz, vp]
+    L.lp_top_p_replay_from_logits.argtypes = [P(vp), P(i64), i64, P(_Partition), vp, vp, f32, P(_Outputs), vp, sz,
+                                              vp]
     L.lp_top_p_replay_dense_mask.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), P(vp), vp, f32,
                                              P(_Outputs), vp, sz, vp]
-    L.lp_backward.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, vp, vp, vp, P(vp), P(vp),
-                              vp, sz, vp]
+    L.lp_backward.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, vp, vp, vp, vp, vp, P(vp),
+                              P(vp), vp, sz, vp]
     L.lp_get_device_error.argtypes = [vp]
     L.lp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     L.lp_device_supported.argtypes = []
     L.lp_status_string.argtypes = [ctypes.c_int]
     L.lp_status_string.restype = ctypes.c_char_p
-    for name in ("lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay", "lp_top_p_replay_dense_mask",
+    for name in ("lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
+                 "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask",
                  "lp_backward", "lp_get_device_error", "lp_selftest_wait_timeout", "lp_device_supported"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -267,12 +270,9 @@ def lp_forward_noalloc(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optiona
     return o
 
 
-def lp_forward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tensor, tau: float,
-                           entropy: bool = True, shard_stats: bool = False) -> dict:
-    """Logits-reuse forward from unscaled bf16 logits[k] [T, V_k] (row stride = stride(0))."""
-    _check(y, "y", torch.int32, 1)
-    n = len(part.ranges)
-    T = y.shape[0]
+def _logits_ld(logits, n: int, T: int):
+    if len(logits) != n:
+        raise ValueError("logits must have one entry per shard")
     ld = (ctypes.c_int64 * max(n, 1))()
     for k, L in enumerate(logits):
         if L is None:
@@ -282,8 +282,16 @@ def lp_forward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tensor
         if L.stride(1) != 1 or L.shape[0] != T:
             raise ValueError(f"logits[{k}] must be [T, V_k] with unit column stride")
         ld[k] = L.stride(0)
-    if len(logits) != n:
-        raise ValueError("logits must have one entry per shard")
+    return ld
+
+
+def lp_forward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tensor, tau: float,
+                           entropy: bool = True, shard_stats: bool = False) -> dict:
+    """Logits-reuse forward from unscaled bf16 logits[k] [T, V_k] (row stride = stride(0))."""
+    _check(y, "y", torch.int32, 1)
+    n = len(part.ranges)
+    T = y.shape[0]
+    ld = _logits_ld(logits, n, T)
     cp, _keep = _c_partition(part)
     with torch.cuda.device(y.device):
         o, co = _outputs(T, n, y.device, entropy, shard_stats)
@@ -315,6 +323,26 @@ def lp_top_p_replay(X: torch.Tensor, W, bias, part, replay_ids: torch.Tensor, y:
     return o
 
 
+def lp_top_p_replay_from_logits(logits: Sequence[torch.Tensor], part, replay_ids: torch.Tensor, y: torch.Tensor,
+                                tau: float, shard_stats: bool = False) -> dict:
+    """Compact top-p replay scored from reused unscaled bf16 logits[k] [T, V_k]."""
+    _check(y, "y", torch.int32, 1)
+    _check(replay_ids, "replay_ids", torch.int32, 2)
+    T = y.shape[0]
+    if replay_ids.shape != (T, LP_REPLAY_SLOTS):
+        raise ValueError("replay_ids must be [T, 64]")
+    n = len(part.ranges)
+    ld = _logits_ld(logits, n, T)
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(y.device):
+        o, co = _outputs(T, n, y.device, False, shard_stats)
+        st = lib().lp_top_p_replay_from_logits(_ptr_array(logits), ld, T, ctypes.byref(cp), replay_ids.data_ptr(),
+                                               y.data_ptr(), float(tau), ctypes.byref(co), None, 0,
+                                               _stream(y.device))
+    _raise(st, "lp_top_p_replay_from_logits")
+    return o
+
+
 def lp_top_p_replay_dense_mask(X: torch.Tensor, W, bias, part, keep_mask: Sequence[torch.Tensor], y: torch.Tensor,
                                tau: float, shard_stats: bool = False,
                                workspace: Optional[torch.Tensor] = None) -> dict:
@@ -341,13 +369,20 @@ def lp_top_p_replay_dense_mask(X: torch.Tensor, W, bias, part, keep_mask: Sequen
 
 def lp_backward(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse: torch.Tensor,
                 grad_logp: torch.Tensor, bias_grad: bool = True,
-                workspace: Optional[torch.Tensor] = None) -> dict:
-    """Backward of sum_t grad_logp[t] logp[t]: returns fp32 dX [T,H], dW (per shard [V_k,H]),
-    db (per shard [V_k], or None). `lse` is the merged LSE returned by lp_forward."""
+                workspace: Optional[torch.Tensor] = None, entropy: Optional[torch.Tensor] = None,
+                grad_entropy: Optional[torch.Tensor] = None) -> dict:
+    """Backward of sum_t grad_logp[t] logp[t] (+ sum_t grad_entropy[t] entropy[t]): returns
+    fp32 dX [T,H], dW (per shard [V_k,H]), db (per shard [V_k], or None). `lse` and
+    `entropy` are the merged outputs of lp_forward."""
     _check(X, "X", torch.bfloat16, 2)
     _check(y, "y", torch.int32, 1)
     _check(lse, "lse", torch.float32, 1)
     _check(grad_logp, "grad_logp", torch.float32, 1)
+    if (entropy is None) != (grad_entropy is None):
+        raise ValueError("entropy and grad_entropy go together")
+    if entropy is not None:
+        _check(entropy, "entropy", torch.float32, 1)
+        _check(grad_entropy, "grad_entropy", torch.float32, 1)
     n = len(part.ranges)
     W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
     bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
@@ -363,6 +398,7 @@ def lp_backward(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse
               for s, e in part.ranges] if bias_grad else None
         st = lib().lp_backward(X.data_ptr(), T, H, _ptr_array(W), _ptr_array(bias) if bias is not None else None,
                                ctypes.byref(cp), y.data_ptr(), float(tau), lse.data_ptr(), grad_logp.data_ptr(),
+                               _ptr(entropy), _ptr(grad_entropy),
                                dX.data_ptr(), _ptr_array(dW), _ptr_array(db) if db is not None else None,
                                _ptr(ws), wsb, _stream(X.device))
     _raise(st, "lp_backward")

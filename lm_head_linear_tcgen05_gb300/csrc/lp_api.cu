@@ -371,6 +371,44 @@ lp_status lp_top_p_replay(const void* X, int64_t T, int64_t H, const void* const
   return LP_OK;
 }
 
+lp_status lp_top_p_replay_from_logits(const void* const* logits, const int64_t* ld, int64_t T,
+                                      const lp_vocab_partition* part, const int32_t* replay_ids, const int32_t* y,
+                                      float tau, const lp_outputs* out, void* workspace, size_t ws_bytes,
+                                      lp_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  Shards sh;
+  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (logits == nullptr || ld == nullptr || replay_ids == nullptr || y == nullptr || out == nullptr ||
+      out->logp == nullptr || out->lse == nullptr || out->entropy != nullptr || !valid_rows(T) || !valid_tau(tau))
+    return LP_ERR_INVALID_ARG;
+  for (int k = 0; k < sh.n; ++k)
+    if (sh.real[k] > 0 && (logits[k] == nullptr || ld[k] < sh.width[k])) return LP_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+  ReplayParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int k = 0; k < sh.n; ++k) {
+    p.logits[k] = static_cast<const __nv_bfloat16*>(logits[k]);
+    p.ld[k] = ld[k];
+    p.shard_start[k] = sh.start[k];
+    p.shard_end[k] = sh.end[k];
+  }
+  p.ids = replay_ids;
+  p.y = y;
+  p.logp = out->logp;
+  p.lse = out->lse;
+  p.shard_stats = out->shard_stats;
+  p.err = dev->err;
+  p.vocab_real = sh.vocab_real;
+  p.n_shards = sh.n;
+  p.T = int32_t(T);
+  p.inv_tau = float(1.0 / double(tau));
+  if (launch_replay_from_logits(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
+}
+
 lp_status lp_top_p_replay_dense_mask(const void* X, int64_t T, int64_t H, const void* const* W,
                                      const void* const* bias, const lp_vocab_partition* part,
                                      const uint8_t* const* keep_mask, const int32_t* y, float tau,
@@ -409,12 +447,13 @@ lp_status lp_top_p_replay_dense_mask(const void* X, int64_t T, int64_t H, const 
 
 lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W, const void* const* bias,
                       const lp_vocab_partition* part, const int32_t* y, float tau, const float* lse,
-                      const float* grad_logp, float* dX, float* const* dW, float* const* db, void* workspace,
-                      size_t ws_bytes, lp_stream_t stream) {
+                      const float* grad_logp, const float* entropy, const float* grad_entropy, float* dX,
+                      float* const* dW, float* const* db, void* workspace, size_t ws_bytes, lp_stream_t stream) {
   Shards sh;
   if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
   if (X == nullptr || W == nullptr || y == nullptr || lse == nullptr || grad_logp == nullptr || dX == nullptr ||
-      dW == nullptr || !valid_rows(T) || !valid_hidden(H) || !valid_tau(tau))
+      dW == nullptr || !valid_rows(T) || !valid_hidden(H) || !valid_tau(tau) ||
+      ((entropy == nullptr) != (grad_entropy == nullptr)))
     return LP_ERR_INVALID_ARG;
   for (int k = 0; k < sh.n; ++k) {
     if (sh.width[k] == 0) continue;
@@ -436,6 +475,8 @@ lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W,
   a.tau = tau;
   a.lse = lse;
   a.grad = grad_logp;
+  a.entropy = entropy;
+  a.grad_entropy = grad_entropy;
   a.dX = dX;
   for (int k = 0; k < sh.n; ++k) {
     a.W[k] = W[k];

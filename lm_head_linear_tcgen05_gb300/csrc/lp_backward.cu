@@ -1,10 +1,11 @@
 // lp_backward.cu - deterministic backward of the linear-logp operator.
 //
-// Gradient of sum_t g_t * logp_t, the quantity whose autograd the provider contract
-// of page "feat(rl-kernel): add CUDA linear logp provider integration" (Summary:
-// detached gradients are rejected) requires. With p = softmax(z) over the real
-// vocabulary and the merged LSE of the forward:
-//     G[t, v] = g_t (1[v = y_t] - exp(z[t, v] - LSE_t)) / tau        (0 on padded ids)
+// Gradient of sum_t g_t * logp_t (+ sum_t h_t * entropy_t), the quantity whose
+// autograd the provider contract of page "feat(rl-kernel): add CUDA linear logp
+// provider integration" (Summary: logp and optional entropy, detached gradients
+// rejected) requires. With p = softmax(z) over the real vocabulary, the merged LSE
+// and entropy of the forward and mu = LSE - entropy:
+//     G[t, v] = (g_t (1[v = y_t] - p_tv) - h_t p_tv (z_tv - mu_t)) / tau   (0 on padded ids)
 //     dX = sum_k G_k W_k,   dW_k = G_k^T X,   db_k = sum_t G_k.
 //
 // Steps (all in the caller's workspace; nothing is allocated):
@@ -132,6 +133,8 @@ struct GradParams {
   const int32_t* y;
   const float* lse;
   const float* grad;
+  const float* entropy;       // or NULL
+  const float* grad_entropy;  // or NULL
   uint16_t* G;  // [T][Vc]
   int64_t Vc;
   int64_t coff[LP_MAX_SHARDS + 1];
@@ -187,17 +190,27 @@ struct GradEpi : GemmEpiBase {
     const int64_t span = (real + 63) / 64 * 64 - n0;  // columns up to the next shard
     const int wlim = int(span < kGemmBlockN ? span : kGemmBlockN);
     const bool in_rows = row < p.T;
-    float gi = 0.f, lse2 = 0.f;
+    float gi = 0.f, lse2 = 0.f, hi = 0.f, mu = 0.f;
     int64_t ycol = -1;
+    bool live = false;
     if (in_rows) {
       const float l = __ldg(p.lse + row);
       const float g = __ldg(p.grad + row);
       const int yv = __ldg(p.y + row);
       // rows without a finite LSE or a valid target get no gradient
       if (isfinite(l) && isfinite(g) && yv >= 0 && int64_t(yv) < p.vocab_real) {
+        live = true;
         gi = __fmul_rn(g, p.inv_tau);
         lse2 = __fmul_rn(l, kLog2e);
         ycol = int64_t(yv) - p.shard_start[c.shard] - n0;
+        if (p.grad_entropy != nullptr) {
+          const float h = __ldg(p.grad_entropy + row);
+          const float e = __ldg(p.entropy + row);
+          if (isfinite(h) && isfinite(e)) {
+            hi = __fmul_rn(h, p.inv_tau);
+            mu = __fsub_rn(l, e);  // sum_v p_v z_v = LSE - entropy
+          }
+        }
       }
     }
     const __nv_bfloat16* bias = p.bias[c.shard];
@@ -221,7 +234,10 @@ struct GradEpi : GemmEpiBase {
             const float v = __fadd_rn(f32(r[j + h]), __shfl_sync(0xffffffffu, bl, j + h));
             const float pr = hw_ex2(__fmaf_rn(v, p.scale_log2, -lse2));
             const float oh = (int64_t(col) == ycol) ? 1.f : 0.f;
-            gv[h] = (col < valid && gi != 0.f) ? __fmul_rn(gi, __fsub_rn(oh, pr)) : 0.f;
+            // logp term g (1[v = y] - p) / tau, entropy term - h p (z - mu) / tau
+            float gval = __fmul_rn(gi, __fsub_rn(oh, pr));
+            if (hi != 0.f) gval = __fsub_rn(gval, __fmul_rn(__fmul_rn(hi, pr), __fsub_rn(__fmul_rn(v, p.inv_tau), mu)));
+            gv[h] = (col < valid && live) ? gval : 0.f;
           }
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(gv[0], gv[1]);
           packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
@@ -454,6 +470,8 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.y = a.y;
     p.lse = a.lse;
     p.grad = a.grad;
+    p.entropy = a.entropy;
+    p.grad_entropy = a.grad_entropy;
     p.G = G;
     p.Vc = L.Vc;
     p.vocab_real = sh.vocab_real;

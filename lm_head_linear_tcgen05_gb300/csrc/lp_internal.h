@@ -98,11 +98,14 @@ struct StreamParams {
   float inv_tau;
 };
 
-// Compact top-p replay, one CTA per row.
+// Compact top-p replay, one CTA per row. Scores come from x . W[v] + b[v] (X, W, bias)
+// or, in the logits-gather variant, from reused unscaled logits (logits, ld).
 struct ReplayParams {
   const __nv_bfloat16* X;
   const __nv_bfloat16* W[LP_MAX_SHARDS];
   const __nv_bfloat16* bias[LP_MAX_SHARDS];
+  const __nv_bfloat16* logits[LP_MAX_SHARDS];
+  int64_t ld[LP_MAX_SHARDS];
   const int32_t* ids;                   // [T][64]
   const int32_t* y;
   float* logp;
@@ -138,6 +141,8 @@ struct BackwardArgs {
   float tau;
   const float* lse;
   const float* grad;
+  const float* entropy;       // with grad_entropy: the forward's entropy, else NULL
+  const float* grad_entropy;  // upstream gradient of the entropy, or NULL
   float* dX;
   const void* W[LP_MAX_SHARDS];
   const void* bias[LP_MAX_SHARDS];
@@ -160,6 +165,7 @@ cudaError_t launch_fused_forward(const FwdParams& p, int num_sms, cudaStream_t s
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_stream_logits(const StreamParams& p, cudaStream_t s);
 cudaError_t launch_replay(const ReplayParams& p, cudaStream_t s);
+cudaError_t launch_replay_from_logits(const ReplayParams& p, cudaStream_t s);
 cudaError_t launch_mask_compact(const MaskParams& p, cudaStream_t s);
 
 }  // namespace lp

@@ -18,6 +18,8 @@
 //      the shards in ascending order.
 // The dense keep-mask route compacts each mask row into the same canonical slots
 // and runs this very kernel, so both routes produce identical bits for equal sets.
+// The logits-gather variant (reused unscaled logits instead of x . W) replaces step 3
+// by one gather per id and keeps steps 1 and 4.
 #include <cuda_bf16.h>
 
 #include "lp_device.cuh"
@@ -82,6 +84,7 @@ __device__ __forceinline__ int shard_of(const ReplayParams& p, int64_t v) {
 
 }  // namespace
 
+template <bool kFromLogits>
 __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const __grid_constant__ ReplayParams p) {
   extern __shared__ uint4 xs[];  // the row of X, H / 8 vectors
   __shared__ int32_t slots[LP_REPLAY_SLOTS];
@@ -137,22 +140,34 @@ __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const __grid_con
       if (any_bad) record_error(p.err, LP_ERR_REPLAY_ID_OUT_OF_RANGE);
     }
   }
-  // 2. stage x
-  const uint4* xrow = reinterpret_cast<const uint4*>(p.X) + size_t(row) * size_t(nvec);
-  for (int v = tid; v < nvec; v += kReplayThreads) xs[v] = __ldg(xrow + v);
+  if constexpr (!kFromLogits) {
+    // 2. stage x
+    const uint4* xrow = reinterpret_cast<const uint4*>(p.X) + size_t(row) * size_t(nvec);
+    for (int v = tid; v < nvec; v += kReplayThreads) xs[v] = __ldg(xrow + v);
+  }
   __syncthreads();
 
   const int n = bad_row ? 0 : n_uniq;
-  // 3. gather GEMV
-  for (int i = warp; i < n; i += kReplayWarps) {
-    const int64_t v = uniq[i];
-    const int k = shard_of(p, v);
-    const int64_t local = v - p.shard_start[k];
-    const uint4* wrow = reinterpret_cast<const uint4*>(p.W[k]) + size_t(local) * size_t(nvec);
-    const float dot = warp_dot(wrow, xs, nvec, lane);
-    if (lane == 0) {
-      const float b = p.bias[k] != nullptr ? __bfloat162float(p.bias[k][local]) : 0.f;
-      zs[i] = __fmul_rn(__fadd_rn(dot, b), p.inv_tau);
+  if constexpr (!kFromLogits) {
+    // 3. gather GEMV
+    for (int i = warp; i < n; i += kReplayWarps) {
+      const int64_t v = uniq[i];
+      const int k = shard_of(p, v);
+      const int64_t local = v - p.shard_start[k];
+      const uint4* wrow = reinterpret_cast<const uint4*>(p.W[k]) + size_t(local) * size_t(nvec);
+      const float dot = warp_dot(wrow, xs, nvec, lane);
+      if (lane == 0) {
+        const float b = p.bias[k] != nullptr ? __bfloat162float(p.bias[k][local]) : 0.f;
+        zs[i] = __fmul_rn(__fadd_rn(dot, b), p.inv_tau);
+      }
+    }
+  } else {
+    // 3. gather of the reused logits, temperature applied here (once)
+    if (tid < n) {
+      const int64_t v = uniq[tid];
+      const int k = shard_of(p, v);
+      const float l = __bfloat162float(p.logits[k][size_t(row) * size_t(p.ld[k]) + size_t(v - p.shard_start[k])]);
+      zs[tid] = __fmul_rn(l, p.inv_tau);
     }
   }
   __syncthreads();
@@ -240,10 +255,16 @@ __global__ void __launch_bounds__(256) mask_compact_kernel(const __grid_constant
 cudaError_t launch_replay(const ReplayParams& p, cudaStream_t s) {
   const size_t smem = size_t(p.H / 8) * sizeof(uint4);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(replay_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e =
+        cudaFuncSetAttribute(replay_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
   }
-  replay_kernel<<<p.T, kReplayThreads, smem, s>>>(p);
+  replay_kernel<false><<<p.T, kReplayThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_replay_from_logits(const ReplayParams& p, cudaStream_t s) {
+  replay_kernel<true><<<p.T, kReplayThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

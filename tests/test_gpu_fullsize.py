@@ -178,3 +178,21 @@ def test_replay_full_size_and_dense_mask(lp):
     assert lp.lp_get_device_error() == 0
     for k in ("logp", "lse", "shard_stats"):
         assert torch.equal(dm[k], out[k]), k
+
+
+def test_replay_from_logits_full_size(lp):
+    import torch
+    part = synth.even_partition(V, 4)
+    T = 8192
+    L, _, tau = synth.logits_inputs(T, part, TAU, seed=6)
+    ids, y = synth.replay_ids(T, part, seed=6)
+    Ld = [dev_bf16(a) for a in L]
+    out = lp.lp_top_p_replay_from_logits(Ld, part_of(part), dev_i32(ids), dev_i32(y), tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    rows = _sample_rows(T, 1024, 5)
+    ref = oracle.top_p_replay_from_logits(L, part, ids, y, tau, rows=rows)
+    assert max_abs(_np(out["logp"])[rows], ref.logp) <= TOL_LOGP
+    assert max_abs(_np(out["lse"])[rows], ref.lse) <= TOL_LSE
+    ss = _np(out["shard_stats"])
+    for k in range(4):
+        assert max_abs(ss[k, 0][rows], ref.shard_lse[k]) <= TOL_LSE

@@ -208,3 +208,79 @@ def test_backward_bitwise_repeatable(lp):
     assert torch.equal(a["dX"], c["dX"])
     for k in range(2):
         assert torch.equal(a["dW"][k], c["dW"][k]) and torch.equal(a["db"][k], c["db"][k])
+
+
+# ---------------------------------------------------------- logits-gather replay
+
+@pytest.mark.parametrize("T,bounds,real", [
+    (150, [0, 2500, 5000, 7500, 10000], 10000),
+    (33, [0, 3000, 3000, 8000, 8192], 8100),          # empty shard, padded ids
+])
+def test_replay_from_logits_parity(lp, T, bounds, real):
+    import torch
+    part = synth.ranges_partition(real, bounds[-1], bounds)
+    L, _, tau = synth.logits_inputs(T, part, 0.7, seed=T)
+    ids, y = synth.replay_ids(T, part, seed=T + 1)
+    Ld = [dev_bf16(a) if a.shape[1] else None for a in L]
+    out = lp.lp_top_p_replay_from_logits(Ld, part_of(part), dev_i32(ids), dev_i32(y), tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.top_p_replay_from_logits(L, part, ids, y, tau)
+    assert max_abs(_np(out["logp"]), ref.logp) <= TOL_LOGP
+    assert max_abs(_np(out["lse"]), ref.lse) <= TOL_LSE
+    ss = _np(out["shard_stats"])
+    for k in range(part.n_shards):
+        assert max_abs(ss[k, 0], ref.shard_lse[k]) <= TOL_LSE
+        assert max_abs(ss[k, 1], ref.shard_t[k]) <= TOL_LOGP
+    again = lp.lp_top_p_replay_from_logits(Ld, part_of(part), dev_i32(ids), dev_i32(y), tau, shard_stats=True)
+    for k in ("logp", "lse", "shard_stats"):
+        assert torch.equal(again[k], out[k])
+
+
+def test_replay_from_exact_logits_is_bitwise_the_projection_replay(lp):
+    # small-integer X and W: every fp32 dot product is exact and equals the bf16 logit,
+    # so scoring from logits and from x . W give the same bits
+    import torch
+    rng = np.random.default_rng(3)
+    part = synth.ranges_partition(500, 512, [0, 200, 200, 512])
+    T, H = 40, 32
+    Xf = rng.integers(-2, 3, size=(T, H)).astype(np.float32)
+    Wf = rng.integers(-2, 3, size=(512, H)).astype(np.float32)
+    X = dev_bf16(synth.bf16_bits(Xf))
+    W = [dev_bf16(synth.bf16_bits(Wf[s:e])) if e > s else None for s, e in part.ranges]
+    L = [dev_bf16(synth.bf16_bits((Xf @ Wf[s:e].T).astype(np.float32))) if e > s else None for s, e in part.ranges]
+    ids, y = synth.replay_ids(T, part, seed=4)
+    P = part_of(part)
+    a = lp.lp_top_p_replay(X, W, None, P, dev_i32(ids), dev_i32(y), 0.7, shard_stats=True)
+    b = lp.lp_top_p_replay_from_logits(L, P, dev_i32(ids), dev_i32(y), 0.7, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    for k in ("logp", "lse", "shard_stats"):
+        assert torch.equal(a[k], b[k]), k
+
+
+# ------------------------------------------------------------ entropy gradient
+
+@pytest.mark.parametrize("T,H,bounds,real,bias", [
+    (96, 256, [0, 1000], 1000, None),
+    (150, 192, [0, 700, 700, 1500, 2048], 2000, 0.3),
+])
+def test_backward_with_entropy_gradient_parity(lp, T, H, bounds, real, bias):
+    part = synth.ranges_partition(real, bounds[-1], bounds)
+    inp = synth.forward_inputs(T, H, part, tau=0.7, seed=T + 1, w_std=0.05, bias_std=bias)
+    g = synth.upstream_grad(T, seed=T)
+    h = synth.upstream_grad(T, seed=T + 100)
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    fwd = lp.lp_forward(X, W, b, P, y, inp.tau)
+    bw = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], dev_f32(g), entropy=fwd["entropy"],
+                        grad_entropy=dev_f32(h))
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g, h=h)
+    assert rel_fro(_np(bw["dX"]), ref.dX) <= TOL_GRAD_REL
+    for k, (s, e) in enumerate(part.ranges):
+        if e == s:
+            continue
+        assert rel_fro(_np(bw["dW"][k]), ref.dW[k]) <= TOL_GRAD_REL, k
+        assert rel_fro(_np(bw["db"][k]), ref.db[k]) <= TOL_GRAD_REL, k
+    # and the entropy term is really there: without it the result is far off
+    plain = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g)
+    assert rel_fro(plain.dX, ref.dX) > 3 * TOL_GRAD_REL
