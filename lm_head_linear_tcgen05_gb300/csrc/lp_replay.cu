@@ -22,6 +22,8 @@
 // by one gather per id and keeps steps 1 and 4.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "lp_device.cuh"
 
 namespace lp {
@@ -255,9 +257,16 @@ __global__ void __launch_bounds__(256) mask_compact_kernel(const __grid_constant
 cudaError_t launch_replay(const ReplayParams& p, cudaStream_t s) {
   const size_t smem = size_t(p.H / 8) * sizeof(uint4);
   if (smem > 48 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(replay_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
+    // the opt-in for the largest x row (H = 65536: 128 KB) once per device
+    static std::atomic<bool> ready[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev].load(std::memory_order_acquire)) {
+      cudaError_t e =
+          cudaFuncSetAttribute(replay_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536 / 8 * 16);
+      if (e != cudaSuccess) return e;
+      ready[dev].store(true, std::memory_order_release);
+    }
   }
   replay_kernel<false><<<p.T, kReplayThreads, smem, s>>>(p);
   return cudaGetLastError();

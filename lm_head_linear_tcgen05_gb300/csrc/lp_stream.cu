@@ -18,6 +18,8 @@
 // row's result never depends on T.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "lp_device.cuh"
 
 namespace lp {
@@ -203,8 +205,14 @@ __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_l
 
 cudaError_t launch_stream_logits(const StreamParams& p, cudaStream_t s) {
   const int smem = kStages * kChunkVecs * int(sizeof(uint4));
-  cudaError_t e = cudaFuncSetAttribute(stream_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  static std::atomic<bool> ready[64];  // shared-memory opt-in done on this device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(stream_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    ready[dev].store(true, std::memory_order_release);
+  }
   stream_logits_kernel<<<p.T, kStreamThreads, smem, s>>>(p);
   return cudaGetLastError();
 }

@@ -44,6 +44,8 @@
 // operands 64 x 64 atoms (with kClusterM = 2 each CTA loads half of B's atoms).
 #pragma once
 
+#include <atomic>
+
 #include "lp_device.cuh"
 
 namespace lp {
@@ -275,28 +277,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   }
 }
 
-// Launches one CTA per SM (rounded to whole clusters) over p.total_tiles tiles.
+// Per-device launch set-up of one GEMM kernel, resolved on the first launch on each
+// device (dynamic shared memory opt-in, clusters that can be co-resident) so that later
+// launches - including launches captured into a CUDA graph - issue nothing but the
+// kernel launch itself.
 template <class E>
-cudaError_t launch_tc_gemm(const typename E::Params& p, int num_sms, cudaStream_t s) {
-  static_assert(kGemmSmemBytes <= 232448, "shared memory budget");
+int gemm_clusters_for_device(int num_sms) {
   constexpr int kCM = E::kClusterM;
-  cudaError_t e =
-      cudaFuncSetAttribute(tc_gemm_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemmSmemBytes));
-  if (e != cudaSuccess) return e;
-  if (p.total_tiles < kCM) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmemBytes;
-  cfg.stream = s;
+  static std::atomic<int> cache[64];  // 0 = unresolved, > 0 = clusters, < 0 = error
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  int c = cache[dev].load(std::memory_order_acquire);
+  if (c != 0) return c;
+  if (cudaFuncSetAttribute(tc_gemm_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemmSmemBytes)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
   int clusters = num_sms / kCM;
   if (kCM > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCM;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
     cfg.gridDim = dim3(kCM * clusters, 1, 1);
     int active = 0;
     if (cudaOccupancyMaxActiveClusters(&active, tc_gemm_kernel<E>, &cfg) == cudaSuccess && active > 0 &&
@@ -304,10 +313,35 @@ cudaError_t launch_tc_gemm(const typename E::Params& p, int num_sms, cudaStream_
       clusters = active;
     cudaGetLastError();
   }
+  if (clusters < 1) clusters = 1;
+  cache[dev].store(clusters, std::memory_order_release);
+  return clusters;
+}
+
+// Launches one CTA per SM (rounded to whole clusters) over p.total_tiles tiles.
+template <class E>
+cudaError_t launch_tc_gemm(const typename E::Params& p, int num_sms, cudaStream_t s) {
+  static_assert(kGemmSmemBytes <= 232448, "shared memory budget");
+  constexpr int kCM = E::kClusterM;
+  int clusters = gemm_clusters_for_device<E>(num_sms);
+  if (clusters < 0) return cudaErrorInvalidConfiguration;
+  if (p.total_tiles < kCM) return cudaSuccess;
   const int cluster_tiles = p.total_tiles / kCM;
   if (clusters > cluster_tiles) clusters = cluster_tiles;
-  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.stream = s;
   cfg.gridDim = dim3(kCM * clusters, 1, 1);
+  if (kCM > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<E>, p);
 }
 
