@@ -194,6 +194,12 @@ def run_ours(args, rank, world, dist):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
 
+    if args.skip_headline:
+        paths = time_other_paths(args, lp, synth, dev, stream, peaks)
+        if rank == 0:
+            print(json.dumps({"paths": paths}), flush=True)
+        return
+
     # ---- headline: fused forward, T=4096, H=4096, V=151936, tau=0.7, no bias
     T_FWD, V = args.rows, args.vocab
     part = synth.even_partition(V, 1)
@@ -265,72 +271,85 @@ def run_ours(args, rank, world, dist):
 
 
 def time_other_paths(args, lp, synth, dev, stream, peaks):
+    """The other hot-path rows, each on its own workload (vocabulary args.vocab)."""
     import torch
     out = {}
-    # logits reuse: T=8192 x 151936 bf16 logits
-    part = synth.even_partition(V, 1)
-    P = lp.VocabPartition(part.vocab_real, part.vocab_padded, part.ranges)
-    L, y = synth.device_logits(8192, part, dev, seed=4)
-    ms = time_steps(lambda: lp.lp_forward_from_logits(L, P, y, TAU), args.steps, args.warmup, stream)
-    nbytes = 8192 * V * 2
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    out["logits_reuse"] = {"workload": "T=8192, V=151936 bf16 logits N(0,9), 1% peaked, tau=0.7",
-                           "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
-                           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                        "frac": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
-                                        "traffic": stored_traffic("stream_logits")}}
+    Vp = args.vocab
+    wanted = set(args.paths.split(","))
+    if wanted & {"logits", "replay"}:
+        part = synth.even_partition(Vp, 1)
+        P = lp.VocabPartition(part.vocab_real, part.vocab_padded, part.ranges)
+        L, y = synth.device_logits(8192, part, dev, seed=4)
+        part4 = synth.even_partition(Vp, 4)
+        P4 = lp.VocabPartition(part4.vocab_real, part4.vocab_padded, part4.ranges)
+        ids, yr = synth.replay_ids(8192, part4, seed=5)
+        ids_d = torch.from_numpy(ids).to(dev)
+        yr_d = torch.from_numpy(yr).to(dev)
+        uniq = sum(len(set(r[r >= 0].tolist())) for r in ids)
+        if "logits" in wanted:
+            # logits reuse: T=8192 x V bf16 logits
+            ms = time_steps(lambda: lp.lp_forward_from_logits(L, P, y, TAU), args.steps, args.warmup, stream)
+            nbytes = 8192 * Vp * 2
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out["logits_reuse"] = {
+                "workload": f"T=8192, V={Vp} bf16 logits N(0,9), 1% peaked, tau=0.7",
+                "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
+                             "traffic": stored_traffic("stream_logits")}}
+        if "replay" in wanted:
+            # the compact replay scored from the reused logits above (one 2-byte gather per id)
+            L4 = [L[0][:, s:e] for s, e in part4.ranges]
+            ms = time_steps(lambda: lp.lp_top_p_replay_from_logits(L4, P4, ids_d, yr_d, TAU), args.steps,
+                            args.warmup, stream)
+            out["top_p_replay_from_logits"] = {
+                "workload": "T=8192 rows of the logits above in 4 shards, 1-64 ids/row",
+                "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms, "ids_scored": uniq}
+        del L
+        torch.cuda.empty_cache()
+        if "replay" in wanted:
+            # compact top-p replay: T=8192, 4 shards, ids as the nucleus recipe
+            X, W, _, _ = synth.device_forward_inputs(8192, H, part4, TAU, dev, seed=5)
+            ms = time_steps(lambda: lp.lp_top_p_replay(X, W, None, P4, ids_d, yr_d, TAU), args.steps, args.warmup,
+                            stream)
+            distinct = len(set(ids[ids >= 0].tolist()))
+            gathered = 8192 * H * 2 + uniq * H * 2
+            distinct_b = 8192 * H * 2 + distinct * H * 2
+            out["top_p_replay"] = {
+                "workload": f"T=8192, H=4096, V={Vp} in 4 shards, 1-64 ids/row (+10% dups), tau=0.7",
+                "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
+                "gathered_bytes": gathered, "distinct_bytes": distinct_b,
+                "roofline": {"bound": "hbm", "achieved": gathered / (ms * 1e-3) / 1e9,
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gathered / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "traffic": stored_traffic("replay")}}
+            del X, W
+            torch.cuda.empty_cache()
 
-    # compact top-p replay: T=8192, 4 shards of 37984; ids as the nucleus recipe
-    part4 = synth.even_partition(V, 4)
-    P4 = lp.VocabPartition(part4.vocab_real, part4.vocab_padded, part4.ranges)
-    ids, yr = synth.replay_ids(8192, part4, seed=5)
-    ids_d = torch.from_numpy(ids).to(dev)
-    yr_d = torch.from_numpy(yr).to(dev)
-    uniq = sum(len(set(r[r >= 0].tolist())) for r in ids)
-
-    # the same replay scored from the reused logits above (one 2-byte gather per id)
-    L4 = [L[0][:, s:e] for s, e in part4.ranges]
-    ms = time_steps(lambda: lp.lp_top_p_replay_from_logits(L4, P4, ids_d, yr_d, TAU), args.steps, args.warmup,
-                    stream)
-    out["top_p_replay_from_logits"] = {"workload": "T=8192 rows of the logits above in 4 shards, 1-64 ids/row",
-                                       "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms, "ids_scored": uniq}
-    del L, L4
-    torch.cuda.empty_cache()
-
-    X, W, _, _ = synth.device_forward_inputs(8192, H, part4, TAU, dev, seed=5)
-    ms = time_steps(lambda: lp.lp_top_p_replay(X, W, None, P4, ids_d, yr_d, TAU), args.steps, args.warmup, stream)
-    distinct = len(set(ids[ids >= 0].tolist()))
-    gathered = 8192 * H * 2 + uniq * H * 2
-    distinct_b = 8192 * H * 2 + distinct * H * 2
-    out["top_p_replay"] = {"workload": "T=8192, H=4096, V=151936 in 4 shards, 1-64 ids/row (+10% dups), tau=0.7",
-                           "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
-                           "gathered_bytes": gathered, "distinct_bytes": distinct_b,
-                           "roofline": {"bound": "hbm", "achieved": gathered / (ms * 1e-3) / 1e9,
-                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                        "frac": gathered / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                                        "traffic": stored_traffic("replay")}}
-    del X, W
-    torch.cuda.empty_cache()
-
-    # vocabulary-sharded forward + backward: V padded to 152064 in 4 shards, bias
-    part3 = synth.ranges_partition(V, 152064, [0, 38016, 76032, 114048, 152064])
-    P3 = lp.VocabPartition(part3.vocab_real, part3.vocab_padded, part3.ranges)
-    X, W, b, y = synth.device_forward_inputs(T_FWD, H, part3, TAU, dev, seed=3, bias_std=0.01)
-    g = torch.randn(T_FWD, generator=torch.Generator(device=dev).manual_seed(3), device=dev)
-    wsf = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
-    wsb = torch.empty(lp.lp_workspace_size(lp.LP_OP_BACKWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
-    fwd = lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf)
-    ms_f = time_steps(lambda: lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf), args.steps, args.warmup, stream)
-    ms_b = time_steps(lambda: lp.lp_backward(X, W, b, P3, y, TAU, fwd["lse"], g, workspace=wsb),
-                      max(3, args.steps // 2), args.warmup, stream)
-    f_fl = 2.0 * T_FWD * H * V
-    out["sharded_fwd_bwd"] = {"workload": "T=4096, H=4096, V=151936 padded to 152064, 4 shards, bias, tau=0.7",
-                              "fwd_tokens_per_s": T_FWD / (ms_f * 1e-3), "fwd_ms": ms_f,
-                              "bwd_tokens_per_s": T_FWD / (ms_b * 1e-3), "bwd_ms": ms_b,
-                              "fwd_bwd_tokens_per_s": T_FWD / ((ms_f + ms_b) * 1e-3),
-                              "fwd_tflops": f_fl / (ms_f * 1e-3) / 1e12,
-                              "bwd_tflops_3gemm": 3 * f_fl / (ms_b * 1e-3) / 1e12,
-                              "bwd_frac_3gemm": 3 * f_fl / (ms_b * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+    if "backward" in wanted:
+        # vocabulary-sharded forward + backward: padded to a multiple of 4 x 64, 4 shards, bias
+        Vpad = (Vp + 4 * 64 * 2 - 1) // (4 * 64 * 2) * (4 * 64 * 2) if Vp != V else 152064
+        w4 = Vpad // 4
+        part3 = synth.ranges_partition(Vp, Vpad, [0, w4, 2 * w4, 3 * w4, Vpad])
+        P3 = lp.VocabPartition(part3.vocab_real, part3.vocab_padded, part3.ranges)
+        X, W, b, y = synth.device_forward_inputs(T_FWD, H, part3, TAU, dev, seed=3, bias_std=0.01)
+        g = torch.randn(T_FWD, generator=torch.Generator(device=dev).manual_seed(3), device=dev)
+        wsf = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(lp.lp_workspace_size(lp.LP_OP_BACKWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
+        fwd = lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf)
+        ms_f = time_steps(lambda: lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf), args.steps, args.warmup,
+                          stream)
+        ms_b = time_steps(lambda: lp.lp_backward(X, W, b, P3, y, TAU, fwd["lse"], g, workspace=wsb),
+                          max(3, args.steps // 2), args.warmup, stream)
+        f_fl = 2.0 * T_FWD * H * Vp
+        out["sharded_fwd_bwd"] = {
+            "workload": f"T=4096, H=4096, V={Vp} padded to {Vpad}, 4 shards, bias, tau=0.7",
+            "fwd_tokens_per_s": T_FWD / (ms_f * 1e-3), "fwd_ms": ms_f,
+            "bwd_tokens_per_s": T_FWD / (ms_b * 1e-3), "bwd_ms": ms_b,
+            "fwd_bwd_tokens_per_s": T_FWD / ((ms_f + ms_b) * 1e-3),
+            "fwd_tflops": f_fl / (ms_f * 1e-3) / 1e12,
+            "bwd_tflops_3gemm": 3 * f_fl / (ms_b * 1e-3) / 1e12,
+            "bwd_frac_3gemm": 3 * f_fl / (ms_b * 1e-3) / 1e12 / peaks["bf16_tflops"]}
     if lp.lp_get_device_error() != 0:
         raise RuntimeError("device error in the path timings")
     return out
@@ -398,7 +417,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per reference step")
     ap.add_argument("--rows", type=int, default=T_FWD, help="headline rows T (profiling of smaller cases)")
-    ap.add_argument("--vocab", type=int, default=V, help="headline vocabulary V (profiling of smaller cases)")
+    ap.add_argument("--vocab", type=int, default=V, help="vocabulary V of every path (profiling of smaller cases)")
+    ap.add_argument("--paths", default="logits,replay,backward",
+                    help="comma list of the other paths to time: logits, replay, backward")
+    ap.add_argument("--skip-headline", action="store_true", help="time only --paths (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -334,9 +334,12 @@ struct DwEpi : GemmEpiBase {
 };
 
 // ------------------------------------------------------------------- dX
-// Tile = (row block of T, column block of H, K range s), row blocks fastest, then
-// column blocks, then s. A = G (K-major, K = global column), B = W_k read MN-major from
-// the shard holding each K block; partial s goes to out + s*T*H.
+// Tile = (row block of T, column block of H, K range s). Within a K range, row blocks
+// go in groups of kDxGroupM: inside a group the row block runs fastest, then the column
+// block, so the tiles in flight at once (about 152) cover ~16 row blocks x ~9 column
+// blocks, and both operands' K slices are shared through L2 by many tiles. A = G
+// (K-major, K = global column), B = W_k read MN-major from the shard holding each K
+// block; partial s goes to out + s*T*H.
 struct DxParams {
   CUtensorMap maps[kGemmMaps];  // [0] G [T, Vc] (boxes 64 v x 128 t); [1 + k] W_k [real_k, H] (64 h x 64 v)
   uint32_t keep_maps;
@@ -362,12 +365,19 @@ struct DxEpi : GemmEpiBase {
     int mb, nb, s;
   };
 
+  static constexpr int kDxGroupM = 16;  // even, so cluster pairs never straddle groups
+
   static __device__ __forceinline__ Coord coord(const Params& p, int tile) {
     Coord c;
-    c.mb = tile % p.num_m_blocks;
-    const int rest = tile / p.num_m_blocks;
-    c.nb = rest % p.num_n;
-    c.s = rest / p.num_n;
+    const int per_split = p.num_m_blocks * p.num_n;
+    c.s = tile / per_split;
+    const int r = tile - c.s * per_split;
+    const int g = r / (kDxGroupM * p.num_n);
+    const int within = r - g * kDxGroupM * p.num_n;
+    const int left = p.num_m_blocks - g * kDxGroupM;
+    const int gs = left < kDxGroupM ? left : kDxGroupM;
+    c.nb = within / gs;
+    c.mb = g * kDxGroupM + within % gs;
     return c;
   }
 

@@ -40,54 +40,105 @@ constexpr int kStreamWarps = kStreamThreads / 32;
 constexpr int kChunkVecs = LP_STREAM_CHUNK_VECS;
 constexpr int kStages = LP_STREAM_STAGES;
 
+// Packed pairs of fp32: the f32x2 instructions of sm_100-family SMs perform two fp32
+// operations per issued instruction.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Per-thread online statistic over raw (unscaled) logits x: the running maximum is
 // tracked on x, m = max(x) * c2 and d = x * c2 - m, so u = x * c2 is never rounded
-// separately from the subtraction. -inf logits (entries a caller masked out) add
-// nothing; a thread that saw only -inf stays empty.
+// separately from the subtraction. Sums are kept as two interleaved partial sums
+// (even / odd elements of each 16-byte vector) in packed fp32 pairs and added at the
+// end. -inf logits (entries a caller masked out) add nothing; a thread that saw only
+// -inf stays empty.
 struct RawStat {
-  float xmax;  // running max of x (-inf while empty)
-  float m;     // xmax * c2
-  float s, a;
+  float xmax;   // running max of x (-inf while empty)
+  float m;      // xmax * c2
+  uint64_t s2;  // {even, odd} partial sums of 2^(u - m)
+  uint64_t a2;  // {even, odd} partial sums of 2^(u - m) (u - m)
 };
 
 __device__ __forceinline__ void raw_rescale(RawStat& st, float new_xmax, float c2) {
   const float nm = __fmul_rn(new_xmax, c2);
   if (st.xmax == -INFINITY) {
-    st.s = 0.f;
-    st.a = 0.f;
+    st.s2 = 0ull;
+    st.a2 = 0ull;
   } else {
     const float d = __fsub_rn(st.m, nm);
     const float e = hw_ex2(d);
-    st.a = __fmul_rn(e, __fmaf_rn(d, st.s, st.a));
-    st.s = __fmul_rn(st.s, e);
+    const uint64_t d2 = pack2(d, d), e2 = pack2(e, e);
+    st.a2 = mul2(e2, fma2(d2, st.s2, st.a2));
+    st.s2 = mul2(st.s2, e2);
   }
   st.xmax = new_xmax;
   st.m = nm;
 }
 
-__device__ __forceinline__ void raw_push8(RawStat& st, const uint4 v, float c2) {
-  float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-  const float vmax = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
-  if (vmax > st.xmax) raw_rescale(st, vmax, c2);
-  const float nm = -st.m;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    // clamping at -256 (2^-256 flushes to 0) keeps -inf (masked) logits from
-    // producing 0 * -inf in the entropy sum
-    const float d = fmaxf(__fmaf_rn(x[j], c2, nm), -256.f);
-    const float e = hw_ex2(d);
-    st.s = __fadd_rn(st.s, e);
-    st.a = __fmaf_rn(e, d, st.a);
-  }
+// fold the pair (lo, hi) of one bf16x2 word
+__device__ __forceinline__ void raw_pair(RawStat& st, uint32_t w, uint64_t c22, uint64_t nm2) {
+  float d0, d1;
+  unpack2(fma2(pack2(bf16_lo(w), bf16_hi(w)), c22, nm2), d0, d1);
+  // clamping at -256 (2^-256 flushes to 0) keeps -inf (masked) logits from
+  // producing 0 * -inf in the entropy sum
+  d0 = fmaxf(d0, -256.f);
+  d1 = fmaxf(d1, -256.f);
+  const uint64_t e2 = pack2(hw_ex2(d0), hw_ex2(d1));
+  st.s2 = add2(st.s2, e2);
+  st.a2 = fma2(e2, pack2(d0, d1), st.a2);
 }
 
+__device__ __forceinline__ void raw_push8(RawStat& st, const uint4 v, float c2) {
+  const uint32_t mm = max_bf16x2(max_bf16x2(v.x, v.y), max_bf16x2(v.z, v.w));
+  const float vmax = fmaxf(bf16_lo(mm), bf16_hi(mm));
+  if (vmax > st.xmax) raw_rescale(st, vmax, c2);
+  const uint64_t c22 = pack2(c2, c2);
+  const uint64_t nm2 = pack2(-st.m, -st.m);
+  raw_pair(st, v.x, c22, nm2);
+  raw_pair(st, v.y, c22, nm2);
+  raw_pair(st, v.z, c22, nm2);
+  raw_pair(st, v.w, c22, nm2);
+}
+
+// one element, folded into the even partial sums
 __device__ __forceinline__ void raw_push1(RawStat& st, float x, float c2) {
   if (x > st.xmax) raw_rescale(st, x, c2);
   const float d = fmaxf(__fmaf_rn(x, c2, -st.m), -256.f);
   const float e = hw_ex2(d);
-  st.s = __fadd_rn(st.s, e);
-  st.a = __fmaf_rn(e, d, st.a);
+  st.s2 = add2(st.s2, pack2(e, 0.f));
+  st.a2 = fma2(pack2(e, 0.f), pack2(d, 0.f), st.a2);
+}
+
+__device__ __forceinline__ Stat raw_to_stat(const RawStat& st) {
+  float s0, s1, a0, a1;
+  unpack2(st.s2, s0, s1);
+  unpack2(st.a2, a0, a1);
+  return Stat{st.m, __fadd_rn(s0, s1), __fadd_rn(a0, a1)};
 }
 
 }  // namespace
@@ -124,7 +175,7 @@ __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_l
     const uint4* src = reinterpret_cast<const uint4*>(L);
     const int64_t nvec = width > 0 ? (width >> 3) : 0;
     const int nchunks = int((nvec + kChunkVecs - 1) / kChunkVecs);
-    RawStat st{-INFINITY, -INFINITY, 0.f, 0.f};
+    RawStat st{-INFINITY, -INFINITY, 0ull, 0ull};
     // thread 0 streams the row through the stage ring; the other threads consume
     auto issue = [&](int c) {
       const int64_t v0 = int64_t(c) * kChunkVecs;
@@ -160,7 +211,7 @@ __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_l
     const int64_t tail0 = nvec << 3;
     if (width > 0 && tail0 + tid < width) raw_push1(st, __bfloat162float(L[tail0 + tid]), c2);
 
-    Stat loc{st.m, st.s, st.a};
+    Stat loc = raw_to_stat(st);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
       const Stat o{__shfl_down_sync(0xffffffffu, loc.m, off), __shfl_down_sync(0xffffffffu, loc.s, off),
