@@ -201,11 +201,25 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
     return workspace, workspace.numel() * workspace.element_size()
 
 
-def _outputs(T: int, n_shards: int, device, entropy: bool, shard_stats: bool):
-    o = {"logp": torch.empty(T, dtype=torch.float32, device=device),
-         "lse": torch.empty(T, dtype=torch.float32, device=device),
-         "entropy": torch.empty(T, dtype=torch.float32, device=device) if entropy else None,
-         "shard_stats": torch.empty((n_shards, 3, T), dtype=torch.float32, device=device) if shard_stats else None}
+def _outputs(T: int, n_shards: int, device, entropy: bool, shard_stats: bool, out: Optional[dict] = None):
+    """Output tensors: the caller's (``out``, contiguous fp32 of the right shapes) or new ones."""
+    if out is None:
+        o = {"logp": torch.empty(T, dtype=torch.float32, device=device),
+             "lse": torch.empty(T, dtype=torch.float32, device=device),
+             "entropy": torch.empty(T, dtype=torch.float32, device=device) if entropy else None,
+             "shard_stats": torch.empty((n_shards, 3, T), dtype=torch.float32, device=device) if shard_stats
+             else None}
+    else:
+        o = {k: out.get(k) for k in ("logp", "lse", "entropy", "shard_stats")}
+        for k in ("logp", "lse", "entropy"):
+            if o[k] is not None:
+                _check(o[k], f"out[{k!r}]", torch.float32, 1)
+                if o[k].shape[0] != T:
+                    raise ValueError(f"out[{k!r}] must have T entries")
+        if o["logp"] is None or o["lse"] is None:
+            raise ValueError("out must hold logp and lse")
+        if o["shard_stats"] is not None:
+            _check(o["shard_stats"], "out['shard_stats']", torch.float32, 3)
     co = _Outputs(_ptr(o["logp"]), _ptr(o["lse"]), _ptr(o["entropy"]), _ptr(o["shard_stats"]))
     return o, co
 
@@ -228,9 +242,10 @@ def _shard_list(ts, n: int, name: str, dtype, ndim: int, allow_none: bool):
 
 def lp_forward(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optional[Sequence[torch.Tensor]], part,
                y: torch.Tensor, tau: float, entropy: bool = True, shard_stats: bool = False,
-               workspace: Optional[torch.Tensor] = None) -> dict:
+               workspace: Optional[torch.Tensor] = None, out: Optional[dict] = None) -> dict:
     """Fused linear-logp forward. X bf16 [T,H]; W[k] bf16 [V_k,H]; bias None or per-shard
-    bf16 [V_k]; y int32 [T]. Returns dict of fp32 tensors logp, lse, entropy, shard_stats."""
+    bf16 [V_k]; y int32 [T]. Returns dict of fp32 tensors logp, lse, entropy, shard_stats
+    (written into ``out`` when given)."""
     _check(X, "X", torch.bfloat16, 2)
     _check(y, "y", torch.int32, 1)
     n = len(part.ranges)
@@ -241,7 +256,7 @@ def lp_forward(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optional[Sequen
     with torch.cuda.device(X.device):
         need = lp_workspace_size(LP_OP_FORWARD, T, H, part)
         ws, wsb = _workspace(need, X.device, workspace)
-        o, co = _outputs(T, n, X.device, entropy, shard_stats)
+        o, co = _outputs(T, n, X.device, entropy, shard_stats, out)
         st = lib().lp_forward(X.data_ptr(), T, H, _ptr_array(W), _ptr_array(bias) if bias is not None else None,
                               ctypes.byref(cp), y.data_ptr(), float(tau), ctypes.byref(co), _ptr(ws), wsb,
                               _stream(X.device))
@@ -403,3 +418,66 @@ def lp_backward(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse
                                _ptr(ws), wsb, _stream(X.device))
     _raise(st, "lp_backward")
     return {"dX": dX, "dW": dW, "db": db}
+
+
+def lp_forward_host(hX: torch.Tensor, W: Sequence[torch.Tensor], bias, part, hy: torch.Tensor, tau: float,
+                    chunk_rows: Optional[int] = None, entropy: bool = True, device=None,
+                    staging: Optional[dict] = None) -> dict:
+    """lp_forward from host memory: pinned CPU hX bf16 [T,H] and hy int32 [T] in, CPU fp32
+    logp / lse / entropy out (pinned tensors owned by ``staging``, overwritten by the next
+    call that reuses it).
+
+    With ``chunk_rows`` the rows go in chunks: chunk c+1 is copied host -> device on a side
+    stream while lp_forward runs on chunk c. A row's results do not depend on the batch it
+    is computed in, so the outputs are bit-identical to one call over all rows. Each chunk
+    streams W again, so chunks pay off only when they stay large (several thousand rows);
+    by default (None) all rows go in one chunk: at T = 4096, H = 4096 the 33.5 MB copy takes
+    0.16 ms against 2.76 ms of projection, while 4 chunks of 1024 rows take 3.33 ms.
+    ``staging`` (optional, reused across calls) holds the device buffers.
+    """
+    if chunk_rows is None:
+        chunk_rows = int(hX.shape[0])
+    if hX.is_cuda or hy.is_cuda:
+        raise ValueError("hX and hy must be host tensors")
+    if hX.dtype != torch.bfloat16 or hy.dtype != torch.int32 or hX.dim() != 2 or hy.dim() != 1:
+        raise TypeError("hX must be bf16 [T, H] and hy int32 [T]")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    T, H = hX.shape
+    st = staging if staging is not None else {}
+    if st.get("shape") != (T, H, entropy) or st.get("device") != dev:
+        st.clear()
+        st.update(shape=(T, H, entropy), device=dev,
+                  X=torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                  y=torch.empty(T, dtype=torch.int32, device=dev),
+                  out={"logp": torch.empty(T, dtype=torch.float32, device=dev),
+                       "lse": torch.empty(T, dtype=torch.float32, device=dev),
+                       "entropy": torch.empty(T, dtype=torch.float32, device=dev) if entropy else None},
+                  host={k: torch.empty(T, dtype=torch.float32, pin_memory=True)
+                        for k in (("logp", "lse", "entropy") if entropy else ("logp", "lse"))},
+                  copy_stream=torch.cuda.Stream(device=dev))
+        with torch.cuda.device(dev):
+            st["ws"] = torch.empty(max(1, lp_workspace_size(LP_OP_FORWARD, min(T, chunk_rows), H, part)),
+                                   dtype=torch.uint8, device=dev)
+    compute = torch.cuda.current_stream(dev)
+    copy = st["copy_stream"]
+    bounds = [(r0, min(T, r0 + chunk_rows)) for r0 in range(0, T, chunk_rows)]
+    ready = []
+    copy.wait_stream(compute)          # the previous call's reads of the staging buffers are done
+    with torch.cuda.stream(copy):
+        for r0, r1 in bounds:
+            st["X"][r0:r1].copy_(hX[r0:r1], non_blocking=True)
+            st["y"][r0:r1].copy_(hy[r0:r1], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy)
+            ready.append(ev)
+    with torch.cuda.device(dev):
+        for (r0, r1), ev in zip(bounds, ready):
+            compute.wait_event(ev)
+            o = {k: (v[r0:r1] if v is not None else None) for k, v in st["out"].items()}
+            lp_forward(st["X"][r0:r1], W, bias, part, st["y"][r0:r1], tau, entropy=entropy,
+                       workspace=st["ws"], out=o)
+        for k, h in st["host"].items():
+            h.copy_(st["out"][k], non_blocking=True)
+    compute.synchronize()
+    return dict(st["host"])
+
