@@ -27,6 +27,8 @@
  *    A shard may be empty (vocab_start == vocab_end).
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and never synchronises, except lp_get_device_error().
+ *  - T = 0 (an empty batch) succeeds without work and without reading any tensor
+ *    pointer; lp_backward then still writes zeros into dW and db.
  *  - Results are bitwise deterministic run to run and batch invariant: a row's
  *    outputs depend only on that row's inputs, never on T or on the row's
  *    position. Reductions over the vocabulary follow a fixed order that

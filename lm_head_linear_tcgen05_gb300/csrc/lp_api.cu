@@ -142,7 +142,9 @@ lp_status check_partition(const lp_vocab_partition* part, Shards* sh) {
   return LP_OK;
 }
 
-bool valid_rows(int64_t T) { return T >= 1 && T <= (int64_t(1) << 30); }
+// T = 0 (an empty batch) is valid: the call succeeds without touching any pointer,
+// except lp_backward, which still zeroes dW and db (the gradient of an empty sum).
+bool valid_rows(int64_t T) { return T >= 0 && T <= (int64_t(1) << 30); }
 bool valid_hidden(int64_t H) { return H >= 8 && H <= 65536 && H % 8 == 0; }
 bool valid_tau(float tau) { return std::isfinite(tau) && tau > 0.f; }
 
@@ -198,8 +200,10 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
                      void* workspace, size_t ws_bytes, lp_stream_t stream) {
   Shards sh;
   if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T) || !valid_hidden(H) || !valid_tau(tau)) return LP_ERR_INVALID_ARG;
+  if (T == 0) return LP_OK;
   if (X == nullptr || W == nullptr || y == nullptr || out == nullptr || out->logp == nullptr ||
-      out->lse == nullptr || !valid_rows(T) || !valid_hidden(H) || !valid_tau(tau))
+      out->lse == nullptr)
     return LP_ERR_INVALID_ARG;
   for (int k = 0; k < sh.n; ++k)
     if (sh.real[k] > 0 && W[k] == nullptr) return LP_ERR_INVALID_ARG;
@@ -283,8 +287,10 @@ lp_status lp_forward_from_logits(const void* const* logits, const int64_t* ld, i
   (void)ws_bytes;
   Shards sh;
   if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T) || !valid_tau(tau)) return LP_ERR_INVALID_ARG;
+  if (T == 0) return LP_OK;
   if (logits == nullptr || ld == nullptr || y == nullptr || out == nullptr || out->logp == nullptr ||
-      out->lse == nullptr || !valid_rows(T) || !valid_tau(tau))
+      out->lse == nullptr)
     return LP_ERR_INVALID_ARG;
   for (int k = 0; k < sh.n; ++k) {
     if (sh.real[k] == 0) continue;
@@ -323,8 +329,10 @@ static lp_status replay_common(const void* X, int64_t T, int64_t H, const void* 
                                const lp_vocab_partition* part, const int32_t* y, float tau, const lp_outputs* out,
                                Shards* sh, ReplayParams* p, DeviceState** dev) {
   if (check_partition(part, sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T) || !valid_hidden(H) || !valid_tau(tau)) return LP_ERR_INVALID_ARG;
+  if (T == 0) return LP_OK;  // callers check T before using the filled parameters
   if (X == nullptr || W == nullptr || y == nullptr || out == nullptr || out->logp == nullptr ||
-      out->lse == nullptr || out->entropy != nullptr || !valid_rows(T) || !valid_hidden(H) || !valid_tau(tau))
+      out->lse == nullptr || out->entropy != nullptr)
     return LP_ERR_INVALID_ARG;
   for (int k = 0; k < sh->n; ++k) {
     if (sh->real[k] == 0) continue;
@@ -360,12 +368,12 @@ lp_status lp_top_p_replay(const void* X, int64_t T, int64_t H, const void* const
                           const lp_outputs* out, void* workspace, size_t ws_bytes, lp_stream_t stream) {
   (void)workspace;
   (void)ws_bytes;
-  if (replay_ids == nullptr) return LP_ERR_INVALID_ARG;
   Shards sh;
   ReplayParams p;
   DeviceState* dev = nullptr;
   lp_status st = replay_common(X, T, H, W, bias, part, y, tau, out, &sh, &p, &dev);
-  if (st != LP_OK) return st;
+  if (st != LP_OK || T == 0) return st;
+  if (replay_ids == nullptr) return LP_ERR_INVALID_ARG;
   p.ids = replay_ids;
   if (launch_replay(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
   return LP_OK;
@@ -379,8 +387,10 @@ lp_status lp_top_p_replay_from_logits(const void* const* logits, const int64_t* 
   (void)ws_bytes;
   Shards sh;
   if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T) || !valid_tau(tau)) return LP_ERR_INVALID_ARG;
+  if (T == 0) return LP_OK;
   if (logits == nullptr || ld == nullptr || replay_ids == nullptr || y == nullptr || out == nullptr ||
-      out->logp == nullptr || out->lse == nullptr || out->entropy != nullptr || !valid_rows(T) || !valid_tau(tau))
+      out->logp == nullptr || out->lse == nullptr || out->entropy != nullptr)
     return LP_ERR_INVALID_ARG;
   for (int k = 0; k < sh.n; ++k)
     if (sh.real[k] > 0 && (logits[k] == nullptr || ld[k] < sh.width[k])) return LP_ERR_INVALID_ARG;
@@ -413,17 +423,15 @@ lp_status lp_top_p_replay_dense_mask(const void* X, int64_t T, int64_t H, const 
                                      const void* const* bias, const lp_vocab_partition* part,
                                      const uint8_t* const* keep_mask, const int32_t* y, float tau,
                                      const lp_outputs* out, void* workspace, size_t ws_bytes, lp_stream_t stream) {
-  if (keep_mask == nullptr) return LP_ERR_INVALID_ARG;
   Shards sh;
   ReplayParams p;
   DeviceState* dev = nullptr;
-  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  lp_status st = replay_common(X, T, H, W, bias, part, y, tau, out, &sh, &p, &dev);
+  if (st != LP_OK || T == 0) return st;
+  if (keep_mask == nullptr) return LP_ERR_INVALID_ARG;
   for (int k = 0; k < sh.n; ++k)
     if (sh.real[k] > 0 && keep_mask[k] == nullptr) return LP_ERR_INVALID_ARG;
-  if (!valid_rows(T)) return LP_ERR_INVALID_ARG;
   const size_t need = align_up(size_t(T) * LP_REPLAY_SLOTS * sizeof(int32_t), 256);
-  lp_status st = replay_common(X, T, H, W, bias, part, y, tau, out, &sh, &p, &dev);
-  if (st != LP_OK) return st;
   if (workspace == nullptr || ws_bytes < need) return LP_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return LP_ERR_ALIGNMENT;
   MaskParams mp;
@@ -451,8 +459,23 @@ lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W,
                       float* const* dW, float* const* db, void* workspace, size_t ws_bytes, lp_stream_t stream) {
   Shards sh;
   if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T) || !valid_hidden(H) || !valid_tau(tau) || dW == nullptr) return LP_ERR_INVALID_ARG;
+  if (T == 0) {
+    // the gradient of an empty sum: dW and db are zero, dX has no rows
+    for (int k = 0; k < sh.n; ++k)
+      if (sh.width[k] > 0 && (dW[k] == nullptr || (db != nullptr && db[k] == nullptr))) return LP_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    lp_status st = device_state(&dev);
+    if (st != LP_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int k = 0; k < sh.n; ++k) {
+      if (sh.width[k] == 0) continue;
+      if (cudaMemsetAsync(dW[k], 0, size_t(sh.width[k]) * size_t(H) * 4, s) != cudaSuccess) return LP_ERR_CUDA;
+      if (db != nullptr && cudaMemsetAsync(db[k], 0, size_t(sh.width[k]) * 4, s) != cudaSuccess) return LP_ERR_CUDA;
+    }
+    return LP_OK;
+  }
   if (X == nullptr || W == nullptr || y == nullptr || lse == nullptr || grad_logp == nullptr || dX == nullptr ||
-      dW == nullptr || !valid_rows(T) || !valid_hidden(H) || !valid_tau(tau) ||
       ((entropy == nullptr) != (grad_entropy == nullptr)))
     return LP_ERR_INVALID_ARG;
   for (int k = 0; k < sh.n; ++k) {

@@ -32,7 +32,7 @@ extern "C" LP_API lp_status lp_forward_noalloc(const void* X, int64_t T, int64_t
                                                const int32_t* y, float tau, const lp_outputs* out,
                                                lp_stream_t stream) {
   const size_t need = lp_workspace_size(LP_OP_FORWARD, T, H, part);
-  if (need == 0)  // invalid sizes or partition: let lp_forward report which
+  if (need == 0)  // an empty batch, or invalid sizes / partition: lp_forward handles both
     return lp_forward(X, T, H, W, bias, part, y, tau, out, nullptr, 0, stream);
   if (need > size_t(LP_NOALLOC_SCRATCH_BYTES)) return LP_ERR_WORKSPACE_TOO_SMALL;
 

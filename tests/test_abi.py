@@ -97,7 +97,9 @@ def test_host_validation_rejects_before_any_launch(lp):
 
     assert call(X=None) == 1
     assert call(H=250) == 1                                  # H % 8 != 0
-    assert call(T=0) == 1
+    assert call(T=-1) == 1
+    assert call(T=0, X=None, y=None, W=[None], logp=None, lse=None, ws=None, wsb=0) == 0   # empty batch: no work
+    assert call(T=0, tau=0.0) == 1                           # scalars are still checked
     assert call(tau=0.0) == 1
     assert call(tau=float("nan")) == 1
     assert call(tau=-1.0) == 1

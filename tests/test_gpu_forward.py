@@ -141,3 +141,63 @@ def test_target_out_of_range_is_a_device_error(lp):
     assert np.all(np.isfinite(np.delete(lg, [3, 5])))
     assert not np.any(np.isnan(_np(out["lse"])))
     assert lp.lp_get_device_error() == 0          # cleared by the read
+
+
+def test_empty_batch_is_a_no_op(lp):
+    import torch
+    part = synth.even_partition(1000, 2)
+    P = part_of(part)
+    X = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    W = [torch.zeros((500, 64), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    y = torch.empty(0, dtype=torch.int32, device="cuda")
+    out = lp.lp_forward(X, W, None, P, y, 0.7)
+    assert out["logp"].numel() == 0
+    g = torch.empty(0, dtype=torch.float32, device="cuda")
+    bw = lp.lp_backward(X, W, None, P, y, 0.7, out["lse"], g)
+    assert all(torch.count_nonzero(d) == 0 for d in bw["dW"]) and all(torch.count_nonzero(d) == 0 for d in bw["db"])
+    ids = torch.empty((0, 64), dtype=torch.int32, device="cuda")
+    assert lp.lp_top_p_replay(X, W, None, P, ids, y, 0.7)["lse"].numel() == 0
+    assert lp.lp_get_device_error() == 0
+
+
+def test_single_real_id(lp):
+    # one real id, the rest padding: every row has logp = 0, LSE = z, entropy = 0
+    part = synth.ranges_partition(1, 300, [0, 1, 300])
+    inp = synth.forward_inputs(5, 64, part, tau=0.7, seed=8, w_std=0.3, bias_std=0.2)
+    inp.y[:] = 0
+    out = _run(lp, inp, shard_stats=True)
+    ref = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau)
+    assert np.all(np.abs(_np(out["logp"])) <= 1e-6)      # 0 up to the base-2 rescaling rounding
+    assert max_abs(_np(out["lse"]), ref.lse) <= TOL_LSE
+    assert np.all(np.abs(_np(out["entropy"])) <= 1e-6)
+    ss = _np(out["shard_stats"])
+    assert np.all(np.isneginf(ss[1, 0])) and np.all(ss[1, 1] == 0)     # the all-padding shard is empty
+
+
+@pytest.mark.parametrize("tau", [0.05, 20.0])
+def test_extreme_temperatures(lp, tau):
+    part = synth.ranges_partition(3000, 3072, [0, 1500, 3072])
+    inp = synth.forward_inputs(130, 128, part, tau=tau, seed=9, w_std=0.05, bias_std=0.1)
+    out = _run(lp, inp)
+    ref = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau)
+    # logits scale as 1/tau: the absolute tolerance applies to z-sized quantities
+    scale = max(1.0, 1.0 / tau)
+    assert max_abs(_np(out["logp"]), ref.logp) <= TOL_LOGP * scale
+    assert max_abs(_np(out["lse"]), ref.lse) <= TOL_LSE * scale
+    assert max_abs(_np(out["entropy"]), ref.entropy) <= TOL_ENT * scale
+
+
+def test_largest_hidden_size(lp):
+    # H = 65536, the largest the library accepts (the replay stages x in 128 KB of shared memory)
+    part = synth.even_partition(600, 2)
+    inp = synth.forward_inputs(3, 65536, part, tau=0.7, seed=10, w_std=0.004)
+    out = _run(lp, inp)
+    ref = oracle.forward(inp.X, inp.W, None, part, inp.y, inp.tau)
+    assert max_abs(_np(out["logp"]), ref.logp) <= TOL_LOGP
+    assert max_abs(_np(out["entropy"]), ref.entropy) <= TOL_ENT
+    ids, yr = synth.replay_ids(3, part, seed=11)
+    X, W, _, _ = dev_inputs(inp)
+    rep = lp.lp_top_p_replay(X, W, None, part_of(part), dev_i32(ids), dev_i32(yr), inp.tau)
+    rref = oracle.top_p_replay(inp.X, inp.W, None, part, ids, yr, inp.tau)
+    assert lp.lp_get_device_error() == 0
+    assert max_abs(_np(rep["lse"]), rref.lse) <= TOL_LSE
