@@ -210,6 +210,12 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
   if (!aligned16(X) || !aligned16(workspace)) return LP_ERR_ALIGNMENT;
   for (int k = 0; k < sh.n; ++k)
     if (sh.real[k] > 0 && !aligned16(W[k])) return LP_ERR_ALIGNMENT;
+  {
+    // tiles are counted in 32-bit integers on the device
+    int64_t nb_total = 0;
+    for (int k = 0; k < sh.n; ++k) nb_total += (sh.real[k] + kFwdBlockN - 1) / kFwdBlockN;
+    if (nb_total * ((T + kFwdBlockM - 1) / kFwdBlockM + kFwdClusterM) > int64_t(INT32_MAX)) return LP_ERR_INVALID_ARG;
+  }
   const size_t need = forward_ws_bytes(T, sh);
   if (workspace == nullptr || ws_bytes < need) return LP_ERR_WORKSPACE_TOO_SMALL;
 
@@ -485,6 +491,12 @@ lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W,
     if ((sh.real[k] > 0 && !aligned16(W[k])) || !aligned16(dW[k])) return LP_ERR_ALIGNMENT;
   }
   if (!aligned16(X) || !aligned16(dX) || !aligned16(workspace)) return LP_ERR_ALIGNMENT;
+  {
+    // tiles are counted in 32-bit integers on the device
+    int64_t nb_total = 0;
+    for (int k = 0; k < sh.n; ++k) nb_total += (sh.real[k] + kFwdBlockN - 1) / kFwdBlockN;
+    if (nb_total * ((T + kFwdBlockM - 1) / kFwdBlockM + kFwdClusterM) > int64_t(INT32_MAX)) return LP_ERR_INVALID_ARG;
+  }
   const size_t need = backward_ws_bytes(T, H, sh);
   if (workspace == nullptr || ws_bytes < need) return LP_ERR_WORKSPACE_TOO_SMALL;
   DeviceState* dev = nullptr;

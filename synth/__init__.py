@@ -147,11 +147,13 @@ def replay_ids(T: int, part: Partition, seed: int = 0, max_ids: int = REPLAY_SLO
     y = np.empty(T, dtype=np.int32)
     V = part.vocab_real
     for t in range(T):
-        c = int(rng.integers(1, max_ids + 1))
+        c = min(int(rng.integers(1, max_ids + 1)), V)
         excluded = None
         if part.n_shards > 1 and rng.random() < empty_shard_frac:
             k = int(rng.integers(0, part.n_shards))
-            excluded = part.ranges[k]
+            lo, hi = min(part.ranges[k][0], V), min(part.ranges[k][1], V)
+            if V - (hi - lo) > 0:          # never exclude every real id
+                excluded = part.ranges[k]
         # the nucleus is ranks 1..c of the Zipf ranking; which vocabulary ids those
         # ranks are is the per-row random permutation drawn here
         if excluded is None:

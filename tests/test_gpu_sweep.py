@@ -1,0 +1,113 @@
+"""Seeded random sweep: small configurations drawn at random (rows, hidden size, shard
+layout with empty and all-padding shards, bias on/off, temperature) through every entry
+point, each compared with the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from lp_util import (TOL_ENT, TOL_GRAD_REL, TOL_LOGP, TOL_LSE, dev_bf16, dev_f32, dev_i32, dev_inputs, max_abs,
+                     part_of, rel_fro)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lp():
+    from lm_head_linear_tcgen05_gb300 import _build
+    _build.build()
+    import lm_head_linear_tcgen05_gb300 as mod
+    import torch
+    assert mod.lp_device_supported()
+    torch.cuda.set_device(0)
+    return mod
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _random_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    T = int(rng.integers(1, 400))
+    H = int(rng.choice([8, 16, 64, 72, 136, 256, 520]))
+    n = int(rng.integers(1, 6))
+    vpad = int(rng.integers(n * 8, 3000)) // 8 * 8
+    cuts = np.sort(rng.choice(np.arange(0, vpad + 1, 8), size=n - 1, replace=True))   # empty shards allowed
+    bounds = [0] + [int(c) for c in cuts] + [vpad]
+    vreal = int(rng.integers(1, vpad + 1))
+    bias = None if rng.random() < 0.5 else float(rng.choice([0.05, 0.5]))
+    tau = float(rng.choice([0.3, 0.7, 1.0, 2.5]))
+    return T, H, bounds, vreal, vpad, bias, tau
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_configuration_all_entry_points(lp, seed):
+    import torch
+    T, H, bounds, vreal, vpad, bias, tau = _random_case(seed)
+    part = synth.ranges_partition(vreal, vpad, bounds)
+    inp = synth.forward_inputs(T, H, part, tau=tau, seed=seed, w_std=0.5 / np.sqrt(H), bias_std=bias)
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    ctx = f"T={T} H={H} bounds={bounds} real={vreal} bias={bias} tau={tau}"
+
+    fwd = lp.lp_forward(X, W, b, P, y, inp.tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0, ctx
+    ref = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau)
+    assert max_abs(_np(fwd["logp"]), ref.logp) <= TOL_LOGP, ctx
+    assert max_abs(_np(fwd["lse"]), ref.lse) <= TOL_LSE, ctx
+    assert max_abs(_np(fwd["entropy"]), ref.entropy) <= TOL_ENT, ctx
+    ss = _np(fwd["shard_stats"])
+    for k, s in enumerate(ref.shards):
+        assert max_abs(ss[k, 0], s.lse) <= TOL_LSE, ctx
+        assert max_abs(ss[k, 1], s.t) <= TOL_LOGP, ctx
+
+    # the same logits, materialised and reused (unscaled, row stride padded to 8)
+    z = oracle.logits_from_bits(inp.X, inp.W, inp.bias, part, 1.0)       # X W^T + b, real ids
+    Lbits = []
+    for k, (s, e) in enumerate(part.ranges):
+        w = e - s
+        full = np.zeros((T, w), np.float32)
+        hi = min(e, vreal)
+        if hi > s:
+            full[:, :hi - s] = z[:, s:hi]
+        Lbits.append(synth.bf16_bits(full))
+    Ld = []
+    for a in Lbits:
+        w = a.shape[1]
+        if w == 0:
+            Ld.append(None)
+            continue
+        buf = torch.zeros((T, (w + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")
+        buf[:, :w] = dev_bf16(a)
+        Ld.append(buf[:, :w])
+    lg = lp.lp_forward_from_logits(Ld, P, y, inp.tau)
+    lref = oracle.forward_from_logits(Lbits, part, inp.y, inp.tau)
+    assert lp.lp_get_device_error() == 0, ctx
+    assert max_abs(_np(lg["lse"]), lref.lse) <= TOL_LSE, ctx
+    assert max_abs(_np(lg["entropy"]), lref.entropy) <= TOL_ENT, ctx
+
+    # replay, both score sources
+    ids, yr = synth.replay_ids(T, part, seed=seed)
+    rp = lp.lp_top_p_replay(X, W, b, P, dev_i32(ids), dev_i32(yr), inp.tau)
+    rref = oracle.top_p_replay(inp.X, inp.W, inp.bias, part, ids, yr, inp.tau)
+    assert lp.lp_get_device_error() == 0, ctx
+    assert max_abs(_np(rp["lse"]), rref.lse) <= TOL_LSE, ctx
+    assert max_abs(_np(rp["logp"]), rref.logp) <= TOL_LOGP, ctx
+    rq = lp.lp_top_p_replay_from_logits(Ld, P, dev_i32(ids), dev_i32(yr), inp.tau)
+    qref = oracle.top_p_replay_from_logits(Lbits, part, ids, yr, inp.tau)
+    assert max_abs(_np(rq["lse"]), qref.lse) <= TOL_LSE, ctx
+
+    # backward with the entropy term
+    g = synth.upstream_grad(T, seed=seed)
+    h = synth.upstream_grad(T, seed=seed + 50)
+    bw = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], dev_f32(g), entropy=fwd["entropy"],
+                        grad_entropy=dev_f32(h))
+    assert lp.lp_get_device_error() == 0, ctx
+    bref = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g, h=h)
+    assert rel_fro(_np(bw["dX"]), bref.dX) <= TOL_GRAD_REL, ctx
+    for k, (s, e) in enumerate(part.ranges):
+        if e == s:
+            continue
+        assert rel_fro(_np(bw["dW"][k]), bref.dW[k]) <= TOL_GRAD_REL, (ctx, k)
+        assert rel_fro(_np(bw["db"][k]), bref.db[k]) <= TOL_GRAD_REL, (ctx, k)
