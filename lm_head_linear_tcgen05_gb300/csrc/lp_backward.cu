@@ -181,7 +181,8 @@ struct GradEpi : GemmEpiBase {
     return j;
   }
 
-  static __device__ __forceinline__ void run(const Params& p, int tile, uint32_t tbase, int q, int lane) {
+  static __device__ __forceinline__ void run(const Params& p, int tile, int /*half*/, uint32_t tbase, int q,
+                                             int lane) {
     const Coord c = coord(p, tile);
     const int row = c.mb * kGemmBlockM + q * 32 + lane;
     const int64_t n0 = int64_t(c.nb_local) * kGemmBlockN;
@@ -311,7 +312,8 @@ struct DwEpi : GemmEpiBase {
     return j;
   }
 
-  static __device__ __forceinline__ void run(const Params& p, int tile, uint32_t tbase, int q, int lane) {
+  static __device__ __forceinline__ void run(const Params& p, int tile, int /*half*/, uint32_t tbase, int q,
+                                             int lane) {
     const Coord c = coord(p, tile);
     const int64_t h = int64_t(c.mb) * kGemmBlockM + q * 32 + lane;
     const int64_t v0 = int64_t(c.nb_local) * kGemmBlockN;
@@ -334,12 +336,14 @@ struct DwEpi : GemmEpiBase {
 };
 
 // ------------------------------------------------------------------- dX
-// Tile = (row block of T, column block of H, K range s). Within a K range, row blocks
-// go in groups of kDxGroupM: inside a group the row block runs fastest, then the column
-// block, so the tiles in flight at once (about 152) cover ~16 row blocks x ~9 column
-// blocks, and both operands' K slices are shared through L2 by many tiles. A = G
-// (K-major, K = global column), B = W_k read MN-major from the shard holding each K
-// block; partial s goes to out + s*T*H.
+// Tile = (block of 256 rows of T, column block of H, K range s): each CTA accumulates
+// two 128-row halves into all 512 TMEM columns (the K loop over a ~38K-long range dwarfs
+// the epilogue, so no second accumulator is needed), which halves the A-tile loads per
+// FLOP and doubles the output each wave of tiles covers. Within a K range, row blocks go
+// in groups of kDxGroupM: inside a group the row block runs fastest, then the column
+// block, so the tiles in flight share both operands' K slices through L2. A = G (K-major,
+// K = global column), B = W_k read MN-major from the shard holding each K block; partial
+// s goes to out + s*T*H.
 struct DxParams {
   CUtensorMap maps[kGemmMaps];  // [0] G [T, Vc] (boxes 64 v x 128 t); [1 + k] W_k [real_k, H] (64 h x 64 v)
   uint32_t keep_maps;
@@ -360,12 +364,14 @@ struct DxEpi : GemmEpiBase {
   using Params = DxParams;
   static constexpr int kClusterM = kFwdClusterM;
   static constexpr bool kBMN = true;
+  static constexpr int kMHalves = 2;  // 256-row tiles: the K loop (a K range of ~38K) dwarfs the epilogue
+  static constexpr int kRows = kMHalves * kGemmBlockM;
 
   struct Coord {
     int mb, nb, s;
   };
 
-  static constexpr int kDxGroupM = 16;  // even, so cluster pairs never straddle groups
+  static constexpr int kDxGroupM = 8;  // row blocks of 256 per group; even, so cluster pairs never straddle groups
 
   static __device__ __forceinline__ Coord coord(const Params& p, int tile) {
     Coord c;
@@ -385,7 +391,7 @@ struct DxEpi : GemmEpiBase {
     const Coord c = coord(p, tile);
     TileJob j;
     j.a_map = 0;
-    j.a_y = c.mb * kGemmBlockM;
+    j.a_y = c.mb * kRows;
     j.b_map = 1;
     j.b_y = c.nb * kGemmBlockN;
     j.kb0 = c.s * p.kb_per_split;
@@ -404,9 +410,10 @@ struct DxEpi : GemmEpiBase {
     k = int(col - p.coff[s]);
   }
 
-  static __device__ __forceinline__ void run(const Params& p, int tile, uint32_t tbase, int q, int lane) {
+  static __device__ __forceinline__ void run(const Params& p, int tile, int half, uint32_t tbase, int q,
+                                             int lane) {
     const Coord c = coord(p, tile);
-    const int64_t row = int64_t(c.mb) * kGemmBlockM + q * 32 + lane;
+    const int64_t row = int64_t(c.mb) * kRows + half * kGemmBlockM + q * 32 + lane;
     const bool ok = row < p.T;
     float* dst = p.out + size_t(c.s) * size_t(p.T) * size_t(p.H) + size_t(ok ? row : 0) * size_t(p.H);
     const int64_t c0 = int64_t(c.nb) * kGemmBlockN;
@@ -533,7 +540,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     for (int k = 0; k <= sh.n; ++k) p.coff[k] = L.coff[k];
     p.keep_maps = 0u;
     p.n_shards = sh.n;
-    p.num_m_blocks = pad_to_cluster((T + kFwdBlockM - 1) / kFwdBlockM);
+    p.num_m_blocks = pad_to_cluster((T + DxEpi::kRows - 1) / DxEpi::kRows);
     p.num_n = int32_t((H + kFwdBlockN - 1) / kFwdBlockN);
     p.nkb_total = int32_t(L.Vc / kFwdBlockK);
     p.kb_per_split = (p.nkb_total + L.split - 1) / L.split;

@@ -117,7 +117,8 @@ struct LogpEpi : GemmEpiBase {
     return j;
   }
 
-  static __device__ __forceinline__ void run(const Params& p, int tile, uint32_t tbase, int q, int lane) {
+  static __device__ __forceinline__ void run(const Params& p, int tile, int /*half*/, uint32_t tbase, int q,
+                                             int lane) {
     const TileCoord c = fwd_coord(p, tile);
     const int row = c.mb * kGemmBlockM + q * 32 + lane;
     const int64_t n0 = int64_t(c.nb_local) * kGemmBlockN;

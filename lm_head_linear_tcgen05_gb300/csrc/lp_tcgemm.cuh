@@ -36,10 +36,12 @@
 //                              reused, loaded with an L2 evict-last hint),
 //                              `int total_tiles` (a multiple of kClusterM),
 //                              `unsigned int* err`, `uint64_t wait_limit_ns`;
+//   kMHalves                              1, or 2 for 256-row tiles (see GemmShape)
 //   static TileJob E::job(const Params&, int tile);
-//   static void E::run(const Params&, int tile, uint32_t tmem_row_base, int quarter, int lane);
-// `tmem_row_base` addresses column 0 of the tile's accumulator at this warp's first
-// lane; column c of this thread's row is at tmem_row_base + c. Boxes: K-major A 64 x 128,
+//   static void E::run(const Params&, int tile, int half, uint32_t tmem_row_base, int quarter, int lane);
+// `tmem_row_base` addresses column 0 of the accumulator of rows [128 half, 128 half + 128)
+// of the tile at this warp's first lane; column c of this thread's row is at
+// tmem_row_base + c. Boxes: K-major A 64 x 128,
 // K-major B 64 x 256 (64 x 128 with kClusterM = 2: each CTA loads half), MN-major
 // operands 64 x 64 atoms (with kClusterM = 2 each CTA loads half of B's atoms).
 #pragma once
@@ -53,14 +55,13 @@ namespace lp {
 constexpr int kGemmBlockM = kFwdBlockM;
 constexpr int kGemmBlockN = kFwdBlockN;
 constexpr int kGemmBlockK = kFwdBlockK;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int kGemmStages = 4;
+constexpr int kGemmMaxStages = 4;
 constexpr int kGemmThreads = 192;
 constexpr int kGemmTmemCols = 512;
 constexpr int kGemmMaps = LP_MAX_SHARDS + 1;
 
-constexpr uint32_t kGemmStageA = kGemmBlockM * kGemmBlockK * 2;  // 16 KB
+constexpr uint32_t kGemmStageA = kGemmBlockM * kGemmBlockK * 2;  // 16 KB per 128-row half
 constexpr uint32_t kGemmStageB = kGemmBlockN * kGemmBlockK * 2;  // 32 KB
-constexpr uint32_t kGemmStageBytes = kGemmStageA + kGemmStageB;
 
 constexpr uint32_t kMNAtomBytes = 64 * kGemmBlockK * 2;  // 64 MN elements x 64 K rows: 8 KB
 
@@ -78,6 +79,7 @@ struct TileJob {
 struct GemmEpiBase {
   static constexpr bool kAMN = false;  // A operand MN-major
   static constexpr bool kBMN = false;  // B operand MN-major
+  static constexpr int kMHalves = 1;   // 128-row halves per CTA tile (2: 256 rows, single accumulator)
   static __device__ __forceinline__ void a_k(const void*, const TileJob& j, int kb, int& map, int& k) {
     map = j.a_map;
     k = (j.kb0 + kb) * kFwdBlockK;
@@ -89,8 +91,8 @@ struct GemmEpiBase {
 };
 
 struct GemmSync {
-  uint64_t full[kGemmStages];
-  uint64_t empty[kGemmStages];
+  uint64_t full[kGemmMaxStages];
+  uint64_t empty[kGemmMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t done;
@@ -98,17 +100,35 @@ struct GemmSync {
   int abort;
 };
 
-constexpr size_t kGemmSmemBytes = 1024 + size_t(kGemmStages) * kGemmStageBytes + sizeof(GemmSync);
+// Ring geometry of an epilogue type: 4 stages of 48 KB for 128-row tiles (two TMEM
+// accumulators, so the epilogue of one tile overlaps the MMAs of the next), or 3 stages
+// of 64 KB for 256-row tiles (both halves fill all 512 TMEM columns: meant for tiles
+// whose K loop is long enough that the epilogue gap does not matter).
+template <class E>
+struct GemmShape {
+  static constexpr int kMH = E::kMHalves;
+  static_assert(kMH == 1 || kMH == 2, "one or two 128-row halves");
+  static constexpr int kStages = kMH == 1 ? 4 : 3;
+  static constexpr uint32_t kStageA = kMH * kGemmStageA;
+  static constexpr uint32_t kStageBytes = kStageA + kGemmStageB;
+  static constexpr int kAcc = kMH == 1 ? 2 : 1;  // accumulators in flight
+  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + sizeof(GemmSync);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 template <class E>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ typename E::Params p) {
   constexpr int kCM = E::kClusterM;
   static_assert(kCM == 1 || kCM == 2, "cluster of one or two CTAs along M");
+  using S = GemmShape<E>;
+  constexpr int kGemmStages = S::kStages;
+  constexpr int kMH = S::kMH;
+  static_assert(kMH == 1 || !E::kAMN, "256-row tiles take a K-major A operand");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kGemmStages * kGemmStageA;
-  GemmSync* sync = reinterpret_cast<GemmSync*>(smem + kGemmStages * kGemmStageBytes);
+  uint8_t* sB = smem + kGemmStages * S::kStageA;
+  GemmSync* sync = reinterpret_cast<GemmSync*>(smem + kGemmStages * S::kStageBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -163,11 +183,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           int am, ak, bm, bk;
           E::a_k(&p, j, kb, am, ak);
           E::b_k(&p, j, kb, bm, bk);
-          mbar_arrive_expect_tx(&sync->full[stage], kGemmStageBytes);
-          uint8_t* dA = sA + stage * kGemmStageA;
+          mbar_arrive_expect_tx(&sync->full[stage], S::kStageBytes);
+          uint8_t* dA = sA + stage * S::kStageA;
           uint8_t* dB = sB + stage * kGemmStageB;
           if constexpr (!E::kAMN) {
-            tma_load_2d(dA, &p.maps[am], &sync->full[stage], ak, j.a_y, pa);
+#pragma unroll
+            for (int h = 0; h < kMH; ++h)
+              tma_load_2d(dA + h * kGemmStageA, &p.maps[am], &sync->full[stage], ak, j.a_y + h * kGemmBlockM, pa);
           } else {  // MN-major: 64-element atoms of 64 K rows each
 #pragma unroll
             for (int i = 0; i < kGemmBlockM / 64; ++i)
@@ -217,20 +239,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         const TileJob j = E::job(p, ct * kCM + int(rank));
         if (!mbar_wait(&sync->tempty[acc], acc_phase ^ 1u, abort, p.wait_limit_ns, p.err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * kGemmBlockN;
+        const uint32_t d_tmem = tmem + acc * kGemmBlockN;  // half h at + h * kGemmBlockN
         for (int kb = 0; kb < j.nkb; ++kb) {
           if (!mbar_wait(&sync->full[stage], phase, abort, p.wait_limit_ns, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t aa = smem_u32(sA + stage * kGemmStageA);
+          const uint32_t aa = smem_u32(sA + stage * S::kStageA);
           const uint32_t ba = smem_u32(sB + stage * kGemmStageB);
-          const uint64_t a_desc = E::kAMN ? sw128_mnmajor_desc(aa, kMNAtomBytes) : sw128_kmajor_desc(aa);
           const uint64_t b_desc = E::kBMN ? sw128_mnmajor_desc(ba, kMNAtomBytes) : sw128_kmajor_desc(ba);
 #pragma unroll
-          for (int k = 0; k < kGemmBlockK / 16; ++k)
-            umma_bf16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int h = 0; h < kMH; ++h) {
+            const uint32_t ah = aa + h * kGemmStageA;
+            const uint64_t a_desc = E::kAMN ? sw128_mnmajor_desc(ah, kMNAtomBytes) : sw128_kmajor_desc(ah);
+#pragma unroll
+            for (int k = 0; k < kGemmBlockK / 16; ++k)
+              umma_bf16(d_tmem + h * kGemmBlockN, a_desc + a_step * k, b_desc + b_step * k, idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          }
           if constexpr (kCM == 2)
             umma_commit_multicast(&sync->empty[stage], uint16_t(0x3));
           else
@@ -242,8 +269,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         }
         if (!ok) break;
         umma_commit(&sync->tfull[acc]);
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == uint32_t(S::kAcc)) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       umma_commit(&sync->done);
       drain_wait(&sync->done, 0, p.wait_limit_ns);
@@ -257,12 +286,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       if (!__all_sync(0xffffffffu, mbar_wait(&sync->tfull[acc], acc_phase, abort, p.wait_limit_ns, p.err)))
         break;
       tc_fence_after();
-      E::run(p, ct * kCM + int(rank), tmem + (uint32_t(q * 32) << 16) + acc * kGemmBlockN, q, lane);
+#pragma unroll 1
+      for (int h = 0; h < kMH; ++h)
+        E::run(p, ct * kCM + int(rank), h, tmem + (uint32_t(q * 32) << 16) + (acc + h) * kGemmBlockN, q, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sync->tempty[acc]);
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == uint32_t(S::kAcc)) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
 
@@ -289,8 +322,8 @@ int gemm_clusters_for_device(int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   int c = cache[dev].load(std::memory_order_acquire);
   if (c != 0) return c;
-  if (cudaFuncSetAttribute(tc_gemm_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemmSmemBytes)) !=
-      cudaSuccess) {
+  if (cudaFuncSetAttribute(tc_gemm_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(GemmShape<E>::kSmemBytes)) != cudaSuccess) {
     cudaGetLastError();
     return -1;
   }
@@ -305,7 +338,7 @@ int gemm_clusters_for_device(int num_sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = kGemmSmemBytes;
+    cfg.dynamicSmemBytes = GemmShape<E>::kSmemBytes;
     cfg.gridDim = dim3(kCM * clusters, 1, 1);
     int active = 0;
     if (cudaOccupancyMaxActiveClusters(&active, tc_gemm_kernel<E>, &cfg) == cudaSuccess && active > 0 &&
@@ -321,7 +354,6 @@ int gemm_clusters_for_device(int num_sms) {
 // Launches one CTA per SM (rounded to whole clusters) over p.total_tiles tiles.
 template <class E>
 cudaError_t launch_tc_gemm(const typename E::Params& p, int num_sms, cudaStream_t s) {
-  static_assert(kGemmSmemBytes <= 232448, "shared memory budget");
   constexpr int kCM = E::kClusterM;
   int clusters = gemm_clusters_for_device<E>(num_sms);
   if (clusters < 0) return cudaErrorInvalidConfiguration;
@@ -331,7 +363,7 @@ cudaError_t launch_tc_gemm(const typename E::Params& p, int num_sms, cudaStream_
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.dynamicSmemBytes = GemmShape<E>::kSmemBytes;
   cfg.stream = s;
   cfg.gridDim = dim3(kCM * clusters, 1, 1);
   if (kCM > 1) {
