@@ -72,7 +72,7 @@ typedef enum {
   LP_ERR_REPLAY_ID_OUT_OF_RANGE = 6, /* device: a replay id not in {-1} U [0, vocab_real) */
   LP_ERR_DEVICE_TIMEOUT = 7,       /* device: a pipeline wait ran past its limit */
   LP_ERR_CUDA = 8,                 /* a CUDA runtime call failed */
-  LP_ERR_REPLAY_TOO_MANY_IDS = 9   /* device: a keep-mask row kept more than 64 ids */
+  LP_ERR_REPLAY_TOO_MANY_IDS = 9   /* device: a keep-mask row kept more than 64 ids (row fails closed) */
 } lp_status;
 
 typedef enum {

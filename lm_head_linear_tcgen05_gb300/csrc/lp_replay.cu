@@ -211,7 +211,9 @@ __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const __grid_con
 
 // Dense keep-mask route: one CTA (256 threads) per row scans the masks of all shards
 // in ascending id order and writes the kept real ids, ascending, into canonical
-// replay slots (-1 padded). More than 64 kept ids in a row is a device error.
+// replay slots (-1 padded). More than 64 kept ids in a row is a device error, and the
+// row fails closed: its first slot is overwritten with an out-of-range id, so the
+// replay kernel reports LSE = logp = -inf for it.
 __global__ void __launch_bounds__(256) mask_compact_kernel(const __grid_constant__ MaskParams p) {
   __shared__ int warp_counts[8];
   __shared__ int base_s;
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(256) mask_compact_kernel(const __grid_constant
       __syncthreads();
     }
   }
+  if (tid == 0 && base_s > LP_REPLAY_SLOTS) out[0] = INT32_MIN;
 }
 
 cudaError_t launch_replay(const ReplayParams& p, cudaStream_t s) {
