@@ -451,3 +451,40 @@ def backward_sampled(X_bits, W_bits, b_bits, part, y, tau, g, dx_rows, dw_rows):
         dW.append(G.T @ Xd)
         db.append(G.sum(axis=0))
     return dX, dW, db
+
+
+def backward_from_logits(L_bits, part, y, tau, g, h=None, rows=None) -> List[np.ndarray]:
+    """Gradient of sum_t g_t logp_t (+ sum_t h_t entropy_t) of ``forward_from_logits`` with
+    respect to the reused unscaled logits L_k (the route that avoids a second projection).
+
+    z = L / tau, so dL = G with G[t,v] = (g_t (1[v = y_t] - p_tv) - h_t p_tv (z_tv - mu_t)) / tau
+    on real ids and 0 on padded ids, exactly the G of ``backward_f64``. Returns one float64
+    [T, V_k] array per shard (``rows`` selects rows of L, y, g and h).
+    """
+    sel = slice(None) if rows is None else np.asarray(rows)
+    yy = np.asarray(y, dtype=np.int64)[sel]
+    gg = np.asarray(g, dtype=np.float64)[sel]
+    T = yy.shape[0]
+    z = np.empty((T, part.vocab_real), dtype=np.float64)
+    for k, (vs, ve) in enumerate(part.ranges):
+        hi = min(ve, part.vocab_real)
+        if hi > vs:
+            z[:, vs:hi] = bf16_to_f64(L_bits[k][sel][:, : hi - vs]) / tau
+    M = z.max(axis=1, keepdims=True)
+    p = np.exp(z - M)
+    p /= p.sum(axis=1, keepdims=True)
+    G = -p
+    G[np.arange(T), yy] += 1.0
+    G *= (gg / tau)[:, None]
+    if h is not None:
+        hh = np.asarray(h, dtype=np.float64)[sel]
+        mu = (p * z).sum(axis=1, keepdims=True)
+        G -= (hh / tau)[:, None] * p * (z - mu)
+    out = []
+    for k, (vs, ve) in enumerate(part.ranges):
+        dL = np.zeros((T, ve - vs))
+        hi = min(ve, part.vocab_real)
+        if hi > vs:
+            dL[:, : hi - vs] = G[:, vs:hi]
+        out.append(dL)
+    return out

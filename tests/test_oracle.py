@@ -467,3 +467,81 @@ def test_entropy_gradient_of_uniform_logits_vanishes():
     a = oracle.backward(X, W, None, part, np.array([1, 2]), 0.7, g)
     b = oracle.backward(X, W, None, part, np.array([1, 2]), 0.7, g, h=np.array([3.0, 7.0]))
     np.testing.assert_allclose(b.db[0], a.db[0], atol=1e-15)
+
+
+# ------------------------------------------------------------ logits gradient
+
+def _real_concat(L_bits, part):
+    cols = []
+    for k, (vs, ve) in enumerate(part.ranges):
+        hi = min(ve, part.vocab_real)
+        if hi > vs:
+            cols.append(oracle.bf16_to_f64(L_bits[k][:, : hi - vs]))
+    return np.concatenate(cols, axis=1)
+
+
+def test_logits_gradient_matches_torch_autograd_fp64():
+    # independent library: torch's log_softmax and autograd in float64 on the CPU
+    torch = pytest.importorskip("torch")
+    part = synth.ranges_partition(90, 104, [0, 40, 40, 104])        # an empty shard, 14 padded ids
+    T, tau = 6, 0.7
+    L, y, _ = synth.logits_inputs(T, part, tau, seed=21)
+    g = synth.upstream_grad(T, seed=21)
+    h = synth.upstream_grad(T, seed=22)
+    z = torch.tensor(_real_concat(L, part), dtype=torch.float64, requires_grad=True)
+    ls = torch.log_softmax(z / tau, dim=1)
+    logp = ls[torch.arange(T), torch.tensor(y, dtype=torch.long)]
+    ent = -(ls.exp() * ls).sum(dim=1)
+    loss = (torch.tensor(g, dtype=torch.float64) * logp).sum() + (torch.tensor(h, dtype=torch.float64) * ent).sum()
+    loss.backward()
+    ref = z.grad.numpy()
+    dL = oracle.backward_from_logits(L, part, y, tau, g, h=h)
+    assert [d.shape for d in dL] == [(T, 40), (T, 0), (T, 64)]
+    np.testing.assert_allclose(np.concatenate([dL[0], dL[2][:, :50]], axis=1), ref, rtol=1e-10, atol=1e-13)
+    assert np.all(dL[2][:, 50:] == 0)                                  # padded ids
+    # logp term alone
+    dL0 = oracle.backward_from_logits(L, part, y, tau, g)
+    z.grad = None
+    ls = torch.log_softmax(z / tau, dim=1)
+    (torch.tensor(g, dtype=torch.float64) * ls[torch.arange(T), torch.tensor(y, dtype=torch.long)]).sum().backward()
+    np.testing.assert_allclose(np.concatenate([dL0[0], dL0[2][:, :50]], axis=1), z.grad.numpy(), rtol=1e-10,
+                               atol=1e-13)
+
+
+def test_logits_gradient_rows_sum_to_zero_and_rows_select():
+    part = synth.even_partition(500, 3, 510)
+    T, tau = 9, 1.3
+    L, y, _ = synth.logits_inputs(T, part, tau, seed=23)
+    g = synth.upstream_grad(T, seed=23)
+    h = synth.upstream_grad(T, seed=24)
+    dL = oracle.backward_from_logits(L, part, y, tau, g, h=h)
+    row_sum = sum(d.sum(axis=1) for d in dL)
+    assert np.max(np.abs(row_sum)) < 1e-14
+    rows = np.array([7, 2, 5])
+    sub = oracle.backward_from_logits(L, part, y, tau, g, h=h, rows=rows)
+    for a, b in zip(sub, dL):
+        np.testing.assert_array_equal(a, b[rows])
+
+
+def test_logits_gradient_chain_rule_to_projection_gradient():
+    # With small-integer X and W the logits X W^T are integers, exact in bf16, so the
+    # logits gradient must carry the projection gradient through L = X W^T:
+    # dX = sum_k dL_k W_k, dW_k = dL_k^T X, db_k = sum_t dL_k.
+    part = synth.ranges_partition(70, 80, [0, 30, 80])
+    rng = np.random.default_rng(25)
+    T, H, tau = 5, 6, 2.5
+    Xi = rng.integers(-2, 3, size=(T, H)).astype(np.float32)
+    Wi = [rng.integers(-2, 3, size=(e - s, H)).astype(np.float32) for s, e in part.ranges]
+    X = synth.bf16_bits(Xi)
+    W = [synth.bf16_bits(w) for w in Wi]
+    L = [synth.bf16_bits(Xi @ w.T) for w in Wi]
+    y = np.array([0, 69, 31, 29, 12])
+    g = synth.upstream_grad(T, seed=25)
+    h = synth.upstream_grad(T, seed=26)
+    ref = oracle.backward(X, W, [np.zeros(e - s, np.uint16) for s, e in part.ranges], part, y, tau, g, h=h)
+    dL = oracle.backward_from_logits(L, part, y, tau, g, h=h)
+    dX = sum(d @ w.astype(np.float64) for d, w in zip(dL, Wi))
+    np.testing.assert_allclose(dX, ref.dX, rtol=1e-12, atol=1e-14)
+    for k in range(2):
+        np.testing.assert_allclose(dL[k].T @ Xi.astype(np.float64), ref.dW[k], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(dL[k].sum(axis=0), ref.db[k], rtol=1e-12, atol=1e-14)
