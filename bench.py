@@ -5,8 +5,9 @@
 Headline (one JSON line on rank 0): the fused forward on the Qwen3-8B-shaped LM head,
 T=4096 rows, H=4096, V=151936 bf16, tau=0.7, logp + LSE + entropy, in tokens/s, with
 the tensor-core roofline of the fused GEMM kernel. The other hot-path rows are timed
-alongside in "paths": logits reuse (T=8192 x 151936 bf16 logits, HBM-bound), compact
-top-p replay (T=8192, 4 shards), and the vocabulary-sharded forward + backward
+alongside in "paths": logits reuse (T=8192 x 151936 bf16 logits, HBM-bound) and the
+gradient with respect to those logits, compact top-p replay (T=8192, 4 shards), and the
+vocabulary-sharded forward + backward
 (T=4096, V=151936 padded to 152064 in 4 shards, bias).
 
 Every input is synthetic and seeded; the weights and logits are larger than the
@@ -56,8 +57,9 @@ def load_peaks():
 # device sources each timed kernel is compiled from
 KERNEL_SOURCES = {
     "fused_forward": ("lp_fused_forward.cu", "lp_tcgemm.cuh", "lp_device.cuh"),
-    "stream_logits": ("lp_stream.cu", "lp_device.cuh"),
+    "stream_logits": ("lp_stream.cu", "lp_device.cuh", "lp_f32x2.cuh"),
     "replay": ("lp_replay.cu", "lp_device.cuh"),
+    "logits_backward": ("lp_logits_backward.cu", "lp_device.cuh", "lp_f32x2.cuh"),
 }
 
 
@@ -298,6 +300,22 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
                              "traffic": stored_traffic("stream_logits")}}
+            # its backward: the gradient with respect to those logits, bf16, out of place
+            fl = lp.lp_forward_from_logits(L, P, y, TAU)
+            gl = torch.randn(8192, generator=torch.Generator(device=dev).manual_seed(4), device=dev)
+            dL = [torch.empty_like(L[0])]
+            ms = time_steps(lambda: lp.lp_backward_from_logits(L, P, y, TAU, fl["lse"], gl, entropy=fl["entropy"],
+                                                               grad_entropy=gl, out=dL),
+                            args.steps, args.warmup, stream)
+            nbytes = 2 * 8192 * Vp * 2
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out["logits_backward"] = {
+                "workload": f"gradient w.r.t. the T=8192 x V={Vp} logits above (logp + entropy terms), bf16 out",
+                "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
+                             "traffic": stored_traffic("logits_backward")}}
+            del dL, fl
         if "replay" in wanted:
             # the compact replay scored from the reused logits above (one 2-byte gather per id)
             L4 = [L[0][:, s:e] for s, e in part4.ranges]

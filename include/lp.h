@@ -80,8 +80,15 @@ typedef enum {
   LP_OP_FORWARD_FROM_LOGITS = 1,
   LP_OP_TOP_P_REPLAY = 2,
   LP_OP_BACKWARD = 3,
-  LP_OP_TOP_P_REPLAY_DENSE_MASK = 4
+  LP_OP_TOP_P_REPLAY_DENSE_MASK = 4,
+  LP_OP_BACKWARD_FROM_LOGITS = 5   /* needs no workspace */
 } lp_op;
+
+/* Element type of an output buffer whose type the caller chooses. */
+typedef enum {
+  LP_DTYPE_F32 = 0,
+  LP_DTYPE_BF16 = 1   /* the fp32 result rounded to nearest, ties to even */
+} lp_dtype;
 
 /* Global id range [vocab_start, vocab_end) of one shard. */
 typedef struct {
@@ -198,6 +205,61 @@ LP_API lp_status lp_backward(const void* X, int64_t T, int64_t H,
                       const float* entropy, const float* grad_entropy,
                       float* dX, float* const* dW, float* const* db,
                       void* workspace, size_t ws_bytes, lp_stream_t stream);
+
+/* Output options of lp_backward_ex (page "feat(rl-kernel): add CUDA linear logp
+ * provider integration", Changes / Megatron integration: the provider sits inside a
+ * Megatron loss path, whose hidden-state gradients are bf16 and whose weight
+ * gradients accumulate into fp32 buffers across micro-batches).
+ *   dx_dtype    LP_DTYPE_F32: dX is float [T,H]; LP_DTYPE_BF16: dX is bf16 [T,H]
+ *               holding the same fp32 sum rounded once to bf16.
+ *   accumulate  0: dW[k] and db[k] are overwritten; 1: the gradient is added to what
+ *               they hold (one fp32 add per element after the fixed-order sum, so the
+ *               result is still deterministic); padded ids keep their old values and
+ *               an empty batch leaves both untouched. dX is always overwritten. */
+typedef struct {
+  int32_t dx_dtype;
+  int32_t accumulate;
+} lp_backward_options;
+
+/* lp_backward with output options; opts NULL means {LP_DTYPE_F32, 0}, which makes it
+ * identical to lp_backward. dX points to float or bf16 per opts->dx_dtype (16-byte
+ * aligned either way). Same workspace (LP_OP_BACKWARD) and errors as lp_backward,
+ * plus LP_ERR_INVALID_ARG for an unknown dx_dtype or accumulate not 0/1. */
+LP_API lp_status lp_backward_ex(const void* X, int64_t T, int64_t H,
+                                const void* const* W, const void* const* bias,
+                                const lp_vocab_partition* part, const int32_t* y, float tau,
+                                const float* lse, const float* grad_logp,
+                                const float* entropy, const float* grad_entropy,
+                                void* dX, float* const* dW, float* const* db,
+                                const lp_backward_options* opts,
+                                void* workspace, size_t ws_bytes, lp_stream_t stream);
+
+/* Backward of the logits-reuse route (page "feat(rl-kernel): add CUDA linear logp
+ * provider integration", Megatron integration: local logits are reused instead of a
+ * second projection, so gradients flow back through them): the gradient of
+ * sum_t grad_logp[t] logp[t] (+ sum_t grad_entropy[t] entropy[t]) of
+ * lp_forward_from_logits with respect to the unscaled logits L_k. Since z = L / tau,
+ *   dlogits[k][t, v - vocab_start_k] = G[t,v]
+ *       = (grad_logp[t] (1[v == y_t] - p_tv) - grad_entropy[t] p_tv (z_tv - mu_t)) / tau
+ * with p = exp(z - lse), mu = lse - entropy, and 0 on padded ids (the G of lp_backward).
+ *   logits, ld  as lp_forward_from_logits (bf16, row stride ld[k] % 8 == 0)
+ *   lse         the merged LSE of lp_forward_from_logits on the same logits
+ *   entropy, grad_entropy   both NULL (logp term only) or both given
+ *   dlogits     host array [n_shards] of device pointers: shard k [T, V_k] with row
+ *               stride ld_out[k] elements, of type out_dtype (bf16: ld_out % 8 == 0;
+ *               f32: ld_out % 4 == 0). dlogits[k] may be logits[k] itself (bf16,
+ *               ld_out[k] == ld[k]): every element is read before it is overwritten
+ *               by the same thread. Other overlaps are not allowed.
+ * Rows whose lse or grad_logp is not finite, or whose target is out of range, get a
+ * zero gradient (as in lp_backward; the forward has already reported a bad target).
+ * Logits of -inf (entries a caller masked out) get a zero gradient. Streams the
+ * logits once and writes the gradient once; needs no workspace. */
+LP_API lp_status lp_backward_from_logits(const void* const* logits, const int64_t* ld, int64_t T,
+                                         const lp_vocab_partition* part, const int32_t* y, float tau,
+                                         const float* lse, const float* grad_logp,
+                                         const float* entropy, const float* grad_entropy,
+                                         void* const* dlogits, const int64_t* ld_out, lp_dtype out_dtype,
+                                         lp_stream_t stream);
 
 /* Fused forward that allocates nothing. The paper has no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory at all - a plugin

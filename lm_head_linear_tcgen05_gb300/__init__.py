@@ -48,11 +48,17 @@ LP_OP_FORWARD_FROM_LOGITS = 1
 LP_OP_TOP_P_REPLAY = 2
 LP_OP_BACKWARD = 3
 LP_OP_TOP_P_REPLAY_DENSE_MASK = 4
+LP_OP_BACKWARD_FROM_LOGITS = 5
+
+LP_DTYPE_F32 = 0
+LP_DTYPE_BF16 = 1
+_LP_DTYPES = {torch.float32: LP_DTYPE_F32, torch.bfloat16: LP_DTYPE_BF16}
 
 # every symbol include/lp.h declares
 EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
-            "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward", "lp_get_device_error",
-            "lp_selftest_wait_timeout", "lp_device_supported", "lp_status_string")
+            "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward", "lp_backward_ex",
+            "lp_backward_from_logits", "lp_get_device_error", "lp_selftest_wait_timeout", "lp_device_supported",
+            "lp_status_string")
 
 
 class LPError(RuntimeError):
@@ -90,6 +96,10 @@ class _Outputs(ctypes.Structure):
                 ("entropy", ctypes.c_void_p), ("shard_stats", ctypes.c_void_p)]
 
 
+class _BackwardOptions(ctypes.Structure):
+    _fields_ = [("dx_dtype", ctypes.c_int32), ("accumulate", ctypes.c_int32)]
+
+
 _lib = None
 
 
@@ -116,6 +126,10 @@ def lib() -> ctypes.CDLL:
                                              P(_Outputs), vp, sz, vp]
     L.lp_backward.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, vp, vp, vp, vp, vp, P(vp),
                               P(vp), vp, sz, vp]
+    L.lp_backward_ex.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, vp, vp, vp, vp, vp, P(vp),
+                                 P(vp), P(_BackwardOptions), vp, sz, vp]
+    L.lp_backward_from_logits.argtypes = [P(vp), P(i64), i64, P(_Partition), vp, f32, vp, vp, vp, vp, P(vp),
+                                          P(i64), ctypes.c_int, vp]
     L.lp_get_device_error.argtypes = [vp]
     L.lp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     L.lp_device_supported.argtypes = []
@@ -123,7 +137,8 @@ def lib() -> ctypes.CDLL:
     L.lp_status_string.restype = ctypes.c_char_p
     for name in ("lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
                  "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask",
-                 "lp_backward", "lp_get_device_error", "lp_selftest_wait_timeout", "lp_device_supported"):
+                 "lp_backward", "lp_backward_ex", "lp_backward_from_logits", "lp_get_device_error",
+                 "lp_selftest_wait_timeout", "lp_device_supported"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -382,13 +397,8 @@ def lp_top_p_replay_dense_mask(X: torch.Tensor, W, bias, part, keep_mask: Sequen
     return o
 
 
-def lp_backward(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse: torch.Tensor,
-                grad_logp: torch.Tensor, bias_grad: bool = True,
-                workspace: Optional[torch.Tensor] = None, entropy: Optional[torch.Tensor] = None,
-                grad_entropy: Optional[torch.Tensor] = None) -> dict:
-    """Backward of sum_t grad_logp[t] logp[t] (+ sum_t grad_entropy[t] entropy[t]): returns
-    fp32 dX [T,H], dW (per shard [V_k,H]), db (per shard [V_k], or None). `lse` and
-    `entropy` are the merged outputs of lp_forward."""
+def _backward(fn: str, X: torch.Tensor, W, bias, part, y, tau, lse, grad_logp, bias_grad, workspace, entropy,
+              grad_entropy, dx_dtype, accumulate, dW, db) -> dict:
     _check(X, "X", torch.bfloat16, 2)
     _check(y, "y", torch.int32, 1)
     _check(lse, "lse", torch.float32, 1)
@@ -398,26 +408,114 @@ def lp_backward(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse
     if entropy is not None:
         _check(entropy, "entropy", torch.float32, 1)
         _check(grad_entropy, "grad_entropy", torch.float32, 1)
+    if dx_dtype not in _LP_DTYPES:
+        raise TypeError("dx_dtype must be torch.float32 or torch.bfloat16")
     n = len(part.ranges)
     W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
     bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
     T, H = X.shape
+    widths = [e - s for s, e in part.ranges]
+    if accumulate and (dW is None or (bias_grad and db is None)):
+        raise ValueError("accumulate=True adds into the caller's dW (and db): pass them")
+    if dW is not None:
+        dW = _shard_list(dW, n, "dW", torch.float32, 2, True)
+        for k, (t, w) in enumerate(zip(dW, widths)):
+            if w and (t is None or tuple(t.shape) != (w, H)):
+                raise ValueError(f"dW[{k}] must be fp32 [{w}, {H}]")
+    if db is not None:
+        db = _shard_list(db, n, "db", torch.float32, 1, True)
+        for k, (t, w) in enumerate(zip(db, widths)):
+            if w and (t is None or t.shape[0] != w):
+                raise ValueError(f"db[{k}] must be fp32 [{w}]")
     cp, _keep = _c_partition(part)
     with torch.cuda.device(X.device):
         need = lp_workspace_size(LP_OP_BACKWARD, T, H, part)
         ws, wsb = _workspace(need, X.device, workspace)
-        dX = torch.empty((T, H), dtype=torch.float32, device=X.device)
-        dW = [torch.empty((e - s, H), dtype=torch.float32, device=X.device) if e > s else None
-              for s, e in part.ranges]
-        db = [torch.empty(e - s, dtype=torch.float32, device=X.device) if e > s else None
-              for s, e in part.ranges] if bias_grad else None
-        st = lib().lp_backward(X.data_ptr(), T, H, _ptr_array(W), _ptr_array(bias) if bias is not None else None,
-                               ctypes.byref(cp), y.data_ptr(), float(tau), lse.data_ptr(), grad_logp.data_ptr(),
-                               _ptr(entropy), _ptr(grad_entropy),
-                               dX.data_ptr(), _ptr_array(dW), _ptr_array(db) if db is not None else None,
-                               _ptr(ws), wsb, _stream(X.device))
-    _raise(st, "lp_backward")
+        dX = torch.empty((T, H), dtype=dx_dtype, device=X.device)
+        if dW is None:
+            dW = [torch.empty((w, H), dtype=torch.float32, device=X.device) if w else None for w in widths]
+        if db is None and bias_grad:
+            db = [torch.empty(w, dtype=torch.float32, device=X.device) if w else None for w in widths]
+        if not bias_grad:
+            db = None
+        args = [X.data_ptr(), T, H, _ptr_array(W), _ptr_array(bias) if bias is not None else None,
+                ctypes.byref(cp), y.data_ptr(), float(tau), lse.data_ptr(), grad_logp.data_ptr(),
+                _ptr(entropy), _ptr(grad_entropy), dX.data_ptr(), _ptr_array(dW),
+                _ptr_array(db) if db is not None else None]
+        if fn == "lp_backward_ex":
+            opts = _BackwardOptions(_LP_DTYPES[dx_dtype], 1 if accumulate else 0)
+            args.append(ctypes.byref(opts))
+        st = getattr(lib(), fn)(*args, _ptr(ws), wsb, _stream(X.device))
+    _raise(st, fn)
     return {"dX": dX, "dW": dW, "db": db}
+
+
+def lp_backward(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse: torch.Tensor,
+                grad_logp: torch.Tensor, bias_grad: bool = True,
+                workspace: Optional[torch.Tensor] = None, entropy: Optional[torch.Tensor] = None,
+                grad_entropy: Optional[torch.Tensor] = None) -> dict:
+    """Backward of sum_t grad_logp[t] logp[t] (+ sum_t grad_entropy[t] entropy[t]): returns
+    fp32 dX [T,H], dW (per shard [V_k,H]), db (per shard [V_k], or None). `lse` and
+    `entropy` are the merged outputs of lp_forward."""
+    return _backward("lp_backward", X, W, bias, part, y, tau, lse, grad_logp, bias_grad, workspace, entropy,
+                     grad_entropy, torch.float32, False, None, None)
+
+
+def lp_backward_ex(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse: torch.Tensor,
+                   grad_logp: torch.Tensor, bias_grad: bool = True, workspace: Optional[torch.Tensor] = None,
+                   entropy: Optional[torch.Tensor] = None, grad_entropy: Optional[torch.Tensor] = None,
+                   dx_dtype=torch.float32, accumulate: bool = False, dW=None, db=None) -> dict:
+    """lp_backward with output options: ``dx_dtype`` torch.float32 or torch.bfloat16 (the
+    fp32 result rounded once); ``accumulate`` adds the weight and bias gradients into the
+    caller's fp32 ``dW`` / ``db`` lists (otherwise those, when given, are overwritten)."""
+    return _backward("lp_backward_ex", X, W, bias, part, y, tau, lse, grad_logp, bias_grad, workspace, entropy,
+                     grad_entropy, dx_dtype, accumulate, dW, db)
+
+
+def lp_backward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tensor, tau: float, lse: torch.Tensor,
+                            grad_logp: torch.Tensor, entropy: Optional[torch.Tensor] = None,
+                            grad_entropy: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                            out: Optional[Sequence[torch.Tensor]] = None) -> list:
+    """Gradient with respect to the reused unscaled logits of lp_forward_from_logits: one
+    [T, V_k] tensor per shard (None for an empty shard) of ``out_dtype``. ``out`` (optional)
+    gives the destination tensors; ``out=logits`` (bf16) overwrites the logits in place."""
+    _check(y, "y", torch.int32, 1)
+    _check(lse, "lse", torch.float32, 1)
+    _check(grad_logp, "grad_logp", torch.float32, 1)
+    if (entropy is None) != (grad_entropy is None):
+        raise ValueError("entropy and grad_entropy go together")
+    if entropy is not None:
+        _check(entropy, "entropy", torch.float32, 1)
+        _check(grad_entropy, "grad_entropy", torch.float32, 1)
+    if out_dtype not in _LP_DTYPES:
+        raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+    n = len(part.ranges)
+    T = y.shape[0]
+    ld = _logits_ld(logits, n, T)
+    widths = [e - s for s, e in part.ranges]
+    if out is None:
+        # rows padded to a 16-byte multiple (the row rule), handed back as [T, V_k] views
+        per16 = 16 // torch.tensor([], dtype=out_dtype).element_size()
+        out = [torch.empty((T, (w + per16 - 1) // per16 * per16), dtype=out_dtype, device=y.device)[:, :w]
+               if w else None for w in widths]
+    elif len(out) != n:
+        raise ValueError("out must have one entry per shard")
+    ld_out = (ctypes.c_int64 * max(n, 1))()
+    for k, (t, w) in enumerate(zip(out, widths)):
+        if t is None:
+            continue
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == out_dtype and t.dim() == 2):
+            raise TypeError(f"out[{k}] must be a 2-D {out_dtype} CUDA tensor")
+        if t.stride(1) != 1 or tuple(t.shape) != (T, w):
+            raise ValueError(f"out[{k}] must be [T, V_k] with unit column stride")
+        ld_out[k] = t.stride(0)
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(y.device):
+        st = lib().lp_backward_from_logits(_ptr_array(logits), ld, T, ctypes.byref(cp), y.data_ptr(), float(tau),
+                                           lse.data_ptr(), grad_logp.data_ptr(), _ptr(entropy), _ptr(grad_entropy),
+                                           _ptr_array(out), ld_out, _LP_DTYPES[out_dtype], _stream(y.device))
+    _raise(st, "lp_backward_from_logits")
+    return list(out)
 
 
 def lp_forward_host(hX: torch.Tensor, W: Sequence[torch.Tensor], bias, part, hy: torch.Tensor, tau: float,

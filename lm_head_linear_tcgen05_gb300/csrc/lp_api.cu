@@ -191,6 +191,7 @@ size_t lp_workspace_size(lp_op op, int64_t T, int64_t H, const lp_vocab_partitio
     case LP_OP_TOP_P_REPLAY: return 0;
     case LP_OP_TOP_P_REPLAY_DENSE_MASK: return align_up(size_t(T) * LP_REPLAY_SLOTS * sizeof(int32_t), 256);
     case LP_OP_BACKWARD: return valid_hidden(H) ? backward_ws_bytes(T, H, sh) : 0;
+    case LP_OP_BACKWARD_FROM_LOGITS: return 0;
   }
   return 0;
 }
@@ -463,13 +464,29 @@ lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W,
                       const lp_vocab_partition* part, const int32_t* y, float tau, const float* lse,
                       const float* grad_logp, const float* entropy, const float* grad_entropy, float* dX,
                       float* const* dW, float* const* db, void* workspace, size_t ws_bytes, lp_stream_t stream) {
+  return lp_backward_ex(X, T, H, W, bias, part, y, tau, lse, grad_logp, entropy, grad_entropy, dX, dW, db, nullptr,
+                        workspace, ws_bytes, stream);
+}
+
+lp_status lp_backward_ex(const void* X, int64_t T, int64_t H, const void* const* W, const void* const* bias,
+                         const lp_vocab_partition* part, const int32_t* y, float tau, const float* lse,
+                         const float* grad_logp, const float* entropy, const float* grad_entropy, void* dX,
+                         float* const* dW, float* const* db, const lp_backward_options* opts, void* workspace,
+                         size_t ws_bytes, lp_stream_t stream) {
   Shards sh;
   if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
   if (!valid_rows(T) || !valid_hidden(H) || !valid_tau(tau) || dW == nullptr) return LP_ERR_INVALID_ARG;
+  const int dx_bf16 = opts != nullptr && opts->dx_dtype == LP_DTYPE_BF16;
+  const int accumulate = opts != nullptr ? opts->accumulate : 0;
+  if (opts != nullptr && ((opts->dx_dtype != LP_DTYPE_F32 && opts->dx_dtype != LP_DTYPE_BF16) ||
+                          (accumulate != 0 && accumulate != 1)))
+    return LP_ERR_INVALID_ARG;
   if (T == 0) {
-    // the gradient of an empty sum: dW and db are zero, dX has no rows
+    // the gradient of an empty sum: dW and db are zero (or unchanged when accumulating),
+    // dX has no rows
     for (int k = 0; k < sh.n; ++k)
       if (sh.width[k] > 0 && (dW[k] == nullptr || (db != nullptr && db[k] == nullptr))) return LP_ERR_INVALID_ARG;
+    if (accumulate) return LP_OK;
     DeviceState* dev = nullptr;
     lp_status st = device_state(&dev);
     if (st != LP_OK) return st;
@@ -513,6 +530,8 @@ lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W,
   a.entropy = entropy;
   a.grad_entropy = grad_entropy;
   a.dX = dX;
+  a.dx_bf16 = dx_bf16;
+  a.accumulate = accumulate;
   for (int k = 0; k < sh.n; ++k) {
     a.W[k] = W[k];
     a.bias[k] = bias != nullptr ? bias[k] : nullptr;
@@ -523,6 +542,85 @@ lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W,
   a.err = dev->err;
   a.num_sms = dev->num_sms;
   return run_backward(a, sh, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// byte range [lo, hi) spanned by rows of `width` elements of `esz` bytes at stride ld
+struct Span {
+  uintptr_t lo, hi;
+};
+
+static Span row_span(const void* base, int64_t T, int64_t width, int64_t ld, int64_t esz) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(base);
+  return Span{lo, lo + uintptr_t(((T - 1) * ld + width) * esz)};
+}
+
+static bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+
+lp_status lp_backward_from_logits(const void* const* logits, const int64_t* ld, int64_t T,
+                                  const lp_vocab_partition* part, const int32_t* y, float tau, const float* lse,
+                                  const float* grad_logp, const float* entropy, const float* grad_entropy,
+                                  void* const* dlogits, const int64_t* ld_out, lp_dtype out_dtype,
+                                  lp_stream_t stream) {
+  Shards sh;
+  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T) || !valid_tau(tau)) return LP_ERR_INVALID_ARG;
+  if (out_dtype != LP_DTYPE_F32 && out_dtype != LP_DTYPE_BF16) return LP_ERR_INVALID_ARG;
+  if (T == 0) return LP_OK;
+  if (logits == nullptr || ld == nullptr || y == nullptr || lse == nullptr || grad_logp == nullptr ||
+      dlogits == nullptr || ld_out == nullptr || ((entropy == nullptr) != (grad_entropy == nullptr)))
+    return LP_ERR_INVALID_ARG;
+  const bool bf16 = out_dtype == LP_DTYPE_BF16;
+  const int64_t esz = bf16 ? 2 : 4;
+  for (int k = 0; k < sh.n; ++k) {
+    if (sh.width[k] == 0) continue;
+    if (sh.real[k] > 0) {
+      if (logits[k] == nullptr || ld[k] < sh.width[k]) return LP_ERR_INVALID_ARG;
+      if (!aligned16(logits[k]) || ld[k] % 8 != 0) return LP_ERR_ALIGNMENT;
+    }
+    if (dlogits[k] == nullptr || ld_out[k] < sh.width[k]) return LP_ERR_INVALID_ARG;
+    if (!aligned16(dlogits[k]) || ld_out[k] % (16 / esz) != 0) return LP_ERR_ALIGNMENT;
+  }
+  // outputs may not overlap each other, nor any shard's logits except their own shard's
+  // exactly (the in-place form)
+  for (int k = 0; k < sh.n; ++k) {
+    if (sh.width[k] == 0) continue;
+    const Span o = row_span(dlogits[k], T, sh.width[k], ld_out[k], esz);
+    for (int j = 0; j < sh.n; ++j) {
+      if (sh.width[j] == 0) continue;
+      if (j != k && overlap(o, row_span(dlogits[j], T, sh.width[j], ld_out[j], esz))) return LP_ERR_INVALID_ARG;
+      if (sh.real[j] == 0) continue;
+      const bool in_place = j == k && bf16 && dlogits[k] == logits[k] && ld_out[k] == ld[k];
+      if (!in_place && overlap(o, row_span(logits[j], T, sh.width[j], ld[j], 2))) return LP_ERR_INVALID_ARG;
+    }
+  }
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+
+  LogitsGradParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int k = 0; k < sh.n; ++k) {
+    p.logits[k] = static_cast<const __nv_bfloat16*>(logits[k]);
+    p.out[k] = dlogits[k];
+    p.ld[k] = ld[k];
+    p.ld_out[k] = ld_out[k];
+    p.shard_start[k] = sh.start[k];
+    p.width[k] = sh.width[k];
+    p.real[k] = sh.real[k];
+  }
+  p.y = y;
+  p.lse = lse;
+  p.grad = grad_logp;
+  p.entropy = entropy;
+  p.grad_entropy = grad_entropy;
+  p.vocab_real = sh.vocab_real;
+  p.n_shards = sh.n;
+  p.T = int32_t(T);
+  p.out_bf16 = bf16 ? 1 : 0;
+  p.scale_log2 = float(1.4426950408889634 / double(tau));
+  p.inv_tau = float(1.0 / double(tau));
+  if (launch_logits_backward(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
 }
 
 lp_status lp_selftest_wait_timeout(uint64_t limit_ns, lp_stream_t stream) {

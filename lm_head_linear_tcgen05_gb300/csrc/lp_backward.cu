@@ -71,9 +71,11 @@ BwdLayout bwd_layout(int64_t T, int64_t H, const Shards& sh) {
 
 __device__ __forceinline__ float f32(uint32_t r) { return __uint_as_float(r); }
 
-// fp32 dX = sum_s part[s] in ascending s (vectors of 4)
+// dX = sum_s part[s] in ascending s (vectors of 4), stored as fp32, or rounded once to
+// bf16 when kBf16
+template <bool kBf16>
 __global__ void __launch_bounds__(256) reduce_split_kernel(const float4* __restrict__ part, int split, size_t n4,
-                                                            float4* __restrict__ out) {
+                                                            void* __restrict__ out) {
   const size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n4) return;
   float4 acc = part[i];
@@ -84,7 +86,13 @@ __global__ void __launch_bounds__(256) reduce_split_kernel(const float4* __restr
     acc.z = __fadd_rn(acc.z, v.z);
     acc.w = __fadd_rn(acc.w, v.w);
   }
-  out[i] = acc;
+  if (kBf16) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    reinterpret_cast<uint2*>(out)[i] =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  } else {
+    reinterpret_cast<float4*>(out)[i] = acc;
+  }
 }
 
 // part[c][v] = sum over rows t in [128 c, 128 c + 128) of G[t][v], rows in order;
@@ -109,15 +117,19 @@ __global__ void __launch_bounds__(256) db_partial_kernel(const uint16_t* __restr
 }
 
 // db[v] = sum_c part[c][col0 + v] in ascending c for v < real; 0 for real <= v < width.
+// With accumulate the sum is added to db[v] and padded ids keep their value.
 __global__ void __launch_bounds__(256) db_reduce_kernel(const float* __restrict__ part, int64_t Vc, int64_t chunks,
-                                                         int64_t col0, int64_t real, int64_t width,
+                                                         int64_t col0, int64_t real, int64_t width, int accumulate,
                                                          float* __restrict__ db) {
   const int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (v >= width) return;
   float acc = 0.f;
   if (v < real)
     for (int64_t c = 0; c < chunks; ++c) acc = __fadd_rn(acc, part[c * Vc + col0 + v]);
-  db[v] = acc;
+  if (!accumulate)
+    db[v] = acc;
+  else if (v < real)
+    db[v] = __fadd_rn(db[v], acc);
 }
 
 }  // namespace
@@ -276,6 +288,7 @@ struct DwParams {
   int32_t n_shards;
   int32_t num_m_blocks;  // row blocks of H, counted in whole clusters
   int32_t nkb;           // K blocks over T
+  int32_t accumulate;    // dW += G^T X instead of dW = G^T X
   int64_t H;
 };
 
@@ -326,7 +339,20 @@ struct DwEpi : GemmEpiBase {
       if (ch * 32 >= valid) break;
       uint32_t r[32];
       tmem_ld32(tbase + ch * 32, r);
-      if (ok) {
+      if (ok && p.accumulate) {
+        // read-add-write in groups of 8 rows (8 loads in flight, few live registers)
+#pragma unroll
+        for (int j0 = 0; j0 < 32; j0 += 8) {
+          float old[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (ch * 32 + j0 + j < valid) old[j] = base[size_t(ch * 32 + j0 + j) * size_t(p.H)];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (ch * 32 + j0 + j < valid)
+              base[size_t(ch * 32 + j0 + j) * size_t(p.H)] = __fadd_rn(old[j], f32(r[j0 + j]));
+        }
+      } else if (ok) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (ch * 32 + j < valid) base[size_t(ch * 32 + j) * size_t(p.H)] = f32(r[j]);
@@ -350,7 +376,8 @@ struct DxParams {
   int32_t total_tiles;
   unsigned int* err;
   uint64_t wait_limit_ns;
-  float* out;
+  float* out;            // fp32 partial s at out + s*T*H, or (one K range) dX itself
+  uint16_t* out_bf16;    // one K range and bf16 dX: dX rounded in the epilogue (out unused)
   int64_t coff[LP_MAX_SHARDS + 1];
   int32_t n_shards;
   int32_t num_m_blocks;  // row blocks of T, counted in whole clusters
@@ -415,9 +442,33 @@ struct DxEpi : GemmEpiBase {
     const Coord c = coord(p, tile);
     const int64_t row = int64_t(c.mb) * kRows + half * kGemmBlockM + q * 32 + lane;
     const bool ok = row < p.T;
-    float* dst = p.out + size_t(c.s) * size_t(p.T) * size_t(p.H) + size_t(ok ? row : 0) * size_t(p.H);
     const int64_t c0 = int64_t(c.nb) * kGemmBlockN;
     const int64_t cols = p.H - c0 < kGemmBlockN ? p.H - c0 : kGemmBlockN;
+    if (p.out_bf16 != nullptr) {
+      // H % 8 == 0, so 8-column groups are whole: one 16-byte store per group
+      uint16_t* dst = p.out_bf16 + size_t(ok ? row : 0) * size_t(p.H) + size_t(c0);
+#pragma unroll 1
+      for (int ch = 0; ch < kGemmBlockN / 32; ++ch) {
+        if (ch * 32 >= cols) break;
+        uint32_t r[32];
+        tmem_ld32(tbase + ch * 32, r);
+        if (ok) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            if (ch * 32 + v * 8 >= cols) break;
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 b = __floats2bfloat162_rn(f32(r[8 * v + 2 * e]), f32(r[8 * v + 2 * e + 1]));
+              w[e] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            *reinterpret_cast<uint4*>(dst + ch * 32 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      return;
+    }
+    float* dst = p.out + size_t(c.s) * size_t(p.T) * size_t(p.H) + size_t(ok ? row : 0) * size_t(p.H);
 #pragma unroll 1
     for (int ch = 0; ch < kGemmBlockN / 32; ++ch) {
       if (ch * 32 >= cols) break;
@@ -519,10 +570,11 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.nkb = int32_t((T + kFwdBlockK - 1) / kFwdBlockK);
     p.H = H;
     p.total_tiles = nb * p.num_m_blocks;
+    p.accumulate = a.accumulate;
     p.err = a.err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
     if (launch_tc_gemm<DwEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
-    for (int k = 0; k < sh.n; ++k) {
+    for (int k = 0; k < sh.n && !a.accumulate; ++k) {
       const int64_t pad = sh.width[k] - sh.real[k];
       if (pad > 0 && cudaMemsetAsync(a.dW[k] + sh.real[k] * H, 0, size_t(pad) * size_t(H) * 4, s) != cudaSuccess)
         return LP_ERR_CUDA;
@@ -547,15 +599,19 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     const int splits = (p.nkb_total + p.kb_per_split - 1) / p.kb_per_split;
     p.T = T;
     p.H = H;
-    p.out = splits > 1 ? part : a.dX;
+    p.out = splits > 1 ? part : static_cast<float*>(a.dX);
+    p.out_bf16 = (splits == 1 && a.dx_bf16) ? static_cast<uint16_t*>(a.dX) : nullptr;
     p.total_tiles = p.num_m_blocks * p.num_n * splits;
     p.err = a.err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
     if (launch_tc_gemm<DxEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
     if (splits > 1) {
       const size_t n4 = size_t(T) * size_t(H) / 4;
-      reduce_split_kernel<<<unsigned((n4 + 255) / 256), 256, 0, s>>>(reinterpret_cast<const float4*>(part), splits,
-                                                                      n4, reinterpret_cast<float4*>(a.dX));
+      const unsigned blocks = unsigned((n4 + 255) / 256);
+      if (a.dx_bf16)
+        reduce_split_kernel<true><<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(part), splits, n4, a.dX);
+      else
+        reduce_split_kernel<false><<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(part), splits, n4, a.dX);
       if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
     }
   }
@@ -572,7 +628,8 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     for (int k = 0; k < sh.n; ++k) {
       if (a.db[k] == nullptr || sh.width[k] == 0) continue;
       db_reduce_kernel<<<unsigned((sh.width[k] + 255) / 256), 256, 0, s>>>(dbp, L.Vc, L.db_chunks, L.coff[k],
-                                                                           sh.real[k], sh.width[k], a.db[k]);
+                                                                           sh.real[k], sh.width[k], a.accumulate,
+                                                                           a.db[k]);
       if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
     }
   }

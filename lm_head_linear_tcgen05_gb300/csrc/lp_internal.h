@@ -98,6 +98,28 @@ struct StreamParams {
   float inv_tau;
 };
 
+// Gradient with respect to reused logits, one CTA per row.
+struct LogitsGradParams {
+  const __nv_bfloat16* logits[LP_MAX_SHARDS];
+  void* out[LP_MAX_SHARDS];              // bf16 or fp32 [T, width], row stride ld_out
+  int64_t ld[LP_MAX_SHARDS];
+  int64_t ld_out[LP_MAX_SHARDS];
+  int64_t shard_start[LP_MAX_SHARDS];
+  int64_t width[LP_MAX_SHARDS];          // all columns of the shard (padded ids included)
+  int64_t real[LP_MAX_SHARDS];           // columns below vocab_real
+  const int32_t* y;
+  const float* lse;
+  const float* grad;
+  const float* entropy;                  // with grad_entropy, else NULL
+  const float* grad_entropy;
+  int64_t vocab_real;
+  int32_t n_shards;
+  int32_t T;
+  int32_t out_bf16;
+  float scale_log2;                      // log2(e) / tau
+  float inv_tau;
+};
+
 // Compact top-p replay, one CTA per row. Scores come from x . W[v] + b[v] (X, W, bias)
 // or, in the logits-gather variant, from reused unscaled logits (logits, ld).
 struct ReplayParams {
@@ -143,7 +165,9 @@ struct BackwardArgs {
   const float* grad;
   const float* entropy;       // with grad_entropy: the forward's entropy, else NULL
   const float* grad_entropy;  // upstream gradient of the entropy, or NULL
-  float* dX;
+  void* dX;                   // float or bf16 [T, H] (dx_bf16)
+  int dx_bf16;
+  int accumulate;             // add into dW and db instead of overwriting them
   const void* W[LP_MAX_SHARDS];
   const void* bias[LP_MAX_SHARDS];
   float* dW[LP_MAX_SHARDS];
@@ -167,5 +191,6 @@ cudaError_t launch_stream_logits(const StreamParams& p, cudaStream_t s);
 cudaError_t launch_replay(const ReplayParams& p, cudaStream_t s);
 cudaError_t launch_replay_from_logits(const ReplayParams& p, cudaStream_t s);
 cudaError_t launch_mask_compact(const MaskParams& p, cudaStream_t s);
+cudaError_t launch_logits_backward(const LogitsGradParams& p, cudaStream_t s);
 
 }  // namespace lp

@@ -21,6 +21,7 @@
 #include <atomic>
 
 #include "lp_device.cuh"
+#include "lp_f32x2.cuh"
 
 namespace lp {
 
@@ -39,37 +40,6 @@ constexpr int kStreamThreads = 256;
 constexpr int kStreamWarps = kStreamThreads / 32;
 constexpr int kChunkVecs = LP_STREAM_CHUNK_VECS;
 constexpr int kStages = LP_STREAM_STAGES;
-
-// Packed pairs of fp32: the f32x2 instructions of sm_100-family SMs perform two fp32
-// operations per issued instruction.
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
 
 // Per-thread online statistic over raw (unscaled) logits x: the running maximum is
 // tracked on x, m = max(x) * c2 and d = x * c2 - m, so u = x * c2 is never rounded

@@ -134,3 +134,61 @@ def test_device_support_query_without_gpu(lp):
     if _has_gpu():
         pytest.skip("a GPU is present")
     assert lp.lp_device_supported() is False
+
+
+@pytest.mark.skipif(_has_gpu(), reason="uses fake device pointers; only safe without a GPU")
+def test_logits_backward_host_validation(lp):
+    L = lp.lib()
+    A, B = 0x100000, 0x900000          # fake, 16-byte aligned, far apart; never dereferenced on the host
+    p = _part(lp, 90, 96, [0, 48, 96])
+    cp, keep = lp._c_partition(p)
+    T = 4
+    assert lp.lp_workspace_size(lp.LP_OP_BACKWARD_FROM_LOGITS, T, 0, p) == 0
+
+    def call(logits=(A, A + 4096), ld=(48, 48), out=(B, B + 4096), ld_out=(48, 48), dtype=lp.LP_DTYPE_BF16,
+             ent=None, gent=None, T=T, tau=0.7):
+        Lg = (ctypes.c_void_p * 2)(*logits)
+        O = (ctypes.c_void_p * 2)(*out)
+        ldv = (ctypes.c_int64 * 2)(*ld)
+        ldo = (ctypes.c_int64 * 2)(*ld_out)
+        return L.lp_backward_from_logits(Lg, ldv, T, ctypes.byref(cp), A, tau, A, A, ent, gent, O, ldo, dtype, None)
+
+    assert call(dtype=2) == 1                                   # unknown output type
+    assert call(ent=A) == 1                                     # entropy without its gradient
+    assert call(ld=(40, 48)) == 1                               # row stride below the shard width
+    assert call(ld=(52, 48)) == 2                               # row stride not a multiple of 8
+    assert call(out=(B + 8, B + 4096)) == 2                     # misaligned output
+    assert call(ld_out=(52, 48)) == 2                           # bf16 rows need a stride % 8 == 0 ...
+    assert call(dtype=lp.LP_DTYPE_F32, ld_out=(52, 48)) == 3    # ... fp32 rows a stride % 4 == 0
+    assert call(out=(A + 4096, B)) == 1                         # shard 0's output over shard 1's logits
+    assert call(out=(B, B + 16)) == 1                           # outputs overlapping each other
+    assert call(out=(A, A + 4096), dtype=lp.LP_DTYPE_F32) == 1  # fp32 over bf16 logits is not in place
+    assert call(out=(A, A + 4096), ld_out=(56, 48)) == 1        # in place needs the same row stride
+    assert call(out=(A, A + 4096)) == 3                         # in place: valid, reaches the device check
+    assert call(T=0, logits=(None, None), out=(None, None)) == 0   # empty batch: no work
+    assert call(T=0, tau=0.0) == 1
+    assert call() == 3                                          # valid: fails only for want of a GPU
+
+
+@pytest.mark.skipif(_has_gpu(), reason="uses fake device pointers; only safe without a GPU")
+def test_backward_ex_host_validation(lp):
+    L = lp.lib()
+    A = 0x100000
+    p = _part(lp, 1000, 1000, [0, 1000])
+    cp, keep = lp._c_partition(p)
+    ws = lp.lp_workspace_size(lp.LP_OP_BACKWARD, 64, 256, p)
+
+    def call(dx_dtype=0, accumulate=0, T=64, opts=True):
+        Wa = (ctypes.c_void_p * 1)(A)
+        dW = (ctypes.c_void_p * 1)(A)
+        o = lp._BackwardOptions(dx_dtype, accumulate)
+        return L.lp_backward_ex(A, T, 256, Wa, None, ctypes.byref(cp), A, 0.7, A, A, None, None, A, dW, None,
+                                ctypes.byref(o) if opts else None, A, ws, None)
+
+    assert call(dx_dtype=2) == 1
+    assert call(dx_dtype=-1) == 1
+    assert call(accumulate=2) == 1
+    assert call(T=0, accumulate=1) == 0       # empty batch, accumulating: nothing to add, no device needed
+    assert call(T=0) == 3                     # empty batch, overwriting: zeroes dW on the device
+    assert call(dx_dtype=1, accumulate=1) == 3
+    assert call(opts=False) == 3
