@@ -19,7 +19,9 @@
 //      shard's own weight (K = every shard's columns in ascending order), split into
 //      a fixed number of K ranges (a function of the vocabulary only) whose fp32
 //      partials are then summed in ascending order;
-//   4. db_k: column sums of G over fixed 128-row chunks, then over the chunks in order.
+//   4. db_k: the G kernel's epilogue also sums each 32-row slice of every G column (a
+//      fixed butterfly across the warp) into a partial; the partials of a column are then
+//      added in ascending row order.
 // Column layout of G: shard k occupies columns [coff_k, coff_k + real_k) with coff_k a
 // multiple of 64 and zero columns up to coff_{k+1}, so K blocks never straddle shards
 // and padded ids contribute exactly zero.
@@ -34,7 +36,7 @@ namespace lp {
 namespace {
 
 constexpr int kSplitChunkCols = 32768;  // dX splits K into Vc / 32768 ranges (1..8)
-constexpr int kDbRows = 128;            // rows per db partial sum
+constexpr int kDbRows = 32;             // rows per db partial sum (one epilogue warp)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -57,7 +59,9 @@ BwdLayout bwd_layout(int64_t T, int64_t H, const Shards& sh) {
   L.Vc = c;
   int split = int(c / kSplitChunkCols);
   L.split = split < 1 ? 1 : (split > 8 ? 8 : split);
-  L.db_chunks = (T + kDbRows - 1) / kDbRows;
+  // one partial per 32-row warp slice of every 128-row block, blocks counted in whole clusters
+  L.db_chunks = (T + kFwdBlockM * kFwdClusterM - 1) / (kFwdBlockM * kFwdClusterM) * kFwdClusterM *
+                (kFwdBlockM / kDbRows);
   size_t off = 0;
   L.off_g = off;
   off += align_up(size_t(T) * size_t(L.Vc) * 2, 256);
@@ -70,6 +74,36 @@ BwdLayout bwd_layout(int64_t T, int64_t H, const Shards& sh) {
 }
 
 __device__ __forceinline__ float f32(uint32_t r) { return __uint_as_float(r); }
+
+// one 32-byte store (a whole sector per lane); p must be 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Column sums of a 32 x 32 block held one row per lane (v[j] = column j of this lane's
+// row): a butterfly that halves the columns each lane keeps at every step (16, 8, 4, 2,
+// 1 columns exchanged with lane ^ 16, ^ 8, ...), so after 31 shuffles lane l holds the
+// sum of column l over the 32 rows. The order of the additions is fixed.
+__device__ __forceinline__ float warp_column_sum(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int j = 0; j < s; ++j) {
+      const float send = up ? v[j] : v[j + s];
+      const float keep = up ? v[j + s] : v[j];
+      v[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, s));
+    }
+  }
+  return v[0];
+}
 
 // dX = sum_s part[s] in ascending s (vectors of 4), stored as fp32, or rounded once to
 // bf16 when kBf16
@@ -93,27 +127,6 @@ __global__ void __launch_bounds__(256) reduce_split_kernel(const float4* __restr
   } else {
     reinterpret_cast<float4*>(out)[i] = acc;
   }
-}
-
-// part[c][v] = sum over rows t in [128 c, 128 c + 128) of G[t][v], rows in order;
-// each thread owns 8 consecutive columns (one 16-byte vector per row).
-__global__ void __launch_bounds__(256) db_partial_kernel(const uint16_t* __restrict__ G, int64_t Vc, int64_t T,
-                                                          float* __restrict__ part) {
-  const int64_t v8 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-  if (v8 >= Vc) return;
-  const int64_t c = blockIdx.y;
-  const int64_t t0 = c * kDbRows;
-  const int64_t t1 = t0 + kDbRows < T ? t0 + kDbRows : T;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int64_t t = t0; t < t1; ++t) {
-    const uint4 q = *reinterpret_cast<const uint4*>(G + t * Vc + v8);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]));
-  }
-  float4* o = reinterpret_cast<float4*>(part + c * Vc + v8);
-  o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 // db[v] = sum_c part[c][col0 + v] in ascending c for v < real; 0 for real <= v < width.
@@ -148,6 +161,7 @@ struct GradParams {
   const float* entropy;       // or NULL
   const float* grad_entropy;  // or NULL
   uint16_t* G;  // [T][Vc]
+  float* dbp;   // [4 * num_m_blocks][Vc] per-warp column sums of G, or NULL (no bias gradient)
   int64_t Vc;
   int64_t coff[LP_MAX_SHARDS + 1];
   int64_t shard_start[LP_MAX_SHARDS];
@@ -229,43 +243,40 @@ struct GradEpi : GemmEpiBase {
     const __nv_bfloat16* bias = p.bias[c.shard];
     const int64_t col_base = p.coff[c.shard] + n0;
     uint16_t* grow = p.G + size_t(in_rows ? row : 0) * size_t(p.Vc) + size_t(col_base);
+    float* dbrow = p.dbp != nullptr ? p.dbp + (size_t(c.mb) * 4 + size_t(q)) * size_t(p.Vc) + size_t(col_base) : nullptr;
 #pragma unroll 1
     for (int ch = 0; ch < kGemmBlockN / 32; ++ch) {
       if (ch * 32 >= wlim) break;
       float bl = 0.f;
       if (bias != nullptr && ch * 32 + lane < valid) bl = __bfloat162float(bias[n0 + ch * 32 + lane]);
-      uint32_t packed[16];
+      float gv[32];
       if (ch * 32 < valid) {
         uint32_t r[32];
         tmem_ld32(tbase + ch * 32, r);
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float gv[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = ch * 32 + j + h;
-            const float v = __fadd_rn(f32(r[j + h]), __shfl_sync(0xffffffffu, bl, j + h));
-            const float pr = hw_ex2(__fmaf_rn(v, p.scale_log2, -lse2));
-            const float oh = (int64_t(col) == ycol) ? 1.f : 0.f;
-            // logp term g (1[v = y] - p) / tau, entropy term - h p (z - mu) / tau
-            float gval = __fmul_rn(gi, __fsub_rn(oh, pr));
-            if (hi != 0.f) gval = __fsub_rn(gval, __fmul_rn(__fmul_rn(hi, pr), __fsub_rn(__fmul_rn(v, p.inv_tau), mu)));
-            gv[h] = (col < valid && live) ? gval : 0.f;
-          }
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(gv[0], gv[1]);
-          packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+        for (int j = 0; j < 32; ++j) {
+          const int col = ch * 32 + j;
+          const float v = __fadd_rn(f32(r[j]), __shfl_sync(0xffffffffu, bl, j));
+          const float pr = hw_ex2(__fmaf_rn(v, p.scale_log2, -lse2));
+          const float oh = (int64_t(col) == ycol) ? 1.f : 0.f;
+          // logp term g (1[v = y] - p) / tau, entropy term - h p (z - mu) / tau
+          float gval = __fmul_rn(gi, __fsub_rn(oh, pr));
+          if (hi != 0.f) gval = __fsub_rn(gval, __fmul_rn(__fmul_rn(hi, pr), __fsub_rn(__fmul_rn(v, p.inv_tau), mu)));
+          gv[j] = (col < valid && live) ? gval : 0.f;
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) packed[j] = 0u;
+        for (int j = 0; j < 32; ++j) gv[j] = 0.f;
       }
-      if (in_rows) {
-        uint4* dst = reinterpret_cast<uint4*>(grow + ch * 32);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        dst[2] = make_uint4(packed[8], packed[9], packed[10], packed[11]);
-        dst[3] = make_uint4(packed[12], packed[13], packed[14], packed[15]);
+      if (in_rows) {  // 64 bytes of this row: two whole-sector stores
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) packed[j] = pack_bf16(gv[2 * j], gv[2 * j + 1]);
+        st_global_v8(grow + ch * 32, packed);
+        st_global_v8(grow + ch * 32 + 16, packed + 8);
       }
+      // bias gradient: this warp's 32 rows of the chunk's 32 columns, summed in fp32
+      if (dbrow != nullptr) dbrow[ch * 32 + lane] = warp_column_sum(gv, lane);
     }
   }
 };
@@ -542,6 +553,9 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.grad_entropy = a.grad_entropy;
     p.G = G;
     p.Vc = L.Vc;
+    bool any_db = false;
+    for (int k = 0; k < sh.n; ++k) any_db = any_db || (a.db[k] != nullptr && sh.width[k] > 0);
+    p.dbp = any_db ? dbp : nullptr;
     p.vocab_real = sh.vocab_real;
     p.scale_log2 = float(1.4426950408889634 / double(a.tau));
     p.inv_tau = float(1.0 / double(a.tau));
@@ -616,15 +630,8 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     }
   }
 
-  // 4. db
-  bool any_db = false;
-  for (int k = 0; k < sh.n; ++k) any_db = any_db || (a.db[k] != nullptr && sh.width[k] > 0);
-  if (any_db) {
-    dim3 grid(unsigned((L.Vc / 8 + 255) / 256), unsigned(L.db_chunks));
-    if (L.Vc > 0) {
-      db_partial_kernel<<<grid, 256, 0, s>>>(G, L.Vc, T, dbp);
-      if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
-    }
+  // 4. db: the G kernel wrote per-warp column sums; add them in ascending row order
+  {
     for (int k = 0; k < sh.n; ++k) {
       if (a.db[k] == nullptr || sh.width[k] == 0) continue;
       db_reduce_kernel<<<unsigned((sh.width[k] + 255) / 256), 256, 0, s>>>(dbp, L.Vc, L.db_chunks, L.coff[k],
