@@ -18,7 +18,11 @@ constexpr int kFwdBlockK = 64;
 // CTAs per cluster along M in the projection GEMMs (forward and the backward's G):
 // the two row blocks of one vocabulary block share its W box through TMA multicast,
 // so row blocks are counted in pairs and W maps have boxes of kFwdBlockN / 2 rows.
-constexpr int kFwdClusterM = 2;
+// (Four also works - a quarter box each - but fewer four-CTA clusters fit on the chip.)
+#ifndef LP_CLUSTER_M
+#define LP_CLUSTER_M 2
+#endif
+constexpr int kFwdClusterM = LP_CLUSTER_M;
 
 // Validated vocabulary partition (host side).
 struct Shards {

@@ -20,7 +20,7 @@
 // box (128 of its 256 rows) and multicasts it into both CTAs' shared memory, so every
 // SM pulls 32 KB instead of 48 KB per K step through L2. A stage may then be refilled
 // only when both CTAs' MMAs are done with it: each MMA commit arrives on the empty
-// barrier of both CTAs (count 2).
+// barrier of both CTAs (count 2). kClusterM = 4 generalises this to quarter boxes.
 //
 // Every mbarrier wait is bounded in time (see lp_device.cuh): a wait that runs past
 // the limit records LP_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag and every
@@ -119,7 +119,8 @@ struct GemmShape {
 template <class E>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ typename E::Params p) {
   constexpr int kCM = E::kClusterM;
-  static_assert(kCM == 1 || kCM == 2, "cluster of one or two CTAs along M");
+  static_assert(kCM == 1 || kCM == 2 || kCM == 4, "cluster of one, two or four CTAs along M");
+  constexpr uint16_t kCtaMask = uint16_t((1u << kCM) - 1u);  // every CTA of the cluster
   using S = GemmShape<E>;
   constexpr int kGemmStages = S::kStages;
   constexpr int kMH = S::kMH;
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = kCM == 2 ? cluster_ctarank() : 0u;
+  const uint32_t rank = kCM > 1 ? cluster_ctarank() : 0u;
   const int cluster_id = int(blockIdx.x) / kCM;
   const int num_clusters = int(gridDim.x) / kCM;
   const int cluster_tiles = p.total_tiles / kCM;
@@ -155,8 +156,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     tmem_relinquish();
   }
   tc_fence_before();
-  if constexpr (kCM == 2)
-    cluster_sync();  // the peer's barriers are initialised before anything targets them
+  if constexpr (kCM > 1)
+    cluster_sync();  // the peers' barriers are initialised before anything targets them
   else
     __syncthreads();
   tc_fence_after();
@@ -196,9 +197,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
               tma_load_2d(dA + i * kMNAtomBytes, &p.maps[am], &sync->full[stage], j.a_y + 64 * i, ak, pa);
           }
           if constexpr (!E::kBMN) {
-            if constexpr (kCM == 2)
-              tma_load_2d_multicast(dB + rank * (kGemmStageB / 2), &p.maps[bm], &sync->full[stage], bk,
-                                    j.b_y + int(rank) * (kGemmBlockN / 2), uint16_t(0x3), pb);
+            if constexpr (kCM > 1)
+              tma_load_2d_multicast(dB + rank * (kGemmStageB / kCM), &p.maps[bm], &sync->full[stage], bk,
+                                    j.b_y + int(rank) * (kGemmBlockN / kCM), kCtaMask, pb);
             else
               tma_load_2d(dB, &p.maps[bm], &sync->full[stage], bk, j.b_y, pb);
           } else {
@@ -206,9 +207,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 #pragma unroll
             for (int i = 0; i < kAtoms / kCM; ++i) {
               const int a = int(rank) * (kAtoms / kCM) + i;
-              if constexpr (kCM == 2)
+              if constexpr (kCM > 1)
                 tma_load_2d_multicast(dB + a * kMNAtomBytes, &p.maps[bm], &sync->full[stage], j.b_y + 64 * a, bk,
-                                      uint16_t(0x3), pb);
+                                      kCtaMask, pb);
               else
                 tma_load_2d(dB + a * kMNAtomBytes, &p.maps[bm], &sync->full[stage], j.b_y + 64 * a, bk, pb);
             }
@@ -258,8 +259,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
               umma_bf16(d_tmem + h * kGemmBlockN, a_desc + a_step * k, b_desc + b_step * k, idesc,
                         (kb | k) != 0 ? 1u : 0u);
           }
-          if constexpr (kCM == 2)
-            umma_commit_multicast(&sync->empty[stage], uint16_t(0x3));
+          if constexpr (kCM > 1)
+            umma_commit_multicast(&sync->empty[stage], kCtaMask);
           else
             umma_commit(&sync->empty[stage]);
           if (++stage == kGemmStages) {
@@ -300,8 +301,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   }
 
   tc_fence_before();
-  if constexpr (kCM == 2)
-    cluster_sync();  // neither CTA leaves while its peer may still signal or write into it
+  if constexpr (kCM > 1)
+    cluster_sync();  // no CTA leaves while a peer may still signal or write into it
   else
     __syncthreads();
   if (warp == 1) {
