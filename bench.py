@@ -278,40 +278,41 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
     import torch
     out = {}
     Vp = args.vocab
+    TP = args.path_rows  # rows of the logits and replay workloads
     wanted = set(args.paths.split(","))
     if wanted & {"logits", "replay"}:
         part = synth.even_partition(Vp, 1)
         P = lp.VocabPartition(part.vocab_real, part.vocab_padded, part.ranges)
-        L, y = synth.device_logits(8192, part, dev, seed=4)
+        L, y = synth.device_logits(TP, part, dev, seed=4)
         part4 = synth.even_partition(Vp, 4)
         P4 = lp.VocabPartition(part4.vocab_real, part4.vocab_padded, part4.ranges)
-        ids, yr = synth.replay_ids(8192, part4, seed=5)
+        ids, yr = synth.replay_ids(TP, part4, seed=5)
         ids_d = torch.from_numpy(ids).to(dev)
         yr_d = torch.from_numpy(yr).to(dev)
         uniq = sum(len(set(r[r >= 0].tolist())) for r in ids)
         if "logits" in wanted:
-            # logits reuse: T=8192 x V bf16 logits
+            # logits reuse: T=TP x V bf16 logits
             ms = time_steps(lambda: lp.lp_forward_from_logits(L, P, y, TAU), args.steps, args.warmup, stream)
-            nbytes = 8192 * Vp * 2
+            nbytes = TP * Vp * 2
             gbs = nbytes / (ms * 1e-3) / 1e9
             out["logits_reuse"] = {
-                "workload": f"T=8192, V={Vp} bf16 logits N(0,9), 1% peaked, tau=0.7",
-                "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
+                "workload": f"T={TP}, V={Vp} bf16 logits N(0,9), 1% peaked, tau=0.7",
+                "tokens_per_s": TP / (ms * 1e-3), "ms": ms,
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
                              "traffic": stored_traffic("stream_logits")}}
             # its backward: the gradient with respect to those logits, bf16, out of place
             fl = lp.lp_forward_from_logits(L, P, y, TAU)
-            gl = torch.randn(8192, generator=torch.Generator(device=dev).manual_seed(4), device=dev)
+            gl = torch.randn(TP, generator=torch.Generator(device=dev).manual_seed(4), device=dev)
             dL = [torch.empty_like(L[0])]
             ms = time_steps(lambda: lp.lp_backward_from_logits(L, P, y, TAU, fl["lse"], gl, entropy=fl["entropy"],
                                                                grad_entropy=gl, out=dL),
                             args.steps, args.warmup, stream)
-            nbytes = 2 * 8192 * Vp * 2
+            nbytes = 2 * TP * Vp * 2
             gbs = nbytes / (ms * 1e-3) / 1e9
             out["logits_backward"] = {
-                "workload": f"gradient w.r.t. the T=8192 x V={Vp} logits above (logp + entropy terms), bf16 out",
-                "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
+                "workload": f"gradient w.r.t. the T={TP} x V={Vp} logits above (logp + entropy terms), bf16 out",
+                "tokens_per_s": TP / (ms * 1e-3), "ms": ms,
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
                              "traffic": stored_traffic("logits_backward")}}
@@ -322,21 +323,21 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
             ms = time_steps(lambda: lp.lp_top_p_replay_from_logits(L4, P4, ids_d, yr_d, TAU), args.steps,
                             args.warmup, stream)
             out["top_p_replay_from_logits"] = {
-                "workload": "T=8192 rows of the logits above in 4 shards, 1-64 ids/row",
-                "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms, "ids_scored": uniq}
+                "workload": f"T={TP} rows of the logits above in 4 shards, 1-64 ids/row",
+                "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "ids_scored": uniq}
         del L
         torch.cuda.empty_cache()
         if "replay" in wanted:
-            # compact top-p replay: T=8192, 4 shards, ids as the nucleus recipe
-            X, W, _, _ = synth.device_forward_inputs(8192, H, part4, TAU, dev, seed=5)
+            # compact top-p replay: T=TP, 4 shards, ids as the nucleus recipe
+            X, W, _, _ = synth.device_forward_inputs(TP, H, part4, TAU, dev, seed=5)
             ms = time_steps(lambda: lp.lp_top_p_replay(X, W, None, P4, ids_d, yr_d, TAU), args.steps, args.warmup,
                             stream)
             distinct = len(set(ids[ids >= 0].tolist()))
-            gathered = 8192 * H * 2 + uniq * H * 2
-            distinct_b = 8192 * H * 2 + distinct * H * 2
+            gathered = TP * H * 2 + uniq * H * 2
+            distinct_b = TP * H * 2 + distinct * H * 2
             out["top_p_replay"] = {
-                "workload": f"T=8192, H=4096, V={Vp} in 4 shards, 1-64 ids/row (+10% dups), tau=0.7",
-                "tokens_per_s": 8192 / (ms * 1e-3), "ms": ms,
+                "workload": f"T={TP}, H=4096, V={Vp} in 4 shards, 1-64 ids/row (+10% dups), tau=0.7",
+                "tokens_per_s": TP / (ms * 1e-3), "ms": ms,
                 "gathered_bytes": gathered, "distinct_bytes": distinct_b,
                 "roofline": {"bound": "hbm", "achieved": gathered / (ms * 1e-3) / 1e9,
                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -436,6 +437,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per reference step")
     ap.add_argument("--rows", type=int, default=T_FWD, help="headline rows T (profiling of smaller cases)")
+    ap.add_argument("--path-rows", type=int, default=8192,
+                    help="rows of the logits-reuse and replay workloads (profiling of smaller cases)")
     ap.add_argument("--vocab", type=int, default=V, help="vocabulary V of every path (profiling of smaller cases)")
     ap.add_argument("--paths", default="logits,replay,backward",
                     help="comma list of the other paths to time: logits, replay, backward")

@@ -235,8 +235,25 @@ def _outputs(T: int, n_shards: int, device, entropy: bool, shard_stats: bool, ou
             raise ValueError("out must hold logp and lse")
         if o["shard_stats"] is not None:
             _check(o["shard_stats"], "out['shard_stats']", torch.float32, 3)
+            _shape(o["shard_stats"], "out['shard_stats']", (n_shards, 3, T))
     co = _Outputs(_ptr(o["logp"]), _ptr(o["lse"]), _ptr(o["entropy"]), _ptr(o["shard_stats"]))
     return o, co
+
+
+def _shape(t: Optional[torch.Tensor], name: str, shape: tuple):
+    """The library sees only pointers, so every extent it will read or write is checked here."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _shard_shapes(ts, part, name: str, inner: Optional[int] = None, rows: Optional[int] = None):
+    """Per shard k: [V_k] (inner and rows None), [V_k, inner] or [rows, V_k]."""
+    if ts is None:
+        return
+    for k, ((s0, e0), t) in enumerate(zip(part.ranges, ts)):
+        w = e0 - s0
+        shape = (w,) if inner is None and rows is None else ((w, inner) if rows is None else (rows, w))
+        _shape(t, f"{name}[{k}]", shape)
 
 
 def _shard_list(ts, n: int, name: str, dtype, ndim: int, allow_none: bool):
@@ -267,6 +284,9 @@ def lp_forward(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optional[Sequen
     W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
     bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
     T, H = X.shape
+    _shape(y, "y", (T,))
+    _shard_shapes(W, part, "W", inner=H)
+    _shard_shapes(bias, part, "bias")
     cp, _keep = _c_partition(part)
     with torch.cuda.device(X.device):
         need = lp_workspace_size(LP_OP_FORWARD, T, H, part)
@@ -290,6 +310,9 @@ def lp_forward_noalloc(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optiona
     W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
     bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
     T, H = X.shape
+    _shape(y, "y", (T,))
+    _shard_shapes(W, part, "W", inner=H)
+    _shard_shapes(bias, part, "bias")
     cp, _keep = _c_partition(part)
     with torch.cuda.device(X.device):
         o, co = _outputs(T, n, X.device, entropy, shard_stats)
@@ -300,17 +323,18 @@ def lp_forward_noalloc(X: torch.Tensor, W: Sequence[torch.Tensor], bias: Optiona
     return o
 
 
-def _logits_ld(logits, n: int, T: int):
+def _logits_ld(logits, part, T: int):
+    n = len(part.ranges)
     if len(logits) != n:
         raise ValueError("logits must have one entry per shard")
     ld = (ctypes.c_int64 * max(n, 1))()
-    for k, L in enumerate(logits):
+    for k, (L, (s0, e0)) in enumerate(zip(logits, part.ranges)):
         if L is None:
             continue
         if not (isinstance(L, torch.Tensor) and L.is_cuda and L.dtype == torch.bfloat16 and L.dim() == 2):
             raise TypeError(f"logits[{k}] must be a 2-D bf16 CUDA tensor")
-        if L.stride(1) != 1 or L.shape[0] != T:
-            raise ValueError(f"logits[{k}] must be [T, V_k] with unit column stride")
+        if L.stride(1) != 1 or tuple(L.shape) != (T, e0 - s0):
+            raise ValueError(f"logits[{k}] must be [T, V_k] = [{T}, {e0 - s0}] with unit column stride")
         ld[k] = L.stride(0)
     return ld
 
@@ -321,7 +345,7 @@ def lp_forward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tensor
     _check(y, "y", torch.int32, 1)
     n = len(part.ranges)
     T = y.shape[0]
-    ld = _logits_ld(logits, n, T)
+    ld = _logits_ld(logits, part, T)
     cp, _keep = _c_partition(part)
     with torch.cuda.device(y.device):
         o, co = _outputs(T, n, y.device, entropy, shard_stats)
@@ -343,6 +367,9 @@ def lp_top_p_replay(X: torch.Tensor, W, bias, part, replay_ids: torch.Tensor, y:
     W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
     bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
     T, H = X.shape
+    _shape(y, "y", (T,))
+    _shard_shapes(W, part, "W", inner=H)
+    _shard_shapes(bias, part, "bias")
     cp, _keep = _c_partition(part)
     with torch.cuda.device(X.device):
         o, co = _outputs(T, n, X.device, False, shard_stats)
@@ -362,7 +389,7 @@ def lp_top_p_replay_from_logits(logits: Sequence[torch.Tensor], part, replay_ids
     if replay_ids.shape != (T, LP_REPLAY_SLOTS):
         raise ValueError("replay_ids must be [T, 64]")
     n = len(part.ranges)
-    ld = _logits_ld(logits, n, T)
+    ld = _logits_ld(logits, part, T)
     cp, _keep = _c_partition(part)
     with torch.cuda.device(y.device):
         o, co = _outputs(T, n, y.device, False, shard_stats)
@@ -384,6 +411,10 @@ def lp_top_p_replay_dense_mask(X: torch.Tensor, W, bias, part, keep_mask: Sequen
     bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
     keep_mask = _shard_list(keep_mask, n, "keep_mask", torch.uint8, 2, True)
     T, H = X.shape
+    _shape(y, "y", (T,))
+    _shard_shapes(W, part, "W", inner=H)
+    _shard_shapes(bias, part, "bias")
+    _shard_shapes(keep_mask, part, "keep_mask", rows=T)
     cp, _keep = _c_partition(part)
     with torch.cuda.device(X.device):
         need = lp_workspace_size(LP_OP_TOP_P_REPLAY_DENSE_MASK, T, H, part)
@@ -414,6 +445,11 @@ def _backward(fn: str, X: torch.Tensor, W, bias, part, y, tau, lse, grad_logp, b
     W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
     bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
     T, H = X.shape
+    for t, nm in ((y, "y"), (lse, "lse"), (grad_logp, "grad_logp"), (entropy, "entropy"),
+                  (grad_entropy, "grad_entropy")):
+        _shape(t, nm, (T,))
+    _shard_shapes(W, part, "W", inner=H)
+    _shard_shapes(bias, part, "bias")
     widths = [e - s for s, e in part.ranges]
     if accumulate and (dW is None or (bias_grad and db is None)):
         raise ValueError("accumulate=True adds into the caller's dW (and db): pass them")
@@ -491,7 +527,9 @@ def lp_backward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tenso
         raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
     n = len(part.ranges)
     T = y.shape[0]
-    ld = _logits_ld(logits, n, T)
+    for t, nm in ((lse, "lse"), (grad_logp, "grad_logp"), (entropy, "entropy"), (grad_entropy, "grad_entropy")):
+        _shape(t, nm, (T,))
+    ld = _logits_ld(logits, part, T)
     widths = [e - s for s, e in part.ranges]
     if out is None:
         # rows padded to a 16-byte multiple (the row rule), handed back as [T, V_k] views

@@ -98,3 +98,37 @@ def test_backward_rows_without_target_or_lse_get_no_gradient(lp):
     for k in range(2):
         assert rel_fro(_np(bw["dW"][k]), ref.dW[k]) <= TOL_GRAD_REL
         assert rel_fro(_np(bw["db"][k]), ref.db[k]) <= TOL_GRAD_REL
+
+
+def test_binding_rejects_mismatched_extents_before_any_launch(lp):
+    # the library sees only pointers: every extent it would read or write is checked first
+    import torch
+    part = synth.ranges_partition(500, 512, [0, 256, 512])
+    T, H = 16, 64
+    inp = synth.forward_inputs(T, H, part, tau=0.7, seed=9, bias_std=0.1)
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    f = lp.lp_forward(X, W, b, P, y, inp.tau)
+    g = torch.ones(T, device="cuda")
+    bad_cases = [
+        lambda: lp.lp_forward(X, [W[0][:, :32].contiguous(), W[1]], b, P, y, inp.tau),   # W of another H
+        lambda: lp.lp_forward(X, [W[0][:200].contiguous(), W[1]], b, P, y, inp.tau),     # W short of V_k rows
+        lambda: lp.lp_forward(X, W, [b[0][:100].contiguous(), b[1]], P, y, inp.tau),     # bias short
+        lambda: lp.lp_forward(X, W, b, P, y[:8].contiguous(), inp.tau),                  # y short
+        lambda: lp.lp_top_p_replay(X, W, b, P, torch.full((T, 64), -1, dtype=torch.int32, device="cuda"),
+                                   y[:8].contiguous(), inp.tau),
+        lambda: lp.lp_backward(X, W, b, P, y, inp.tau, f["lse"][:8].contiguous(), g),     # lse short
+        lambda: lp.lp_forward_from_logits([torch.zeros((T, 200), dtype=torch.bfloat16, device="cuda"),
+                                           torch.zeros((T, 256), dtype=torch.bfloat16, device="cuda")], P, y,
+                                          inp.tau),                                        # logits narrower
+        lambda: lp.lp_top_p_replay_dense_mask(X, W, b, P, [torch.zeros((T, 256), dtype=torch.uint8, device="cuda"),
+                                                           torch.zeros((T, 100), dtype=torch.uint8,
+                                                                       device="cuda")], y, inp.tau),
+        lambda: lp.lp_forward(X, W, b, P, y, inp.tau, shard_stats=True,
+                              out={"logp": torch.empty(T, device="cuda"), "lse": torch.empty(T, device="cuda"),
+                                   "shard_stats": torch.empty((1, 3, T), device="cuda")}),
+    ]
+    for i, case in enumerate(bad_cases):
+        with pytest.raises(ValueError):
+            case()
+    assert lp.lp_get_device_error() == 0
