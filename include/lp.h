@@ -81,7 +81,8 @@ typedef enum {
   LP_OP_TOP_P_REPLAY = 2,
   LP_OP_BACKWARD = 3,
   LP_OP_TOP_P_REPLAY_DENSE_MASK = 4,
-  LP_OP_BACKWARD_FROM_LOGITS = 5   /* needs no workspace */
+  LP_OP_BACKWARD_FROM_LOGITS = 5,  /* needs no workspace */
+  LP_OP_FORWARD_HOST = 6
 } lp_op;
 
 /* Element type of an output buffer whose type the caller chooses. */
@@ -140,6 +141,21 @@ LP_API lp_status lp_forward(const void* X, int64_t T, int64_t H,
                      const lp_vocab_partition* part, const int32_t* y, float tau,
                      const lp_outputs* out, void* workspace, size_t ws_bytes,
                      lp_stream_t stream);
+
+/* lp_forward on host-resident rows: the whole call as a host program sees it. X_host
+ * (bf16 [T, H]) and y_host (int32 [T]) are HOST memory, and so are the buffers in
+ * out_host (logp, lse, and entropy / shard_stats when non-NULL); W and bias are device
+ * memory as in lp_forward. On `stream` the call copies X and y into device staging held
+ * in the workspace, runs lp_forward there and copies the requested outputs back, all
+ * asynchronously: the host buffers hold the results once the stream has been
+ * synchronised, and must stay valid until then. Page-locked host buffers make the copies
+ * truly asynchronous; pageable ones also work. Results are bitwise those of lp_forward.
+ * Workspace: lp_workspace_size(LP_OP_FORWARD_HOST, T, H, part) bytes of device memory. */
+LP_API lp_status lp_forward_host(const void* X_host, int64_t T, int64_t H,
+                                 const void* const* W, const void* const* bias,
+                                 const lp_vocab_partition* part, const int32_t* y_host, float tau,
+                                 const lp_outputs* out_host, void* workspace, size_t ws_bytes,
+                                 lp_stream_t stream);
 
 /* Logits-reuse forward (page "feat(rl-kernel): add CUDA linear logp provider
  * integration", Changes / Megatron integration: reuse local logits instead of a

@@ -49,16 +49,17 @@ LP_OP_TOP_P_REPLAY = 2
 LP_OP_BACKWARD = 3
 LP_OP_TOP_P_REPLAY_DENSE_MASK = 4
 LP_OP_BACKWARD_FROM_LOGITS = 5
+LP_OP_FORWARD_HOST = 6
 
 LP_DTYPE_F32 = 0
 LP_DTYPE_BF16 = 1
 _LP_DTYPES = {torch.float32: LP_DTYPE_F32, torch.bfloat16: LP_DTYPE_BF16}
 
 # every symbol include/lp.h declares
-EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
-            "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward", "lp_backward_ex",
-            "lp_backward_from_logits", "lp_get_device_error", "lp_selftest_wait_timeout", "lp_device_supported",
-            "lp_status_string")
+EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward_host", "lp_forward_from_logits",
+            "lp_top_p_replay", "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward",
+            "lp_backward_ex", "lp_backward_from_logits", "lp_get_device_error", "lp_selftest_wait_timeout",
+            "lp_device_supported", "lp_status_string")
 
 
 class LPError(RuntimeError):
@@ -130,6 +131,7 @@ def lib() -> ctypes.CDLL:
                                  P(vp), P(_BackwardOptions), vp, sz, vp]
     L.lp_backward_from_logits.argtypes = [P(vp), P(i64), i64, P(_Partition), vp, f32, vp, vp, vp, vp, P(vp),
                                           P(i64), ctypes.c_int, vp]
+    L.lp_forward_host.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, P(_Outputs), vp, sz, vp]
     L.lp_get_device_error.argtypes = [vp]
     L.lp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     L.lp_device_supported.argtypes = []
@@ -137,7 +139,7 @@ def lib() -> ctypes.CDLL:
     L.lp_status_string.restype = ctypes.c_char_p
     for name in ("lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
                  "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask",
-                 "lp_backward", "lp_backward_ex", "lp_backward_from_logits", "lp_get_device_error",
+                 "lp_backward", "lp_backward_ex", "lp_backward_from_logits", "lp_forward_host", "lp_get_device_error",
                  "lp_selftest_wait_timeout", "lp_device_supported"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -557,63 +559,52 @@ def lp_backward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tenso
 
 
 def lp_forward_host(hX: torch.Tensor, W: Sequence[torch.Tensor], bias, part, hy: torch.Tensor, tau: float,
-                    chunk_rows: Optional[int] = None, entropy: bool = True, device=None,
-                    staging: Optional[dict] = None) -> dict:
-    """lp_forward from host memory: pinned CPU hX bf16 [T,H] and hy int32 [T] in, CPU fp32
-    logp / lse / entropy out (pinned tensors owned by ``staging``, overwritten by the next
-    call that reuses it).
-
-    With ``chunk_rows`` the rows go in chunks: chunk c+1 is copied host -> device on a side
-    stream while lp_forward runs on chunk c. A row's results do not depend on the batch it
-    is computed in, so the outputs are bit-identical to one call over all rows. Each chunk
-    streams W again, so chunks pay off only when they stay large (several thousand rows);
-    by default (None) all rows go in one chunk: at T = 4096, H = 4096 the 33.5 MB copy takes
-    0.16 ms against 2.76 ms of projection, while 4 chunks of 1024 rows take 3.33 ms.
-    ``staging`` (optional, reused across calls) holds the device buffers.
-    """
-    if chunk_rows is None:
-        chunk_rows = int(hX.shape[0])
+                    entropy: bool = True, shard_stats: bool = False, workspace: Optional[torch.Tensor] = None,
+                    out: Optional[dict] = None, device=None) -> dict:
+    """lp_forward from host memory, through the C entry point of the same name: CPU hX bf16
+    [T,H] and hy int32 [T] in (page-locked for asynchronous copies), CPU fp32 logp / lse /
+    entropy / shard_stats out (``out`` holds reusable page-locked tensors, else new ones are
+    allocated). W and bias are CUDA tensors on ``device``. Synchronises the stream before
+    returning, so the host tensors hold the results."""
     if hX.is_cuda or hy.is_cuda:
         raise ValueError("hX and hy must be host tensors")
     if hX.dtype != torch.bfloat16 or hy.dtype != torch.int32 or hX.dim() != 2 or hy.dim() != 1:
         raise TypeError("hX must be bf16 [T, H] and hy int32 [T]")
+    if not (hX.is_contiguous() and hy.is_contiguous()):
+        raise ValueError("hX and hy must be contiguous")
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     T, H = hX.shape
-    st = staging if staging is not None else {}
-    if st.get("shape") != (T, H, entropy) or st.get("device") != dev:
-        st.clear()
-        st.update(shape=(T, H, entropy), device=dev,
-                  X=torch.empty((T, H), dtype=torch.bfloat16, device=dev),
-                  y=torch.empty(T, dtype=torch.int32, device=dev),
-                  out={"logp": torch.empty(T, dtype=torch.float32, device=dev),
-                       "lse": torch.empty(T, dtype=torch.float32, device=dev),
-                       "entropy": torch.empty(T, dtype=torch.float32, device=dev) if entropy else None},
-                  host={k: torch.empty(T, dtype=torch.float32, pin_memory=True)
-                        for k in (("logp", "lse", "entropy") if entropy else ("logp", "lse"))},
-                  copy_stream=torch.cuda.Stream(device=dev))
-        with torch.cuda.device(dev):
-            st["ws"] = torch.empty(max(1, lp_workspace_size(LP_OP_FORWARD, min(T, chunk_rows), H, part)),
-                                   dtype=torch.uint8, device=dev)
-    compute = torch.cuda.current_stream(dev)
-    copy = st["copy_stream"]
-    bounds = [(r0, min(T, r0 + chunk_rows)) for r0 in range(0, T, chunk_rows)]
-    ready = []
-    copy.wait_stream(compute)          # the previous call's reads of the staging buffers are done
-    with torch.cuda.stream(copy):
-        for r0, r1 in bounds:
-            st["X"][r0:r1].copy_(hX[r0:r1], non_blocking=True)
-            st["y"][r0:r1].copy_(hy[r0:r1], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(copy)
-            ready.append(ev)
+    _shape(hy, "hy", (T,))
+    n = len(part.ranges)
+    W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
+    bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
+    _shard_shapes(W, part, "W", inner=H)
+    _shard_shapes(bias, part, "bias")
+    pin = torch.cuda.is_available()
+    if out is None:
+        out = {"logp": torch.empty(T, dtype=torch.float32, pin_memory=pin),
+               "lse": torch.empty(T, dtype=torch.float32, pin_memory=pin),
+               "entropy": torch.empty(T, dtype=torch.float32, pin_memory=pin) if entropy else None,
+               "shard_stats": torch.empty((n, 3, T), dtype=torch.float32, pin_memory=pin) if shard_stats else None}
+    for k, shape in (("logp", (T,)), ("lse", (T,)), ("entropy", (T,)), ("shard_stats", (n, 3, T))):
+        t = out.get(k)
+        if t is None:
+            if k in ("logp", "lse"):
+                raise ValueError("out must hold logp and lse")
+            continue
+        if t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"out[{k!r}] must be a contiguous fp32 host tensor")
+        _shape(t, f"out[{k!r}]", shape)
+    co = _Outputs(_ptr(out["logp"]), _ptr(out["lse"]), _ptr(out.get("entropy")), _ptr(out.get("shard_stats")))
+    cp, _keep = _c_partition(part)
     with torch.cuda.device(dev):
-        for (r0, r1), ev in zip(bounds, ready):
-            compute.wait_event(ev)
-            o = {k: (v[r0:r1] if v is not None else None) for k, v in st["out"].items()}
-            lp_forward(st["X"][r0:r1], W, bias, part, st["y"][r0:r1], tau, entropy=entropy,
-                       workspace=st["ws"], out=o)
-        for k, h in st["host"].items():
-            h.copy_(st["out"][k], non_blocking=True)
-    compute.synchronize()
-    return dict(st["host"])
+        need = lp_workspace_size(LP_OP_FORWARD_HOST, T, H, part)
+        ws, wsb = _workspace(need, dev, workspace)
+        stream = torch.cuda.current_stream(dev)
+        st = lib().lp_forward_host(hX.data_ptr(), T, H, _ptr_array(W), _ptr_array(bias) if bias is not None else None,
+                                   ctypes.byref(cp), hy.data_ptr(), float(tau), ctypes.byref(co), _ptr(ws), wsb,
+                                   stream.cuda_stream)
+        _raise(st, "lp_forward_host")
+        stream.synchronize()
+    return {k: out.get(k) for k in ("logp", "lse", "entropy", "shard_stats")}
 

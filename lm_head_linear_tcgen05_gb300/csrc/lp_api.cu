@@ -155,6 +155,31 @@ size_t forward_ws_bytes(int64_t T, const Shards& sh) {
   return 3 * per + align_up(size_t(T) * sizeof(float), 256);
 }
 
+// Workspace of lp_forward_host: the forward's own, then device staging for X, y and
+// every output (logp, LSE, entropy, shard statistics), each 256-byte aligned.
+struct HostLayout {
+  size_t off_x, off_y, off_logp, off_lse, off_ent, off_ss, total;
+};
+
+HostLayout host_layout(int64_t T, int64_t H, const Shards& sh) {
+  HostLayout L;
+  size_t off = forward_ws_bytes(T, sh);
+  L.off_x = off;
+  off += align_up(size_t(T) * size_t(H) * 2, 256);
+  L.off_y = off;
+  off += align_up(size_t(T) * 4, 256);
+  L.off_logp = off;
+  off += align_up(size_t(T) * 4, 256);
+  L.off_lse = off;
+  off += align_up(size_t(T) * 4, 256);
+  L.off_ent = off;
+  off += align_up(size_t(T) * 4, 256);
+  L.off_ss = off;
+  off += align_up(size_t(sh.n) * 3 * size_t(T) * 4, 256);
+  L.total = off;
+  return L;
+}
+
 }  // namespace lp
 
 using namespace lp;
@@ -192,6 +217,7 @@ size_t lp_workspace_size(lp_op op, int64_t T, int64_t H, const lp_vocab_partitio
     case LP_OP_TOP_P_REPLAY_DENSE_MASK: return align_up(size_t(T) * LP_REPLAY_SLOTS * sizeof(int32_t), 256);
     case LP_OP_BACKWARD: return valid_hidden(H) ? backward_ws_bytes(T, H, sh) : 0;
     case LP_OP_BACKWARD_FROM_LOGITS: return 0;
+    case LP_OP_FORWARD_HOST: return valid_hidden(H) ? host_layout(T, H, sh).total : 0;
   }
   return 0;
 }
@@ -284,6 +310,53 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (launch_fused_forward(p, dev->num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
   if (launch_merge(mp, s) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
+}
+
+lp_status lp_forward_host(const void* X_host, int64_t T, int64_t H, const void* const* W, const void* const* bias,
+                          const lp_vocab_partition* part, const int32_t* y_host, float tau, const lp_outputs* out_host,
+                          void* workspace, size_t ws_bytes, lp_stream_t stream) {
+  Shards sh;
+  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T) || !valid_hidden(H) || !valid_tau(tau)) return LP_ERR_INVALID_ARG;
+  if (T == 0) return LP_OK;
+  if (X_host == nullptr || y_host == nullptr || out_host == nullptr || out_host->logp == nullptr ||
+      out_host->lse == nullptr)
+    return LP_ERR_INVALID_ARG;
+  const HostLayout L = host_layout(T, H, sh);
+  if (workspace == nullptr || ws_bytes < L.total) return LP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return LP_ERR_ALIGNMENT;
+  DeviceState* dev = nullptr;
+  const lp_status dst = device_state(&dev);
+  if (dst != LP_OK) return dst;
+  char* ws = static_cast<char*>(workspace);
+  void* dX = ws + L.off_x;
+  int32_t* dy = reinterpret_cast<int32_t*>(ws + L.off_y);
+  lp_outputs dout;
+  dout.logp = reinterpret_cast<float*>(ws + L.off_logp);
+  dout.lse = reinterpret_cast<float*>(ws + L.off_lse);
+  dout.entropy = out_host->entropy != nullptr ? reinterpret_cast<float*>(ws + L.off_ent) : nullptr;
+  dout.shard_stats = out_host->shard_stats != nullptr ? reinterpret_cast<float*>(ws + L.off_ss) : nullptr;
+  // lp_forward validates everything else (W, bias, device) before it launches anything,
+  // so a rejected call has enqueued at most the two input copies
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t tb = size_t(T) * 4;
+  if (cudaMemcpyAsync(dX, X_host, size_t(T) * size_t(H) * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dy, y_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return LP_ERR_CUDA;
+  }
+  const lp_status st = lp_forward(dX, T, H, W, bias, part, dy, tau, &dout, ws, forward_ws_bytes(T, sh), stream);
+  if (st != LP_OK) return st;
+  if (cudaMemcpyAsync(out_host->logp, dout.logp, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(out_host->lse, dout.lse, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      (dout.entropy != nullptr &&
+       cudaMemcpyAsync(out_host->entropy, dout.entropy, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+      (dout.shard_stats != nullptr && cudaMemcpyAsync(out_host->shard_stats, dout.shard_stats, size_t(sh.n) * 3 * tb,
+                                                      cudaMemcpyDeviceToHost, s) != cudaSuccess)) {
+    cudaGetLastError();
+    return LP_ERR_CUDA;
+  }
   return LP_OK;
 }
 

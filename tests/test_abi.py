@@ -192,3 +192,28 @@ def test_backward_ex_host_validation(lp):
     assert call(T=0) == 3                     # empty batch, overwriting: zeroes dW on the device
     assert call(dx_dtype=1, accumulate=1) == 3
     assert call(opts=False) == 3
+
+
+@pytest.mark.skipif(_has_gpu(), reason="uses fake pointers; only safe without a GPU")
+def test_forward_host_validation(lp):
+    L = lp.lib()
+    A = 0x100000  # fake device / host addresses; never dereferenced before the checks fail
+    p = _part(lp, 1000, 1000, [0, 1000])
+    cp, keep = lp._c_partition(p)
+    T, H = 64, 256
+    need = lp.lp_workspace_size(lp.LP_OP_FORWARD_HOST, T, H, p)
+    # forward workspace + X + y + logp/lse/entropy + shard statistics, each 256-byte aligned
+    assert need == lp.lp_workspace_size(lp.LP_OP_FORWARD, T, H, p) + T * H * 2 + 4 * 256 + 768
+    Wa = (ctypes.c_void_p * 1)(A)
+
+    def call(X=A, y=A, logp=A, lse=A, ws=A, wsb=need, T=T):
+        out = lp._Outputs(logp, lse, None, None)
+        return L.lp_forward_host(X, T, H, Wa, None, ctypes.byref(cp), y, 0.7, ctypes.byref(out), ws, wsb, None)
+
+    assert call(X=None) == 1
+    assert call(y=None) == 1
+    assert call(lse=None) == 1
+    assert call(wsb=need - 1) == 4
+    assert call(ws=A + 8) == 2
+    assert call(T=0, X=None, y=None, logp=None, lse=None, ws=None, wsb=0) == 0
+    assert call() == 3                       # valid: fails only for want of a GPU, before any copy

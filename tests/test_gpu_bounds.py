@@ -91,7 +91,7 @@ def test_logits_and_replay_write_only_inside_their_buffers(lp):
     P = part_of(part)
     Lb = lp.lib()
     cp, keep = lp._c_partition(P)
-    ld = lp._logits_ld(Ld, 3, T)
+    ld = lp._logits_ld(Ld, P, T)
     logp, lse, ent, ss = Guarded(T), Guarded(T), Guarded(T), Guarded(9 * T)
     out = lp._Outputs(logp.ptr, lse.ptr, ent.ptr, ss.ptr)
     st = Lb.lp_forward_from_logits(lp._ptr_array(Ld), ld, T, ctypes.byref(cp), dev_i32(yl).data_ptr(), tau,

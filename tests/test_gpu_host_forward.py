@@ -1,5 +1,7 @@
-"""lp_forward_host: rows copied from pinned host memory in chunks that overlap the
-forward give the same bits as one lp_forward call on device-resident inputs."""
+"""lp_forward_host (the C entry point on host-resident rows): its results are bitwise those
+of lp_forward on device-resident inputs, with page-locked or pageable host buffers, with
+every optional output, with reused workspace and output buffers, and for an empty batch."""
+import numpy as np
 import pytest
 
 import synth
@@ -19,20 +21,47 @@ def lp():
     return mod
 
 
-@pytest.mark.parametrize("T,chunk", [(3000, 1024), (700, 128), (64, 1024)])
-def test_host_forward_is_bitwise_the_device_forward(lp, T, chunk):
-    import numpy as np
+@pytest.mark.parametrize("T,pinned", [(3000, True), (700, False), (64, True)])
+def test_host_forward_is_bitwise_the_device_forward(lp, T, pinned):
     import torch
-    part = synth.ranges_partition(5000, 5120, [0, 2560, 5120])
+    part = synth.ranges_partition(5000, 5120, [0, 2560, 2560, 5120])     # an empty shard, padding
     inp = synth.forward_inputs(T, 256, part, tau=0.7, seed=T, bias_std=0.1)
     X, W, b, y = dev_inputs(inp)
     P = part_of(part)
-    ref = lp.lp_forward(X, W, b, P, y, inp.tau)
-    hX = torch.from_numpy(inp.X.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hy = torch.from_numpy(inp.y).pin_memory()
-    staging = {}
-    for _ in range(2):                      # reuse of the staging buffers across calls
-        out = lp.lp_forward_host(hX, W, b, P, hy, inp.tau, chunk_rows=chunk, staging=staging)
-        for k in ("logp", "lse", "entropy"):
-            assert torch.equal(out[k], ref[k].cpu()), k
+    ref = lp.lp_forward(X, W, b, P, y, inp.tau, shard_stats=True)
+    hX = torch.from_numpy(inp.X.view(np.int16)).view(torch.bfloat16)
+    hy = torch.from_numpy(inp.y)
+    if pinned:
+        hX, hy = hX.pin_memory(), hy.pin_memory()
+    ws = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD_HOST, T, 256, P), dtype=torch.uint8, device="cuda")
+    out = None
+    for _ in range(2):                      # reuse of the workspace and the host outputs
+        got = lp.lp_forward_host(hX, W, b, P, hy, inp.tau, shard_stats=True, workspace=ws, out=out)
+        out = got
+        for k in ("logp", "lse", "entropy", "shard_stats"):
+            assert not got[k].is_cuda and torch.equal(got[k], ref[k].cpu()), k
+    # optional outputs off
+    got = lp.lp_forward_host(hX, W, b, P, hy, inp.tau, entropy=False)
+    assert got["entropy"] is None and got["shard_stats"] is None
+    assert torch.equal(got["logp"], ref["logp"].cpu()) and torch.equal(got["lse"], ref["lse"].cpu())
+    assert lp.lp_get_device_error() == 0
+
+
+def test_host_forward_empty_batch_and_errors(lp):
+    import torch
+    part = synth.even_partition(1000, 1)
+    inp = synth.forward_inputs(8, 64, part, tau=0.7, seed=2)
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    hX = torch.from_numpy(inp.X.view(np.int16)).view(torch.bfloat16)
+    hy = torch.from_numpy(inp.y)
+    e = lp.lp_forward_host(hX[:0], W, b, P, hy[:0], inp.tau)
+    assert e["logp"].shape == (0,)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lp.LPError, match="WORKSPACE_TOO_SMALL"):
+        lp.lp_forward_host(hX, W, b, P, hy, inp.tau, workspace=small)
+    with pytest.raises(ValueError):
+        lp.lp_forward_host(X, W, b, P, hy, inp.tau)                      # device tensors are not host rows
+    with pytest.raises(ValueError):
+        lp.lp_forward_host(hX, W, b, P, hy[:4].contiguous(), inp.tau)     # y of another length
     assert lp.lp_get_device_error() == 0
