@@ -85,6 +85,87 @@ def stored_traffic(kernel: str):
     return None
 
 
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (read-only queries) every
+    `period` seconds by a background thread while the timed region runs. Raises on entry if
+    NVML cannot be used; ClockSampler (nvidia-smi) is the fallback."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, device, period: float = 0.005):
+        import ctypes
+        import threading
+        import torch
+        self.ct, self.threading, self.period = ctypes, threading, period
+        lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None or lib.nvmlInit_v2() != 0:
+            raise RuntimeError("NVML unavailable")
+        self.nvml = lib
+        props = torch.cuda.get_device_properties(device)
+        h = ctypes.c_void_p()
+        bus = getattr(props, "pci_bus_id", None)
+        ok = False
+        if bus is not None:
+            busid = f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(busid.encode(), ctypes.byref(h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(torch.cuda.current_device()),
+                                                         ctypes.byref(h)) != 0:
+            raise RuntimeError("NVML device handle unavailable")
+        self.h = h
+        self.get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.samples, self.reason_bits = [], 0
+
+    def _read(self):
+        c = self.ct.c_uint()
+        r = self.ct.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(c)) == 0:  # 1: SM clock
+            self.samples.append(c.value)
+        if self.get_reasons(self.h, self.ct.byref(r)) == 0:
+            self.reason_bits |= r.value
+
+    def _loop(self):
+        while not self.stop.is_set():
+            self._read()
+            self.stop.wait(self.period)
+
+    def __enter__(self):
+        self.stop = self.threading.Event()
+        self.thread = self.threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self.stop.set()
+        self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return None
+        mx = self.ct.c_uint()
+        max_mhz = float(mx.value) if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(mx)) == 0 else None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": max_mhz,
+                "sm_min_mhz": float(min(self.samples)),
+                "reasons": sorted(n for b, n in self.REASONS.items() if self.reason_bits & b),
+                "samples": len(self.samples), "source": f"NVML, every {self.period * 1e3:.0f} ms of the timed region"}
+
+
+def clock_sampler(device):
+    try:
+        return NvmlClockSampler(device)
+    except Exception:
+        return ClockSampler(torch_index(device))
+
+
+def torch_index(device) -> int:
+    return device.index if getattr(device, "index", None) is not None else 0
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples every 200 ms while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -161,19 +242,22 @@ def whole_job_rate(rows_per_rank: int, world: int, ms_max: float) -> float:
     return world * rows_per_rank / (ms_max * 1e-3)
 
 
-def time_steps(fn, steps, warmup, stream):
-    """Average ms per step over `steps` calls of fn(), CUDA events on `stream`."""
+def time_steps(fn, steps, warmup, stream, sampler=None):
+    """Average ms per step over `steps` calls of fn(), CUDA events on `stream`; `sampler`
+    (a context manager) runs around the timed calls only, after the warm-up."""
+    import contextlib
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
-        fn()
-    end.record(stream)
-    torch.cuda.synchronize()
+    with sampler if sampler is not None else contextlib.nullcontext():
+        start.record(stream)
+        for _ in range(steps):
+            fn()
+        end.record(stream)
+        torch.cuda.synchronize()
     return start.elapsed_time(end) / steps
 
 
@@ -211,8 +295,8 @@ def run_ours(args, rank, world, dist):
     step = lambda: lp.lp_forward(X, W, None, P, y, TAU, workspace=ws)
     if dist is not None:
         dist.barrier()
-    with ClockSampler(local) as clk:
-        ms = time_steps(step, args.steps, args.warmup, stream)
+    clk = clock_sampler(dev)
+    ms = time_steps(step, args.steps, args.warmup, stream, sampler=clk)
     if lp.lp_get_device_error() != 0:
         raise RuntimeError("device error during the timed forward")
     ms = reduce_max_ms(ms, dist, dev)
@@ -241,6 +325,16 @@ def run_ours(args, rank, world, dist):
     if not torch.equal(host_out["logp"], ref["logp"].cpu()):
         raise RuntimeError("host-staged forward differs from the device forward")
     del hX, ws_host
+    # ---- bitwise checks on the timed workload (outside the timed region): a repeat of the
+    # call, and the same rows as 8 batches of T/8, give the same bits
+    base = lp.lp_forward(X, W, None, P, y, TAU, workspace=ws)
+    again = lp.lp_forward(X, W, None, P, y, TAU, workspace=ws)
+    bit_repeat = all(torch.equal(base[k], again[k]) for k in ("logp", "lse", "entropy"))
+    chunk = max(1, T_FWD // 8)
+    parts = [lp.lp_forward(X[s0:s0 + chunk].contiguous(), W, None, P, y[s0:s0 + chunk].contiguous(), TAU)
+             for s0 in range(0, T_FWD, chunk)]
+    bit_batch = all(torch.equal(torch.cat([q[k] for q in parts]), base[k]) for k in ("logp", "lse", "entropy"))
+    del again, parts
     paths = {}
     if not args.headline_only:
         paths = time_other_paths(args, lp, synth, dev, stream, peaks)
@@ -269,9 +363,10 @@ def run_ours(args, rank, world, dist):
                      "timed": "whole lp_forward call (fused GEMM kernel + row merge kernel)",
                      "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"]},
         "paths": paths,
+        "bitwise": {"repeat": bit_repeat, f"1x{T_FWD}_vs_{-(-T_FWD // chunk)}x{chunk}": bit_batch},
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_forward(rows=64)
+        line["cpu_baseline"], line["parity"] = cpu_baseline_forward(X, W, y, base, rows=64)
     print(json.dumps(line), flush=True)
 
 
@@ -386,20 +481,36 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline_forward(rows: int):
-    """The fp64 oracle on `rows` rows of the headline workload (full H and V)."""
+def cpu_baseline_forward(X, W, y, gpu_out, rows: int):
+    """The fp64 oracle on `rows` rows of the timed workload itself (full H and V; rows spread
+    evenly over T): its speed on the host cores, and the GPU outputs' largest deviation from it
+    on those rows."""
     import numpy as np
+    import torch
 
     import oracle
     import synth
+    T, V = X.shape[0], W[0].shape[0]
+    idx = torch.linspace(0, T - 1, rows).round().long().unique()
+    Xb = X[idx.to(X.device)].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    Wb = [w.view(torch.int16).cpu().numpy().view(np.uint16) for w in W]
+    yb = y[idx.to(y.device)].cpu().numpy()
     part = synth.even_partition(V, 1)
-    inp = synth.forward_inputs(rows, H, part, tau=TAU, seed=0)
+    tau32 = float(np.float32(TAU))  # the fp32 temperature the library receives
     t0 = time.perf_counter()
-    oracle.forward(inp.X, inp.W, None, part, inp.y, inp.tau)
+    ref = oracle.forward(Xb, Wb, None, part, yb, tau32)
     dt = time.perf_counter() - t0
-    return {"value": rows / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{rows} of {T_FWD} rows of the headline workload (full H={H}, V={V}), fp64 numpy oracle; "
+    n = int(idx.numel())
+    got = {k: gpu_out[k][idx.to(X.device)].cpu().numpy().astype(np.float64) for k in ("logp", "lse", "entropy")}
+    parity = {"rows": n, "oracle": "fp64 numpy",
+              "max_abs_dlogp": float(np.max(np.abs(got["logp"] - ref.logp))),
+              "max_abs_dlse": float(np.max(np.abs(got["lse"] - ref.lse))),
+              "max_abs_dentropy": float(np.max(np.abs(got["entropy"] - ref.entropy))),
+              "tolerance": {"logp": 2e-3, "lse": 2e-3, "entropy": 5e-3}}
+    base = {"value": n / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} of {T} rows of the timed workload (full H={X.shape[1]}, V={V}), fp64 numpy oracle; "
                       f"{dt:.1f} s"}
+    return base, parity
 
 
 def run_reference(args, rank, world):

@@ -1,6 +1,7 @@
 """Seeded random sweep: small configurations drawn at random (rows, hidden size, shard
 layout with empty and all-padding shards, bias on/off, temperature) through every entry
-point, each compared with the fp64 oracle."""
+point, each compared with the fp64 oracle; the option and host entry points are checked
+bit for bit against their plain counterparts on the same configurations."""
 import numpy as np
 import pytest
 
@@ -41,7 +42,7 @@ def _random_case(seed):
     return T, H, bounds, vreal, vpad, bias, tau
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_configuration_all_entry_points(lp, seed):
     import torch
     T, H, bounds, vreal, vpad, bias, tau = _random_case(seed)
@@ -111,3 +112,39 @@ def test_random_configuration_all_entry_points(lp, seed):
             continue
         assert rel_fro(_np(bw["dW"][k]), bref.dW[k]) <= TOL_GRAD_REL, (ctx, k)
         assert rel_fro(_np(bw["db"][k]), bref.db[k]) <= TOL_GRAD_REL, (ctx, k)
+
+    # the same gradient with a bf16 dX, and accumulated onto random fp32 buffers
+    dX16 = lp.lp_backward_ex(X, W, b, P, y, inp.tau, fwd["lse"], dev_f32(g), entropy=fwd["entropy"],
+                             grad_entropy=dev_f32(h), dx_dtype=torch.bfloat16)["dX"]
+    assert torch.equal(dX16, bw["dX"].to(torch.bfloat16)), ctx
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    dW0 = [None if d is None else torch.randn(d.shape, generator=gen, device="cuda") for d in bw["dW"]]
+    db0 = [None if d is None else torch.randn(d.shape, generator=gen, device="cuda") for d in bw["db"]]
+    acc = lp.lp_backward_ex(X, W, b, P, y, inp.tau, fwd["lse"], dev_f32(g), entropy=fwd["entropy"],
+                            grad_entropy=dev_f32(h), accumulate=True,
+                            dW=[None if d is None else d.clone() for d in dW0],
+                            db=[None if d is None else d.clone() for d in db0])
+    for k, (s0, e0) in enumerate(part.ranges):
+        if e0 == s0:
+            continue
+        r = max(min(e0, vreal) - s0, 0)
+        assert torch.equal(acc["dW"][k][:r], dW0[k][:r] + bw["dW"][k][:r]), (ctx, k)
+        assert torch.equal(acc["dW"][k][r:], dW0[k][r:]), (ctx, k)
+        assert torch.equal(acc["db"][k][:r], db0[k][:r] + bw["db"][k][:r]), (ctx, k)
+
+    # gradient with respect to the reused logits, against the oracle
+    dL = lp.lp_backward_from_logits(Ld, P, y, inp.tau, lg["lse"], dev_f32(g), entropy=lg["entropy"],
+                                    grad_entropy=dev_f32(h), out_dtype=torch.float32)
+    dref = oracle.backward_from_logits(Lbits, part, inp.y, inp.tau, g, h=h)
+    for k, (d, r) in enumerate(zip(dL, dref)):
+        if r.shape[1] == 0:
+            assert d is None, (ctx, k)
+            continue
+        assert rel_fro(_np(d), r) <= TOL_GRAD_REL, (ctx, k)
+
+    # the host entry point gives the device forward's bits
+    hX = torch.from_numpy(inp.X.view(np.int16)).view(torch.bfloat16)
+    ho = lp.lp_forward_host(hX, W, b, P, torch.from_numpy(inp.y), inp.tau, shard_stats=True)
+    for k in ("logp", "lse", "entropy", "shard_stats"):
+        assert torch.equal(ho[k], fwd[k].cpu()), (ctx, k)
+    assert lp.lp_get_device_error() == 0, ctx
