@@ -284,3 +284,36 @@ def test_backward_with_entropy_gradient_parity(lp, T, H, bounds, real, bias):
     # and the entropy term is really there: without it the result is far off
     plain = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g)
     assert rel_fro(plain.dX, ref.dX) > 3 * TOL_GRAD_REL
+
+
+def test_many_row_blocks_forward_replay_logits_backward(lp):
+    # T = 70000 rows (547 row blocks, 8750 replay CTAs) with a small vocabulary: sampled rows
+    # against the oracle, and dW / db in full (the oracle's T x V x H is small here)
+    import torch
+    part = synth.ranges_partition(1000, 1024, [0, 512, 1024])
+    T, H = 70000, 64
+    inp = synth.forward_inputs(T, H, part, tau=0.8, seed=77, w_std=0.3, bias_std=0.1)
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, T - 129, T - 1],
+                                     np.random.default_rng(78).choice(T, 200, replace=False)]))
+    fwd = lp.lp_forward(X, W, b, P, y, inp.tau)
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, rows=rows)
+    assert max_abs(_np(fwd["logp"])[rows], ref.logp) <= TOL_LOGP
+    assert max_abs(_np(fwd["entropy"])[rows], ref.entropy) <= TOL_ENT
+    ids, yr = synth.replay_ids(T, part, seed=79)
+    rp = lp.lp_top_p_replay(X, W, b, P, dev_i32(ids), dev_i32(yr), inp.tau)
+    rref = oracle.top_p_replay(inp.X, inp.W, inp.bias, part, ids, yr, inp.tau, rows=rows)
+    assert max_abs(_np(rp["lse"])[rows], rref.lse) <= TOL_LSE
+    g = synth.upstream_grad(T, seed=80)
+    bw = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], dev_f32(g))
+    assert lp.lp_get_device_error() == 0
+    bref = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g)
+    assert rel_fro(_np(bw["dX"])[rows], bref.dX[rows]) <= TOL_GRAD_REL
+    for k in range(2):
+        assert rel_fro(_np(bw["dW"][k]), bref.dW[k]) <= TOL_GRAD_REL, k
+        assert rel_fro(_np(bw["db"][k]), bref.db[k]) <= TOL_GRAD_REL, k
+    # the first 4096 rows alone give the same forward bits (batch invariance at this size)
+    head = lp.lp_forward(X[:4096].contiguous(), W, b, P, y[:4096].contiguous(), inp.tau)
+    assert torch.equal(head["logp"], fwd["logp"][:4096]) and torch.equal(head["lse"], fwd["lse"][:4096])
