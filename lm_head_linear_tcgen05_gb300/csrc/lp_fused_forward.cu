@@ -193,43 +193,78 @@ struct LogpEpi : GemmEpiBase {
 };
 
 // ------------------------------------------------------------------ merge
-// One warp per row. Within a shard, lane l folds the shard's vocabulary blocks
-// l, l+32, ... in ascending order, then the lanes are combined by a fixed shuffle
-// tree; shards are folded in ascending order by lane 0 (the rank-ordered reduction
-// of page "Perf/cuda compact top p replay", Summary).
-__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeParams p) {
-  const int row = int((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= p.T) return;
-  const int yv = __ldg(p.y + row);
-  const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
-  Stat tot = stat_empty();
+// The statistics of vocabulary block nb for row t sit at slot nb * T + t, so consecutive
+// rows are adjacent. A block of 256 threads takes 8 rows: thread (g, r) with r = tid % 8
+// and g = tid / 8 folds, for row r, the blocks nb = g, g + 32, ... of each shard in
+// ascending order, so every load instruction of a warp reads whole 32-byte sectors (4
+// groups x 8 adjacent rows). The 32 partials of a row are then combined in a fixed order:
+// a shuffle tree over the warp's 4 groups, then the 8 warps in ascending order; shards are
+// folded in ascending order (the rank-ordered reduction of page "Perf/cuda compact top p
+// replay", Summary). The order depends only on the vocabulary layout, never on T.
+constexpr int kMergeRows = 8;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeGroups = kMergeThreads / kMergeRows;  // 32
+constexpr int kMergeWarps = kMergeThreads / 32;           // 8
+constexpr int kMergeBatch = 8;                            // blocks per thread loaded ahead of folding
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeParams p) {
+  __shared__ Stat part[kMergeWarps][kMergeRows];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int r = tid % kMergeRows;
+  const int g = tid / kMergeRows;
+  const int row = int(blockIdx.x) * kMergeRows + r;
+  const bool in_rows = row < p.T;
   const size_t T = size_t(p.T);
+  Stat tot = stat_empty();  // meaningful in threads tid < kMergeRows
   for (int k = 0; k < p.n_shards; ++k) {
     Stat loc = stat_empty();
-    for (int nb = p.nb_start[k] + lane; nb < p.nb_start[k + 1]; nb += 32) {
-      const size_t slot = size_t(nb) * T + size_t(row);
-      const Stat b{__ldg(p.ws_m + slot), __ldg(p.ws_s + slot), __ldg(p.ws_a + slot)};
-      stat_merge(loc, b);
-    }
+    if (in_rows) {
+      const int nb_end = p.nb_start[k + 1];
+      // batches of kMergeBatch blocks: all their loads are issued before the (dependent) folds
+      for (int nb0 = p.nb_start[k] + g; nb0 < nb_end; nb0 += kMergeBatch * kMergeGroups) {
+        float m[kMergeBatch], sm[kMergeBatch], am[kMergeBatch];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
+        for (int i = 0; i < kMergeBatch; ++i) {
+          const int nb = nb0 + i * kMergeGroups;
+          const size_t slot = size_t(nb < nb_end ? nb : nb0) * T + size_t(row);
+          m[i] = __ldg(p.ws_m + slot);
+          sm[i] = __ldg(p.ws_s + slot);
+          am[i] = __ldg(p.ws_a + slot);
+        }
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i)
+          if (nb0 + i * kMergeGroups < nb_end) stat_merge(loc, Stat{m[i], sm[i], am[i]});
+      }
+    }
+    // the warp's four groups of this row: lanes r, r + 8, r + 16, r + 24
+#pragma unroll
+    for (int off = 16; off >= kMergeRows; off >>= 1) {
       const Stat o{__shfl_down_sync(0xffffffffu, loc.m, off), __shfl_down_sync(0xffffffffu, loc.s, off),
                    __shfl_down_sync(0xffffffffu, loc.a, off)};
       if (lane < off) stat_merge(loc, o);
     }
-    if (lane == 0) {
+    if (lane < kMergeRows) part[warp][lane] = loc;
+    __syncthreads();
+    if (tid < kMergeRows && in_rows) {
+      Stat sh = part[0][tid];
+      for (int w = 1; w < kMergeWarps; ++w) stat_merge(sh, part[w][tid]);
       if (p.shard_stats != nullptr) {
-        const bool own = y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k];
+        const int yv = __ldg(p.y + row);
+        const bool own = yv >= 0 && int64_t(yv) < p.vocab_real && yv >= p.shard_start[k] && yv < p.shard_end[k];
         float* ss = p.shard_stats + size_t(k) * 3 * T;
-        ss[row] = stat_lse(loc);
+        ss[row] = stat_lse(sh);
         ss[T + row] = own ? p.ws_t[row] : 0.f;
-        ss[2 * T + row] = stat_mean(loc);
+        ss[2 * T + row] = stat_mean(sh);
       }
-      stat_merge(tot, loc);
+      stat_merge(tot, sh);
     }
+    __syncthreads();  // part is rewritten for the next shard
   }
-  if (lane == 0) {
+  if (tid < kMergeRows && in_rows) {
+    const int yv = __ldg(p.y + row);
+    const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
     const float lse = stat_lse(tot);
     p.lse[row] = lse;
     if (p.entropy != nullptr) p.entropy[row] = stat_entropy(tot);
@@ -243,9 +278,8 @@ cudaError_t launch_fused_forward(const FwdParams& p, int num_sms, cudaStream_t s
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
-  const int rows_per_block = 8;
-  const int grid = (p.T + rows_per_block - 1) / rows_per_block;
-  merge_kernel<<<grid, 32 * rows_per_block, 0, s>>>(p);
+  const int grid = (p.T + kMergeRows - 1) / kMergeRows;
+  merge_kernel<<<grid, kMergeThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
