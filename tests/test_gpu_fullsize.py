@@ -196,3 +196,32 @@ def test_replay_from_logits_full_size(lp):
     ss = _np(out["shard_stats"])
     for k in range(4):
         assert max_abs(ss[k, 0][rows], ref.shard_lse[k]) <= TOL_LSE
+
+
+@pytest.mark.parametrize("T,Hh,Vv,shards", [(2048, 8192, 128256, 2), (1024, 2048, 262144 - 517, 4)])
+def test_other_lm_head_shapes_sampled_rows(lp, T, Hh, Vv, shards):
+    # larger hidden size with a 128256-id vocabulary in two shards, and a wide vocabulary whose
+    # size is not a multiple of any tile (padded to split evenly): sampled rows against the
+    # oracle, the backward's dX on a few rows, and batch invariance on a row slice
+    import torch
+    Vpad = -(-Vv // (shards * 64)) * shards * 64
+    w = Vpad // shards
+    part = synth.ranges_partition(Vv, Vpad, [k * w for k in range(shards + 1)])
+    inp = synth.forward_inputs(T, Hh, part, tau=0.9, seed=T + Hh, w_std=0.02, bias_std=0.01)
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    out = lp.lp_forward(X, W, b, P, y, inp.tau)
+    assert lp.lp_get_device_error() == 0
+    rows = _sample_rows(T, 24, Hh)
+    ref = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, rows=rows)
+    assert max_abs(_np(out["logp"])[rows], ref.logp) <= TOL_LOGP
+    assert max_abs(_np(out["lse"])[rows], ref.lse) <= TOL_LSE
+    assert max_abs(_np(out["entropy"])[rows], ref.entropy) <= TOL_ENT
+    sl = lp.lp_forward(X[100:612].contiguous(), W, b, P, y[100:612].contiguous(), inp.tau)
+    assert torch.equal(sl["logp"], out["logp"][100:612]) and torch.equal(sl["entropy"], out["entropy"][100:612])
+    g = synth.upstream_grad(T, seed=Hh)
+    bw = lp.lp_backward(X, W, b, P, y, inp.tau, out["lse"], dev_f32(g))
+    assert lp.lp_get_device_error() == 0
+    dx_rows = rows[:6]
+    dX, _, _ = oracle.backward_sampled(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g, dx_rows, [[]] * shards)
+    assert rel_fro(_np(bw["dX"])[dx_rows], dX) <= TOL_GRAD_REL
