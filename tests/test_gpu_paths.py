@@ -195,7 +195,7 @@ def test_backward_parity(lp, T, H, bounds, real, bias):
         assert np.all(_np(bw["dW"][k])[pad] == 0) and np.all(_np(bw["db"][k])[pad] == 0)
 
 
-def test_backward_bitwise_repeatable(lp):
+def test_backward_bitwise_repeatable_and_dx_batch_invariant(lp):
     import torch
     part = synth.ranges_partition(3000, 3072, [0, 1500, 3072])
     inp = synth.forward_inputs(300, 256, part, tau=0.7, seed=2, bias_std=0.1)
@@ -208,6 +208,22 @@ def test_backward_bitwise_repeatable(lp):
     assert torch.equal(a["dX"], c["dX"])
     for k in range(2):
         assert torch.equal(a["dW"][k], c["dW"][k]) and torch.equal(a["db"][k], c["db"][k])
+    # a row's dX depends only on that row: the same rows in another batch give the same bits,
+    # also with 70000 K columns split into two fixed K ranges
+    for lo, hi in ((0, 1), (37, 300), (129, 257)):
+        sub = lp.lp_backward(X[lo:hi].contiguous(), W, b, P, y[lo:hi].contiguous(), inp.tau,
+                             fwd["lse"][lo:hi].contiguous(), g[lo:hi].contiguous())
+        assert torch.equal(sub["dX"], a["dX"][lo:hi]), (lo, hi)
+    part2 = synth.ranges_partition(70000, 70016, [0, 35008, 70016])
+    inp2 = synth.forward_inputs(260, 128, part2, tau=0.7, seed=3, w_std=0.05)
+    X2, W2, _, y2 = dev_inputs(inp2)
+    P2 = part_of(part2)
+    g2 = dev_f32(synth.upstream_grad(260, seed=3))
+    f2 = lp.lp_forward(X2, W2, None, P2, y2, inp2.tau)
+    full = lp.lp_backward(X2, W2, None, P2, y2, inp2.tau, f2["lse"], g2)["dX"]
+    sub = lp.lp_backward(X2[3:200].contiguous(), W2, None, P2, y2[3:200].contiguous(), inp2.tau,
+                         f2["lse"][3:200].contiguous(), g2[3:200].contiguous())["dX"]
+    assert torch.equal(sub, full[3:200])
 
 
 # ---------------------------------------------------------- logits-gather replay
