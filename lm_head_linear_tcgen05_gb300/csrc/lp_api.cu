@@ -271,6 +271,7 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
   const int64_t mblocks = (T + kFwdBlockM - 1) / kFwdBlockM;  // row blocks, counted in whole clusters
   p.num_m_blocks = int32_t((mblocks + kFwdClusterM - 1) / kFwdClusterM * kFwdClusterM);
   p.num_k_blocks = int32_t((H + kFwdBlockK - 1) / kFwdBlockK);
+  p.m_chunk = proj_row_chunk(H, p.num_m_blocks);
   p.total_tiles = nb * p.num_m_blocks;
   p.err = dev->err;
   p.wait_limit_ns = kDefaultWaitLimitNs;

@@ -172,6 +172,7 @@ struct GradParams {
   int32_t T;
   int32_t num_m_blocks;
   int32_t num_k_blocks;
+  int32_t m_chunk;  // row blocks per tile-order chunk
   float scale_log2;
   float inv_tau;
 };
@@ -186,8 +187,8 @@ struct GradEpi : GemmEpiBase {
 
   static __device__ __forceinline__ Coord coord(const Params& p, int tile) {
     Coord c;
-    c.mb = tile % p.num_m_blocks;
-    const int nbg = tile / p.num_m_blocks;
+    int nbg;
+    proj_raster(tile, p.num_m_blocks, p.m_chunk, p.nb_start[p.n_shards], c.mb, nbg);
     int k = 0;
     while (k + 1 < p.n_shards && nbg >= p.nb_start[k + 1]) ++k;
     c.shard = k;
@@ -543,6 +544,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.T = int32_t(T);
     p.num_m_blocks = pad_to_cluster((T + kFwdBlockM - 1) / kFwdBlockM);
     p.num_k_blocks = int32_t((H + kFwdBlockK - 1) / kFwdBlockK);
+    p.m_chunk = proj_row_chunk(H, p.num_m_blocks);
     p.total_tiles = nb * p.num_m_blocks;
     p.err = a.err;
     p.wait_limit_ns = kDefaultWaitLimitNs;

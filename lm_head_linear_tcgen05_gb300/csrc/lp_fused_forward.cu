@@ -90,8 +90,7 @@ struct TileCoord {
 
 __device__ __forceinline__ TileCoord fwd_coord(const FwdParams& p, int tile) {
   TileCoord c;
-  c.mb = tile % p.num_m_blocks;
-  c.nb_global = tile / p.num_m_blocks;
+  proj_raster(tile, p.num_m_blocks, p.m_chunk, p.nb_start[p.n_shards], c.mb, c.nb_global);
   int k = 0;
   while (k + 1 < p.n_shards && c.nb_global >= p.nb_start[k + 1]) ++k;
   c.shard = k;

@@ -58,9 +58,21 @@ struct FwdParams {
   int32_t T;
   int32_t num_m_blocks;
   int32_t num_k_blocks;
+  int32_t m_chunk;                      // row blocks per tile-order chunk (proj_row_chunk)
   float scale_log2;                     // log2(e) / tau
   float inv_tau;                        // 1 / tau
 };
+
+// Row blocks per chunk of the projection GEMMs' tile order: every vocabulary block of a
+// chunk is visited before the next chunk starts, so a chunk's rows of X (at most 32 MiB)
+// stay in L2 while W streams past them once per chunk. A multiple of the cluster size.
+inline int32_t proj_row_chunk(int64_t H, int64_t num_m_blocks) {
+  const int64_t per_block = int64_t(kFwdBlockM) * H * 2;
+  int64_t m = (int64_t(32) << 20) / per_block / kFwdClusterM * kFwdClusterM;
+  if (m < kFwdClusterM) m = kFwdClusterM;
+  if (m > num_m_blocks) m = num_m_blocks;
+  return int32_t(m);
+}
 
 // Merge of per-tile (or per-chunk) statistics, one warp per row.
 struct MergeParams {

@@ -65,6 +65,20 @@ constexpr uint32_t kGemmStageB = kGemmBlockN * kGemmBlockK * 2;  // 32 KB
 
 constexpr uint32_t kMNAtomBytes = 64 * kGemmBlockK * 2;  // 64 MN elements x 64 K rows: 8 KB
 
+// Tile order of the projection GEMMs: row blocks in chunks of m_chunk (see
+// proj_row_chunk), and inside a chunk row blocks fastest, then vocabulary blocks. Pairs
+// of tiles (2j, 2j+1) stay two row blocks of one vocabulary block, as clusters need.
+__device__ __forceinline__ void proj_raster(int tile, int num_m_blocks, int m_chunk, int nb_total, int& mb,
+                                            int& nb) {
+  const int per_chunk = m_chunk * nb_total;
+  const int c = tile / per_chunk;
+  const int r = tile - c * per_chunk;
+  const int m0 = c * m_chunk;
+  const int rows = num_m_blocks - m0 < m_chunk ? num_m_blocks - m0 : m_chunk;
+  mb = m0 + r % rows;
+  nb = r / rows;
+}
+
 // What one tile reads: rows (MN indices) a_y.. of map a_map and b_y.. of map b_map,
 // for k blocks kb0 .. kb0 + nkb - 1; nkb >= 1. A K-major operand is one box at
 // (x = k, y = row); an MN-major one is a row of 64-wide atoms at (x = mn, y = k).
