@@ -333,3 +333,34 @@ def test_many_row_blocks_forward_replay_logits_backward(lp):
     # the first 4096 rows alone give the same forward bits (batch invariance at this size)
     head = lp.lp_forward(X[:4096].contiguous(), W, b, P, y[:4096].contiguous(), inp.tau)
     assert torch.equal(head["logp"], fwd["logp"][:4096]) and torch.equal(head["lse"], fwd["lse"][:4096])
+
+
+def test_projection_row_chunks_forward_and_backward(lp):
+    # T = 9000 rows at H = 4096 makes the projection GEMMs take their rows in three chunks
+    # (4096, 4096, 808): the forward and dX must equal the same rows computed as their own
+    # batches bit for bit, and dW / db must match the oracle over all 9000 rows
+    import torch
+    part = synth.ranges_partition(4000, 4096, [0, 2048, 4096])
+    T, H = 9000, 4096
+    inp = synth.forward_inputs(T, H, part, tau=0.7, seed=90, w_std=0.01, bias_std=0.05)
+    X, W, b, y = dev_inputs(inp)
+    P = part_of(part)
+    fwd = lp.lp_forward(X, W, b, P, y, inp.tau)
+    g = dev_f32(synth.upstream_grad(T, seed=91))
+    bw = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], g)
+    assert lp.lp_get_device_error() == 0
+    for lo, hi in ((0, 4096), (4096, 8192), (8192, 9000), (3000, 5000)):
+        sub = lp.lp_forward(X[lo:hi].contiguous(), W, b, P, y[lo:hi].contiguous(), inp.tau)
+        assert torch.equal(sub["logp"], fwd["logp"][lo:hi]) and torch.equal(sub["lse"], fwd["lse"][lo:hi]), (lo, hi)
+        sb = lp.lp_backward(X[lo:hi].contiguous(), W, b, P, y[lo:hi].contiguous(), inp.tau,
+                            fwd["lse"][lo:hi].contiguous(), g[lo:hi].contiguous())
+        assert torch.equal(sb["dX"], bw["dX"][lo:hi]), (lo, hi)
+    rows = np.unique(np.concatenate([[0, 4095, 4096, 8191, 8192, 8999],
+                                     np.random.default_rng(92).choice(T, 40, replace=False)]))
+    ref = oracle.forward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, rows=rows)
+    assert max_abs(_np(fwd["logp"])[rows], ref.logp) <= TOL_LOGP
+    bref = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, _np(g))
+    assert rel_fro(_np(bw["dX"])[rows], bref.dX[rows]) <= TOL_GRAD_REL
+    for k in range(2):
+        assert rel_fro(_np(bw["dW"][k]), bref.dW[k]) <= TOL_GRAD_REL, k
+        assert rel_fro(_np(bw["db"][k]), bref.db[k]) <= TOL_GRAD_REL, k
