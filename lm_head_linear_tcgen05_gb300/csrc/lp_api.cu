@@ -253,10 +253,14 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_bf16_2d(&p.maps[0], X, uint64_t(H), uint64_t(T), uint64_t(H), kFwdBlockM)) return LP_ERR_CUDA;
+  // a batch of a single row block runs without clusters (launch_fused_forward): each CTA
+  // fetches its whole W box, instead of half of it for a partner CTA with padding rows
+  const int64_t mblocks = (T + kFwdBlockM - 1) / kFwdBlockM;
+  const int cm = mblocks == 1 ? 1 : kFwdClusterM;
   int nb = 0;
   for (int k = 0; k < sh.n; ++k) {
     if (sh.real[k] > 0 && !encode_bf16_2d(&p.maps[1 + k], W[k], uint64_t(H), uint64_t(sh.width[k]), uint64_t(H),
-                                          kFwdBlockN / kFwdClusterM))
+                                          uint32_t(kFwdBlockN / cm)))
       return LP_ERR_CUDA;
     p.bias[k] = bias != nullptr ? static_cast<const __nv_bfloat16*>(bias[k]) : nullptr;
     p.shard_start[k] = sh.start[k];
@@ -268,8 +272,7 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
   p.keep_maps = 1u;  // X is re-read by every vocabulary block: keep it in L2
   p.n_shards = sh.n;
   p.T = int32_t(T);
-  const int64_t mblocks = (T + kFwdBlockM - 1) / kFwdBlockM;  // row blocks, counted in whole clusters
-  p.num_m_blocks = int32_t((mblocks + kFwdClusterM - 1) / kFwdClusterM * kFwdClusterM);
+  p.num_m_blocks = int32_t((mblocks + cm - 1) / cm * cm);  // row blocks, counted in whole clusters
   p.num_k_blocks = int32_t((H + kFwdBlockK - 1) / kFwdBlockK);
   p.m_chunk = proj_row_chunk(H, p.num_m_blocks);
   p.total_tiles = nb * p.num_m_blocks;

@@ -100,9 +100,13 @@ __device__ __forceinline__ TileCoord fwd_coord(const FwdParams& p, int tile) {
 
 }  // namespace
 
+// CM CTAs per cluster along M: kFwdClusterM in general, 1 when the batch is a single row
+// block (the second row block of a pair would be padding only). Both compute every tile
+// identically - only who fetches the W box differs - so a row's bits do not depend on it.
+template <int CM>
 struct LogpEpi : GemmEpiBase {
   using Params = FwdParams;
-  static constexpr int kClusterM = kFwdClusterM;
+  static constexpr int kClusterM = CM;
 
   static __device__ __forceinline__ TileJob job(const Params& p, int tile) {
     const TileCoord c = fwd_coord(p, tile);
@@ -273,7 +277,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 }
 
 cudaError_t launch_fused_forward(const FwdParams& p, int num_sms, cudaStream_t s) {
-  return launch_tc_gemm<LogpEpi>(p, num_sms, s);
+  // the W maps were encoded with boxes of kGemmBlockN / cluster rows to match (lp_api.cu)
+  if (p.num_m_blocks == 1) return launch_tc_gemm<LogpEpi<1>>(p, num_sms, s);
+  return launch_tc_gemm<LogpEpi<kFwdClusterM>>(p, num_sms, s);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
