@@ -252,11 +252,14 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
 
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
-  if (!encode_bf16_2d(&p.maps[0], X, uint64_t(H), uint64_t(T), uint64_t(H), kFwdBlockM)) return LP_ERR_CUDA;
   // a batch of a single row block runs without clusters (launch_fused_forward): each CTA
-  // fetches its whole W box, instead of half of it for a partner CTA with padding rows
+  // fetches its whole W box, instead of half of it for a partner CTA with padding rows, and
+  // its X boxes hold only the batch's rows (rounded up to 16)
   const int64_t mblocks = (T + kFwdBlockM - 1) / kFwdBlockM;
   const int cm = mblocks == 1 ? 1 : kFwdClusterM;
+  p.a_box_rows = cm == 1 ? int32_t((T + 15) / 16 * 16) : kFwdBlockM;
+  if (!encode_bf16_2d(&p.maps[0], X, uint64_t(H), uint64_t(T), uint64_t(H), uint32_t(p.a_box_rows)))
+    return LP_ERR_CUDA;
   int nb = 0;
   for (int k = 0; k < sh.n; ++k) {
     if (sh.real[k] > 0 && !encode_bf16_2d(&p.maps[1 + k], W[k], uint64_t(H), uint64_t(sh.width[k]), uint64_t(H),

@@ -107,6 +107,9 @@ template <int CM>
 struct LogpEpi : GemmEpiBase {
   using Params = FwdParams;
   static constexpr int kClusterM = CM;
+  // a single row block loads only its T (rounded up to 16) rows of X: a 128-row box that is
+  // nearly all out-of-bounds fill slowed the W stream of tiny batches (T <= 8) by ~20 %
+  static constexpr bool kVarABox = CM == 1;
 
   static __device__ __forceinline__ TileJob job(const Params& p, int tile) {
     const TileCoord c = fwd_coord(p, tile);

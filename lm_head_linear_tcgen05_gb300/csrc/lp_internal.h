@@ -59,6 +59,7 @@ struct FwdParams {
   int32_t num_m_blocks;
   int32_t num_k_blocks;
   int32_t m_chunk;                      // row blocks per tile-order chunk (proj_row_chunk)
+  int32_t a_box_rows;                   // rows of the X boxes (a batch of one row block: T rounded up to 16)
   float scale_log2;                     // log2(e) / tau
   float inv_tau;                        // 1 / tau
 };

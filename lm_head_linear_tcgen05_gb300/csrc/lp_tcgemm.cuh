@@ -94,6 +94,9 @@ struct GemmEpiBase {
   static constexpr bool kAMN = false;  // A operand MN-major
   static constexpr bool kBMN = false;  // B operand MN-major
   static constexpr int kMHalves = 1;   // 128-row halves per CTA tile (2: 256 rows, single accumulator)
+  // K-major A boxes of p.a_box_rows (<= 128) rows instead of 128: the rows of the A tile
+  // past them keep stale shared memory, so only output rows < a_box_rows are meaningful
+  static constexpr bool kVarABox = false;
   static __device__ __forceinline__ void a_k(const void*, const TileJob& j, int kb, int& map, int& k) {
     map = j.a_map;
     k = (j.kb0 + kb) * kFwdBlockK;
@@ -183,6 +186,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       // --------------------------------------------------------- TMA producer
       const uint64_t pol_keep = l2_policy_evict_last();
       const uint64_t pol_norm = l2_policy_evict_normal();
+      uint32_t stage_tx = S::kStageBytes;  // bytes that complete one stage
+      if constexpr (E::kVarABox) {
+        static_assert(kMH == 1 && !E::kAMN, "short A boxes: one K-major 128-row half");
+        stage_tx = kGemmStageB + uint32_t(p.a_box_rows) * (kGemmBlockK * 2);
+      }
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, armed_phase = 0;  // stages with a copy issued, and its phase
       bool ok = true;
@@ -198,7 +206,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           int am, ak, bm, bk;
           E::a_k(&p, j, kb, am, ak);
           E::b_k(&p, j, kb, bm, bk);
-          mbar_arrive_expect_tx(&sync->full[stage], S::kStageBytes);
+          mbar_arrive_expect_tx(&sync->full[stage], stage_tx);
           uint8_t* dA = sA + stage * S::kStageA;
           uint8_t* dB = sB + stage * kGemmStageB;
           if constexpr (!E::kAMN) {
