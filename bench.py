@@ -375,7 +375,7 @@ def run_ours(args, rank, world, dist):
         "paths": paths,
         "bitwise": {"repeat": bit_repeat, f"1x{T_FWD}_vs_{-(-T_FWD // chunk)}x{chunk}": bit_batch},
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the host-core oracle runs at N = 1 only
         line["cpu_baseline"], line["parity"] = cpu_baseline_forward(X, W, y, base, rows=64)
     print(json.dumps(line), flush=True)
 
