@@ -20,8 +20,19 @@ def _has_gpu():
         return False
 
 
+# Every GPU test gets a time limit (pytest-timeout, where installed) so that a test that
+# stalls ends with a failure instead of holding the GPU; the kernels' own waits are bounded
+# at 2 s, so this only guards the host side.
+GPU_TEST_TIMEOUT_S = 1200
+
+
 def pytest_collection_modifyitems(config, items):
+    has_timeout = config.pluginmanager.hasplugin("timeout")
     if _has_gpu():
+        if has_timeout:
+            for it in items:
+                if "gpu" in it.keywords and it.get_closest_marker("timeout") is None:
+                    it.add_marker(pytest.mark.timeout(GPU_TEST_TIMEOUT_S))
         return
     skip = pytest.mark.skip(reason="no CUDA device in this process")
     for it in items:

@@ -95,6 +95,21 @@ def test_random_configuration_all_entry_points(lp, seed):
     assert lp.lp_get_device_error() == 0, ctx
     assert max_abs(_np(rp["lse"]), rref.lse) <= TOL_LSE, ctx
     assert max_abs(_np(rp["logp"]), rref.logp) <= TOL_LOGP, ctx
+    # the dense keep-mask route over the same sets: bitwise equal, whatever the shard
+    # offsets and empty shards of this partition
+    ids_d = dev_i32(ids)
+    masks = []
+    for k, (s0, e0) in enumerate(part.ranges):
+        if e0 == s0:
+            masks.append(None)
+            continue
+        m = torch.zeros((T, e0 - s0), dtype=torch.uint8, device="cuda")
+        sel = (ids_d >= s0) & (ids_d < e0)
+        rr = torch.arange(T, device="cuda").unsqueeze(1).expand_as(ids_d)[sel]
+        m[rr.long(), (ids_d[sel] - s0).long()] = 1
+        masks.append(m)
+    dm = lp.lp_top_p_replay_dense_mask(X, W, b, P, masks, dev_i32(yr), inp.tau)
+    assert torch.equal(dm["lse"], rp["lse"]) and torch.equal(dm["logp"], rp["logp"]), ctx
     rq = lp.lp_top_p_replay_from_logits(Ld, P, dev_i32(ids), dev_i32(yr), inp.tau)
     qref = oracle.top_p_replay_from_logits(Lbits, part, ids, yr, inp.tau)
     assert max_abs(_np(rq["lse"]), qref.lse) <= TOL_LSE, ctx
