@@ -376,7 +376,7 @@ def run_ours(args, rank, world, dist):
         "bitwise": {"repeat": bit_repeat, f"1x{T_FWD}_vs_{-(-T_FWD // chunk)}x{chunk}": bit_batch},
     }
     if not args.no_cpu_baseline and world == 1:  # the host-core oracle runs at N = 1 only
-        line["cpu_baseline"], line["parity"] = cpu_baseline_forward(X, W, y, base, rows=640)
+        line["cpu_baseline"], line["parity"] = cpu_baseline_forward(X, W, y, base, rows=1536)
     print(json.dumps(line), flush=True)
 
 
@@ -496,7 +496,7 @@ def cpu_cores():
 
 def cpu_baseline_forward(X, W, y, gpu_out, rows: int):
     """The fp64 oracle on `rows` rows of the timed workload itself (full H and V; rows spread
-    evenly over T; 640 rows are ~10 s of host work): its speed on the host cores, and the GPU
+    evenly over T; 1536 rows are ~10 s of host work): its speed on the host cores, and the GPU
     outputs' largest deviation from it on those rows."""
     import numpy as np
     import torch
