@@ -231,22 +231,27 @@ LP_API lp_status lp_backward(const void* X, int64_t T, int64_t H,
  *   accumulate  0: dW[k] and db[k] are overwritten; 1: the gradient is added to what
  *               they hold (one fp32 add per element after the fixed-order sum, so the
  *               result is still deterministic); padded ids keep their old values and
- *               an empty batch leaves both untouched. dX is always overwritten. */
+ *               an empty batch leaves both untouched. dX is always overwritten.
+ *   dw_dtype    LP_DTYPE_F32: dW[k] is float [V_k,H]; LP_DTYPE_BF16: bf16 [V_k,H], the
+ *               same fp32 result rounded once to bf16 (half the largest write of the
+ *               backward). Accumulation needs fp32 dW. db is always fp32. */
 typedef struct {
   int32_t dx_dtype;
   int32_t accumulate;
+  int32_t dw_dtype;
 } lp_backward_options;
 
-/* lp_backward with output options; opts NULL means {LP_DTYPE_F32, 0}, which makes it
- * identical to lp_backward. dX points to float or bf16 per opts->dx_dtype (16-byte
- * aligned either way). Same workspace (LP_OP_BACKWARD) and errors as lp_backward,
- * plus LP_ERR_INVALID_ARG for an unknown dx_dtype or accumulate not 0/1. */
+/* lp_backward with output options; opts NULL means {LP_DTYPE_F32, 0, LP_DTYPE_F32}, which
+ * makes it identical to lp_backward. dX and the dW[k] point to float or bf16 per
+ * opts->dx_dtype / opts->dw_dtype (16-byte aligned either way). Same workspace
+ * (LP_OP_BACKWARD) and errors as lp_backward, plus LP_ERR_INVALID_ARG for an unknown
+ * dtype, accumulate not 0/1, or accumulation into bf16 dW. */
 LP_API lp_status lp_backward_ex(const void* X, int64_t T, int64_t H,
                                 const void* const* W, const void* const* bias,
                                 const lp_vocab_partition* part, const int32_t* y, float tau,
                                 const float* lse, const float* grad_logp,
                                 const float* entropy, const float* grad_entropy,
-                                void* dX, float* const* dW, float* const* db,
+                                void* dX, void* const* dW, float* const* db,
                                 const lp_backward_options* opts,
                                 void* workspace, size_t ws_bytes, lp_stream_t stream);
 

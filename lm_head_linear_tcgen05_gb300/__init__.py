@@ -98,7 +98,7 @@ class _Outputs(ctypes.Structure):
 
 
 class _BackwardOptions(ctypes.Structure):
-    _fields_ = [("dx_dtype", ctypes.c_int32), ("accumulate", ctypes.c_int32)]
+    _fields_ = [("dx_dtype", ctypes.c_int32), ("accumulate", ctypes.c_int32), ("dw_dtype", ctypes.c_int32)]
 
 
 _lib = None
@@ -431,7 +431,7 @@ def lp_top_p_replay_dense_mask(X: torch.Tensor, W, bias, part, keep_mask: Sequen
 
 
 def _backward(fn: str, X: torch.Tensor, W, bias, part, y, tau, lse, grad_logp, bias_grad, workspace, entropy,
-              grad_entropy, dx_dtype, accumulate, dW, db) -> dict:
+              grad_entropy, dx_dtype, accumulate, dW, db, dw_dtype=torch.float32) -> dict:
     _check(X, "X", torch.bfloat16, 2)
     _check(y, "y", torch.int32, 1)
     _check(lse, "lse", torch.float32, 1)
@@ -441,8 +441,10 @@ def _backward(fn: str, X: torch.Tensor, W, bias, part, y, tau, lse, grad_logp, b
     if entropy is not None:
         _check(entropy, "entropy", torch.float32, 1)
         _check(grad_entropy, "grad_entropy", torch.float32, 1)
-    if dx_dtype not in _LP_DTYPES:
-        raise TypeError("dx_dtype must be torch.float32 or torch.bfloat16")
+    if dx_dtype not in _LP_DTYPES or dw_dtype not in _LP_DTYPES:
+        raise TypeError("dx_dtype and dw_dtype must be torch.float32 or torch.bfloat16")
+    if accumulate and dw_dtype != torch.float32:
+        raise ValueError("accumulation needs fp32 dW")
     n = len(part.ranges)
     W = _shard_list(W, n, "W", torch.bfloat16, 2, True)
     bias = _shard_list(bias, n, "bias", torch.bfloat16, 1, True) if bias is not None else None
@@ -456,10 +458,10 @@ def _backward(fn: str, X: torch.Tensor, W, bias, part, y, tau, lse, grad_logp, b
     if accumulate and (dW is None or (bias_grad and db is None)):
         raise ValueError("accumulate=True adds into the caller's dW (and db): pass them")
     if dW is not None:
-        dW = _shard_list(dW, n, "dW", torch.float32, 2, True)
+        dW = _shard_list(dW, n, "dW", dw_dtype, 2, True)
         for k, (t, w) in enumerate(zip(dW, widths)):
             if w and (t is None or tuple(t.shape) != (w, H)):
-                raise ValueError(f"dW[{k}] must be fp32 [{w}, {H}]")
+                raise ValueError(f"dW[{k}] must be {dw_dtype} [{w}, {H}]")
     if db is not None:
         db = _shard_list(db, n, "db", torch.float32, 1, True)
         for k, (t, w) in enumerate(zip(db, widths)):
@@ -471,7 +473,7 @@ def _backward(fn: str, X: torch.Tensor, W, bias, part, y, tau, lse, grad_logp, b
         ws, wsb = _workspace(need, X.device, workspace)
         dX = torch.empty((T, H), dtype=dx_dtype, device=X.device)
         if dW is None:
-            dW = [torch.empty((w, H), dtype=torch.float32, device=X.device) if w else None for w in widths]
+            dW = [torch.empty((w, H), dtype=dw_dtype, device=X.device) if w else None for w in widths]
         if db is None and bias_grad:
             db = [torch.empty(w, dtype=torch.float32, device=X.device) if w else None for w in widths]
         if not bias_grad:
@@ -481,7 +483,7 @@ def _backward(fn: str, X: torch.Tensor, W, bias, part, y, tau, lse, grad_logp, b
                 _ptr(entropy), _ptr(grad_entropy), dX.data_ptr(), _ptr_array(dW),
                 _ptr_array(db) if db is not None else None]
         if fn == "lp_backward_ex":
-            opts = _BackwardOptions(_LP_DTYPES[dx_dtype], 1 if accumulate else 0)
+            opts = _BackwardOptions(_LP_DTYPES[dx_dtype], 1 if accumulate else 0, _LP_DTYPES[dw_dtype])
             args.append(ctypes.byref(opts))
         st = getattr(lib(), fn)(*args, _ptr(ws), wsb, _stream(X.device))
     _raise(st, fn)
@@ -502,12 +504,14 @@ def lp_backward(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse
 def lp_backward_ex(X: torch.Tensor, W, bias, part, y: torch.Tensor, tau: float, lse: torch.Tensor,
                    grad_logp: torch.Tensor, bias_grad: bool = True, workspace: Optional[torch.Tensor] = None,
                    entropy: Optional[torch.Tensor] = None, grad_entropy: Optional[torch.Tensor] = None,
-                   dx_dtype=torch.float32, accumulate: bool = False, dW=None, db=None) -> dict:
-    """lp_backward with output options: ``dx_dtype`` torch.float32 or torch.bfloat16 (the
-    fp32 result rounded once); ``accumulate`` adds the weight and bias gradients into the
-    caller's fp32 ``dW`` / ``db`` lists (otherwise those, when given, are overwritten)."""
+                   dx_dtype=torch.float32, accumulate: bool = False, dW=None, db=None,
+                   dw_dtype=torch.float32) -> dict:
+    """lp_backward with output options: ``dx_dtype`` / ``dw_dtype`` torch.float32 or
+    torch.bfloat16 (the fp32 result rounded once); ``accumulate`` adds the weight and bias
+    gradients into the caller's fp32 ``dW`` / ``db`` lists (otherwise those, when given,
+    are overwritten)."""
     return _backward("lp_backward_ex", X, W, bias, part, y, tau, lse, grad_logp, bias_grad, workspace, entropy,
-                     grad_entropy, dx_dtype, accumulate, dW, db)
+                     grad_entropy, dx_dtype, accumulate, dW, db, dw_dtype)
 
 
 def lp_backward_from_logits(logits: Sequence[torch.Tensor], part, y: torch.Tensor, tau: float, lse: torch.Tensor,

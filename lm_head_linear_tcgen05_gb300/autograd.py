@@ -53,9 +53,11 @@ class _LinearLogp(torch.autograd.Function):
             return (None,) * (6 + len(wb))
         g = _f32(g_logp) if g_logp is not None else _zeros_like_rows(X)
         want_db = bias is not None and any(b is not None and b.requires_grad for b in bias)
+        # X and W are bf16, so their gradients are bf16: the library rounds its fp32 results
+        # once, as autograd's own cast would, and writes half the bytes
         r = lp_backward_ex(X, W, bias, ctx.part, y, ctx.tau, lse, g, bias_grad=want_db,
                            entropy=entropy if g_entropy is not None else None, grad_entropy=_f32(g_entropy),
-                           dx_dtype=torch.bfloat16 if X.dtype == torch.bfloat16 else torch.float32)
+                           dx_dtype=torch.bfloat16, dw_dtype=torch.bfloat16)
         dX = r["dX"] if ctx.needs_input_grad[0] else None
         dW = [d if ctx.needs_input_grad[6 + k] else None for k, d in enumerate(r["dW"])]
         db = [None] * n

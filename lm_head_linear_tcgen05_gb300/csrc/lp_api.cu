@@ -544,22 +544,24 @@ lp_status lp_backward(const void* X, int64_t T, int64_t H, const void* const* W,
                       const lp_vocab_partition* part, const int32_t* y, float tau, const float* lse,
                       const float* grad_logp, const float* entropy, const float* grad_entropy, float* dX,
                       float* const* dW, float* const* db, void* workspace, size_t ws_bytes, lp_stream_t stream) {
-  return lp_backward_ex(X, T, H, W, bias, part, y, tau, lse, grad_logp, entropy, grad_entropy, dX, dW, db, nullptr,
-                        workspace, ws_bytes, stream);
+  return lp_backward_ex(X, T, H, W, bias, part, y, tau, lse, grad_logp, entropy, grad_entropy, dX,
+                        reinterpret_cast<void* const*>(dW), db, nullptr, workspace, ws_bytes, stream);
 }
 
 lp_status lp_backward_ex(const void* X, int64_t T, int64_t H, const void* const* W, const void* const* bias,
                          const lp_vocab_partition* part, const int32_t* y, float tau, const float* lse,
                          const float* grad_logp, const float* entropy, const float* grad_entropy, void* dX,
-                         float* const* dW, float* const* db, const lp_backward_options* opts, void* workspace,
+                         void* const* dW, float* const* db, const lp_backward_options* opts, void* workspace,
                          size_t ws_bytes, lp_stream_t stream) {
   Shards sh;
   if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
   if (!valid_rows(T) || !valid_hidden(H) || !valid_tau(tau) || dW == nullptr) return LP_ERR_INVALID_ARG;
   const int dx_bf16 = opts != nullptr && opts->dx_dtype == LP_DTYPE_BF16;
   const int accumulate = opts != nullptr ? opts->accumulate : 0;
+  const int dw_bf16 = opts != nullptr && opts->dw_dtype == LP_DTYPE_BF16;
   if (opts != nullptr && ((opts->dx_dtype != LP_DTYPE_F32 && opts->dx_dtype != LP_DTYPE_BF16) ||
-                          (accumulate != 0 && accumulate != 1)))
+                          (opts->dw_dtype != LP_DTYPE_F32 && opts->dw_dtype != LP_DTYPE_BF16) ||
+                          (accumulate != 0 && accumulate != 1) || (accumulate && dw_bf16)))
     return LP_ERR_INVALID_ARG;
   if (T == 0) {
     // the gradient of an empty sum: dW and db are zero (or unchanged when accumulating),
@@ -573,7 +575,8 @@ lp_status lp_backward_ex(const void* X, int64_t T, int64_t H, const void* const*
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (int k = 0; k < sh.n; ++k) {
       if (sh.width[k] == 0) continue;
-      if (cudaMemsetAsync(dW[k], 0, size_t(sh.width[k]) * size_t(H) * 4, s) != cudaSuccess) return LP_ERR_CUDA;
+      if (cudaMemsetAsync(dW[k], 0, size_t(sh.width[k]) * size_t(H) * (dw_bf16 ? 2 : 4), s) != cudaSuccess)
+        return LP_ERR_CUDA;
       if (db != nullptr && cudaMemsetAsync(db[k], 0, size_t(sh.width[k]) * 4, s) != cudaSuccess) return LP_ERR_CUDA;
     }
     return LP_OK;
@@ -612,6 +615,7 @@ lp_status lp_backward_ex(const void* X, int64_t T, int64_t H, const void* const*
   a.dX = dX;
   a.dx_bf16 = dx_bf16;
   a.accumulate = accumulate;
+  a.dw_bf16 = dw_bf16;
   for (int k = 0; k < sh.n; ++k) {
     a.W[k] = W[k];
     a.bias[k] = bias != nullptr ? bias[k] : nullptr;

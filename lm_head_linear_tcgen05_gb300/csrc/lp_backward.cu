@@ -293,7 +293,7 @@ struct DwParams {
   int32_t total_tiles;
   unsigned int* err;
   uint64_t wait_limit_ns;
-  float* dW[LP_MAX_SHARDS];
+  void* dW[LP_MAX_SHARDS];  // float, or bf16 with dw_bf16
   int64_t coff[LP_MAX_SHARDS];
   int32_t real[LP_MAX_SHARDS];
   int32_t nb_start[LP_MAX_SHARDS + 1];
@@ -301,6 +301,7 @@ struct DwParams {
   int32_t num_m_blocks;  // row blocks of H, counted in whole clusters
   int32_t nkb;           // K blocks over T
   int32_t accumulate;    // dW += G^T X instead of dW = G^T X
+  int32_t dw_bf16;       // store dW rounded to bf16
   int64_t H;
 };
 
@@ -345,7 +346,23 @@ struct DwEpi : GemmEpiBase {
     const int64_t left = p.real[c.shard] - v0;
     const int valid = int(left < kGemmBlockN ? left : kGemmBlockN);
     const bool ok = h < p.H;
-    float* base = p.dW[c.shard] + size_t(v0) * size_t(p.H) + size_t(ok ? h : 0);
+    const size_t off = size_t(v0) * size_t(p.H) + size_t(ok ? h : 0);
+    if (p.dw_bf16) {  // a warp stores 64 contiguous bytes of one dW row per instruction
+      __nv_bfloat16* b16 = static_cast<__nv_bfloat16*>(p.dW[c.shard]) + off;
+#pragma unroll 1
+      for (int ch = 0; ch < kGemmBlockN / 32; ++ch) {
+        if (ch * 32 >= valid) break;
+        uint32_t r[32];
+        tmem_ld32(tbase + ch * 32, r);
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (ch * 32 + j < valid) b16[size_t(ch * 32 + j) * size_t(p.H)] = __float2bfloat16_rn(f32(r[j]));
+        }
+      }
+      return;
+    }
+    float* base = static_cast<float*>(p.dW[c.shard]) + off;
 #pragma unroll 1
     for (int ch = 0; ch < kGemmBlockN / 32; ++ch) {
       if (ch * 32 >= valid) break;
@@ -587,12 +604,15 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.H = H;
     p.total_tiles = nb * p.num_m_blocks;
     p.accumulate = a.accumulate;
+    p.dw_bf16 = a.dw_bf16;
     p.err = a.err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
     if (launch_tc_gemm<DwEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
+    const size_t esz = a.dw_bf16 ? 2 : 4;
     for (int k = 0; k < sh.n && !a.accumulate; ++k) {
       const int64_t pad = sh.width[k] - sh.real[k];
-      if (pad > 0 && cudaMemsetAsync(a.dW[k] + sh.real[k] * H, 0, size_t(pad) * size_t(H) * 4, s) != cudaSuccess)
+      if (pad > 0 && cudaMemsetAsync(static_cast<char*>(a.dW[k]) + size_t(sh.real[k]) * size_t(H) * esz, 0,
+                                     size_t(pad) * size_t(H) * esz, s) != cudaSuccess)
         return LP_ERR_CUDA;
     }
   }

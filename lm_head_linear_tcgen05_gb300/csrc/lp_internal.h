@@ -185,9 +185,10 @@ struct BackwardArgs {
   void* dX;                   // float or bf16 [T, H] (dx_bf16)
   int dx_bf16;
   int accumulate;             // add into dW and db instead of overwriting them
+  int dw_bf16;                // dW in bf16 (not with accumulate)
   const void* W[LP_MAX_SHARDS];
   const void* bias[LP_MAX_SHARDS];
-  float* dW[LP_MAX_SHARDS];
+  void* dW[LP_MAX_SHARDS];    // float or bf16 [V_k, H] (dw_bf16)
   float* db[LP_MAX_SHARDS];
   void* workspace;
   unsigned int* err;

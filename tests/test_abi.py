@@ -178,16 +178,19 @@ def test_backward_ex_host_validation(lp):
     cp, keep = lp._c_partition(p)
     ws = lp.lp_workspace_size(lp.LP_OP_BACKWARD, 64, 256, p)
 
-    def call(dx_dtype=0, accumulate=0, T=64, opts=True):
+    def call(dx_dtype=0, accumulate=0, T=64, opts=True, dw_dtype=0):
         Wa = (ctypes.c_void_p * 1)(A)
         dW = (ctypes.c_void_p * 1)(A)
-        o = lp._BackwardOptions(dx_dtype, accumulate)
+        o = lp._BackwardOptions(dx_dtype, accumulate, dw_dtype)
         return L.lp_backward_ex(A, T, 256, Wa, None, ctypes.byref(cp), A, 0.7, A, A, None, None, A, dW, None,
                                 ctypes.byref(o) if opts else None, A, ws, None)
 
     assert call(dx_dtype=2) == 1
     assert call(dx_dtype=-1) == 1
     assert call(accumulate=2) == 1
+    assert call(dw_dtype=3) == 1
+    assert call(accumulate=1, dw_dtype=1) == 1  # accumulation needs fp32 dW
+    assert call(dw_dtype=1, dx_dtype=1) == 3
     assert call(T=0, accumulate=1) == 0       # empty batch, accumulating: nothing to add, no device needed
     assert call(T=0) == 3                     # empty batch, overwriting: zeroes dW on the device
     assert call(dx_dtype=1, accumulate=1) == 3

@@ -226,6 +226,15 @@ def test_backward_ex_bf16_dx_and_accumulate(lp, V, bounds):
     assert torch.equal(ex["dX"], base["dX"].to(torch.bfloat16))
     for k in range(len(bounds) - 1):
         assert torch.equal(ex["dW"][k], base["dW"][k]) and torch.equal(ex["db"][k], base["db"][k])
+    # bf16 dW: the same fp32 result rounded once; padded ids exactly zero
+    e16 = lp.lp_backward_ex(X, W, b, P, y, inp.tau, fwd["lse"], g, dw_dtype=torch.bfloat16)
+    for k, (s, e) in enumerate(part.ranges):
+        assert e16["dW"][k].dtype == torch.bfloat16
+        assert torch.equal(e16["dW"][k], base["dW"][k].to(torch.bfloat16)), k
+        assert torch.equal(e16["db"][k], base["db"][k]), k
+        real = max(min(e, V) - s, 0)
+        assert torch.all(e16["dW"][k][real:] == 0), k
+    assert torch.equal(e16["dX"], base["dX"])
     # accumulate: one fp32 add onto the caller's buffers; padded ids keep their values
     gen = torch.Generator(device="cuda").manual_seed(7)
     dW0 = [torch.randn(w.shape, generator=gen, device="cuda") for w in base["dW"]]
@@ -266,6 +275,10 @@ def test_backward_ex_rejects_bad_options(lp):
         lp.lp_backward_ex(X, W, b, P, y, 1.0, lse, g, dx_dtype=torch.float16)
     with pytest.raises(ValueError):
         lp.lp_backward_ex(X, W, b, P, y, 1.0, lse, g, accumulate=True)
+    with pytest.raises(ValueError):
+        lp.lp_backward_ex(X, W, b, P, y, 1.0, lse, g, accumulate=True, dw_dtype=torch.bfloat16,
+                          dW=[torch.zeros((64, 16), dtype=torch.bfloat16, device="cuda")],
+                          db=[torch.zeros(64, device="cuda")])
 
 
 # ------------------------------------------------------------------- autograd
