@@ -7,18 +7,19 @@
 // temperature scaling happens exactly once for reused logits - the logits given
 // here are unscaled and 1/tau is applied in this kernel only.
 //
-// One CTA (256 threads) per row, three CTAs per SM. Thread 0 streams the row through
-// a 2-stage ring of 32 KB shared-memory chunks with 1-D bulk copies (cp.async.bulk,
-// completion on mbarriers, L2 evict-first), so up to 192 KB per SM are in flight
-// without holding registers (the ring shape was chosen by measurement: 6.18 TB/s on
-// 8192 x 151936 bf16 logits, against 5.96 TB/s for 3 x 16 KB at four rows per SM). Each thread folds the 16-byte vectors j = tid, tid+256,
-// ... of every chunk into an online base-2 statistic; the threads are combined by a
-// fixed shuffle tree per warp and then warp by warp in ascending order, shard after
-// shard in ascending order. The work split depends only on the shard width, so a
-// row's result never depends on T.
+// One CTA (256 threads) per row, four per SM. Each thread loads its 16-byte vectors
+// j = tid, tid+256, ... of a shard's row straight into registers, eight at a time
+// (128 KB in flight per SM, streaming cache hint), takes the maximum of the whole batch
+// with max.bf16x2 and rescales its running statistic at most once per batch, then
+// folds the 64 logits in packed f32x2 arithmetic. Logits far below the running maximum
+// are first raised to a floor whose scaled value is at least 200 binary orders below it:
+// 2^d flushes to 0 there exactly as it would for the original logit, and a -inf logit
+// (an entry the caller masked out) never forms 0 * inf. The threads of a shard are
+// combined by a fixed shuffle tree per warp; the per-warp results of every shard wait in
+// shared memory until the row is done, and thread 0 then merges warp after warp and
+// shard after shard in ascending order. The work split depends only on the shard width,
+// so a row's result never depends on T. No thread waits on another while streaming.
 #include <cuda_bf16.h>
-
-#include <atomic>
 
 #include "lp_device.cuh"
 #include "lp_f32x2.cuh"
@@ -27,34 +28,37 @@ namespace lp {
 
 namespace {
 
-#ifndef LP_STREAM_STAGES
-#define LP_STREAM_STAGES 2        // 64 KB of copies in flight per row
-#endif
-#ifndef LP_STREAM_CHUNK_VECS
-#define LP_STREAM_CHUNK_VECS 2048  // 32 KB of logits per stage
+#ifndef LP_STREAM_UNROLL
+#define LP_STREAM_UNROLL 8       // 16-byte vectors per thread in flight
 #endif
 #ifndef LP_STREAM_MIN_BLOCKS
-#define LP_STREAM_MIN_BLOCKS 3     // rows resident per SM
+#define LP_STREAM_MIN_BLOCKS 4   // rows resident per SM
 #endif
 constexpr int kStreamThreads = 256;
 constexpr int kStreamWarps = kStreamThreads / 32;
-constexpr int kChunkVecs = LP_STREAM_CHUNK_VECS;
-constexpr int kStages = LP_STREAM_STAGES;
+constexpr int kUnroll = LP_STREAM_UNROLL;
+// the most negative finite bf16, exactly
+constexpr float kBf16Lowest = -3.38953138925153547590470800371487866880e38f;
+// padding for the vectors of a partial batch: eight bf16 -inf
+constexpr uint32_t kNegInfPair = 0xFF80FF80u;
 
 // Per-thread online statistic over raw (unscaled) logits x: the running maximum is
 // tracked on x, m = max(x) * c2 and d = x * c2 - m, so u = x * c2 is never rounded
 // separately from the subtraction. Sums are kept as two interleaved partial sums
 // (even / odd elements of each 16-byte vector) in packed fp32 pairs and added at the
-// end. -inf logits (entries a caller masked out) add nothing; a thread that saw only
-// -inf stays empty.
+// end. floor2 holds, twice in bf16, the largest bf16 value <= max(x) - 200 / c2 (never
+// below the lowest finite bf16): a logit below it is folded as if it were the floor,
+// which changes nothing - both give 2^d < 2^-126, flushed to 0 - but keeps d finite.
 struct RawStat {
-  float xmax;   // running max of x (-inf while empty)
-  float m;      // xmax * c2
-  uint64_t s2;  // {even, odd} partial sums of 2^(u - m)
-  uint64_t a2;  // {even, odd} partial sums of 2^(u - m) (u - m)
+  float xmax;       // running max of x (-inf while empty)
+  float m;          // xmax * c2
+  uint64_t s2;      // {even, odd} partial sums of 2^(u - m)
+  uint64_t a2;      // {even, odd} partial sums of 2^(u - m) (u - m)
+  uint32_t floor2;  // {floor, floor} in bf16
 };
 
-__device__ __forceinline__ void raw_rescale(RawStat& st, float new_xmax, float c2) {
+// span = 200 / c2 rounded up, so that floor * c2 <= max(x) * c2 - 200
+__device__ __forceinline__ void raw_rescale(RawStat& st, float new_xmax, float c2, float span) {
   const float nm = __fmul_rn(new_xmax, c2);
   if (st.xmax == -INFINITY) {
     st.s2 = 0ull;
@@ -68,36 +72,52 @@ __device__ __forceinline__ void raw_rescale(RawStat& st, float new_xmax, float c
   }
   st.xmax = new_xmax;
   st.m = nm;
+  const __nv_bfloat16 f = __float2bfloat16_rd(fmaxf(__fsub_rd(new_xmax, span), kBf16Lowest));
+  const uint32_t fb = *reinterpret_cast<const uint16_t*>(&f);
+  st.floor2 = fb | (fb << 16);
 }
 
-// fold the pair (lo, hi) of one bf16x2 word
+// fold the pair (lo, hi) of one bf16x2 word; nm2 = {-m, -m}
 __device__ __forceinline__ void raw_pair(RawStat& st, uint32_t w, uint64_t c22, uint64_t nm2) {
+  const uint32_t wc = max_bf16x2(w, st.floor2);
+  const uint64_t d2 = fma2(pack2(bf16_lo(wc), bf16_hi(wc)), c22, nm2);
   float d0, d1;
-  unpack2(fma2(pack2(bf16_lo(w), bf16_hi(w)), c22, nm2), d0, d1);
-  // clamping at -256 (2^-256 flushes to 0) keeps -inf (masked) logits from
-  // producing 0 * -inf in the entropy sum
-  d0 = fmaxf(d0, -256.f);
-  d1 = fmaxf(d1, -256.f);
+  unpack2(d2, d0, d1);
   const uint64_t e2 = pack2(hw_ex2(d0), hw_ex2(d1));
   st.s2 = add2(st.s2, e2);
-  st.a2 = fma2(e2, pack2(d0, d1), st.a2);
+  st.a2 = fma2(e2, d2, st.a2);
 }
 
-__device__ __forceinline__ void raw_push8(RawStat& st, const uint4 v, float c2) {
-  const uint32_t mm = max_bf16x2(max_bf16x2(v.x, v.y), max_bf16x2(v.z, v.w));
+__device__ __forceinline__ uint32_t vec_max(const uint4& v) {
+  return max_bf16x2(max_bf16x2(v.x, v.y), max_bf16x2(v.z, v.w));
+}
+
+// Fold one batch of vectors, in order; only the first n_valid are folded (the rest are
+// -inf padding). The running maximum is raised once, to the maximum of the batch.
+__device__ __forceinline__ void raw_fold_batch(RawStat& st, const uint4 (&v)[kUnroll], int n_valid, float c2,
+                                               float span) {
+  uint32_t mm = vec_max(v[0]);
+#pragma unroll
+  for (int u = 1; u < kUnroll; ++u) mm = max_bf16x2(mm, vec_max(v[u]));
   const float vmax = fmaxf(bf16_lo(mm), bf16_hi(mm));
-  if (vmax > st.xmax) raw_rescale(st, vmax, c2);
+  if (vmax > st.xmax) raw_rescale(st, vmax, c2, span);
+  if (st.xmax == -INFINITY) return;  // every logit so far is -inf: nothing to add
   const uint64_t c22 = pack2(c2, c2);
   const uint64_t nm2 = pack2(-st.m, -st.m);
-  raw_pair(st, v.x, c22, nm2);
-  raw_pair(st, v.y, c22, nm2);
-  raw_pair(st, v.z, c22, nm2);
-  raw_pair(st, v.w, c22, nm2);
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    if (u < n_valid) {
+      raw_pair(st, v[u].x, c22, nm2);
+      raw_pair(st, v[u].y, c22, nm2);
+      raw_pair(st, v[u].z, c22, nm2);
+      raw_pair(st, v[u].w, c22, nm2);
+    }
+  }
 }
 
 // one element, folded into the even partial sums
-__device__ __forceinline__ void raw_push1(RawStat& st, float x, float c2) {
-  if (x > st.xmax) raw_rescale(st, x, c2);
+__device__ __forceinline__ void raw_push1(RawStat& st, float x, float c2, float span) {
+  if (x > st.xmax) raw_rescale(st, x, c2, span);
   const float d = fmaxf(__fmaf_rn(x, c2, -st.m), -256.f);
   const float e = hw_ex2(d);
   st.s2 = add2(st.s2, pack2(e, 0.f));
@@ -114,72 +134,43 @@ __device__ __forceinline__ Stat raw_to_stat(const RawStat& st) {
 }  // namespace
 
 __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_logits_kernel(const __grid_constant__ StreamParams p) {
-  extern __shared__ uint4 sbuf[];  // kStages x kChunkVecs vectors of 8 bf16
-  __shared__ uint64_t full[kStages];
-  __shared__ Stat red[kStreamWarps];
-  __shared__ int abort_flag;
+  __shared__ Stat red[LP_MAX_SHARDS][kStreamWarps];  // per shard, per warp
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const float c2 = p.scale_log2;
+  const float span = __fdiv_ru(200.f, c2);
   const int yv = __ldg(p.y + row);
   const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
   const size_t T = size_t(p.T);
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-    abort_flag = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
-  const uint64_t pol = l2_policy_evict_first();
+  constexpr int64_t kBatch = int64_t(kUnroll) * kStreamThreads;
 
-  Stat tot = stat_empty();  // meaningful in thread 0 only
-  float t_val = 0.f;
-  uint32_t g0 = 0;          // chunks of this row consumed so far (all shards): fixes stage and parity
-  bool ok = true;
-
-  for (int k = 0; k < p.n_shards && ok; ++k) {
+  for (int k = 0; k < p.n_shards; ++k) {
     const int64_t width = p.shard_width[k];
     const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
     const uint4* src = reinterpret_cast<const uint4*>(L);
     const int64_t nvec = width > 0 ? (width >> 3) : 0;
-    const int nchunks = int((nvec + kChunkVecs - 1) / kChunkVecs);
-    RawStat st{-INFINITY, -INFINITY, 0ull, 0ull};
-    // thread 0 streams the row through the stage ring; the other threads consume
-    auto issue = [&](int c) {
-      const int64_t v0 = int64_t(c) * kChunkVecs;
-      const int64_t nv = nvec - v0 < kChunkVecs ? nvec - v0 : kChunkVecs;
-      const uint32_t s = (g0 + c) % kStages;
-      mbar_arrive_expect_tx(&full[s], uint32_t(nv) * 16u);
-      bulk_load(sbuf + size_t(s) * kChunkVecs, src + v0, uint32_t(nv) * 16u, &full[s], pol);
-    };
-    if (tid == 0)
-      for (int c = 0; c < nchunks && c < kStages; ++c) issue(c);
-    for (int c = 0; c < nchunks; ++c) {
-      const uint32_t g = g0 + c;
-      const uint32_t s = g % kStages;
-      const bool got = mbar_wait(&full[s], (g / kStages) & 1u, &abort_flag, kDefaultWaitLimitNs, p.err);
-      if (!__syncthreads_and(got)) {
-        ok = false;
-        if (tid == 0)  // let the copies already issued land before the CTA exits
-          for (int d = c; d < nchunks && d < c + kStages; ++d)
-            drain_wait(&full[(g0 + d) % kStages], ((g0 + d) / kStages) & 1u, kDefaultWaitLimitNs);
-        break;
-      }
-      const int64_t v0 = int64_t(c) * kChunkVecs;
-      const int nv = int(nvec - v0 < kChunkVecs ? nvec - v0 : kChunkVecs);
-      const uint4* chunk = sbuf + size_t(s) * kChunkVecs;
-#pragma unroll 4
-      for (int j = tid; j < nv; j += kStreamThreads) raw_push8(st, chunk[j], c2);
-      __syncthreads();  // stage s fully read
-      if (tid == 0 && c + kStages < nchunks) issue(c + kStages);
+    RawStat st{-INFINITY, -INFINITY, 0ull, 0ull, 0u};
+    int64_t j0 = tid;  // this thread's vectors: j0, j0 + 256, ...
+    for (; j0 + kBatch - kStreamThreads < nvec; j0 += kBatch) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) v[u] = __ldcs(src + j0 + int64_t(u) * kStreamThreads);
+      raw_fold_batch(st, v, kUnroll, c2, span);
     }
-    g0 += uint32_t(nchunks);
-    if (!ok) break;
+    if (j0 < nvec) {  // the last, partial batch: fewer than kUnroll vectors for this thread
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t j = j0 + int64_t(u) * kStreamThreads;
+        v[u] = j < nvec ? __ldcs(src + j) : make_uint4(kNegInfPair, kNegInfPair, kNegInfPair, kNegInfPair);
+      }
+      raw_fold_batch(st, v, int((nvec - j0 + kStreamThreads - 1) / kStreamThreads), c2, span);
+    }
     // ragged tail (width % 8 elements) by the first threads, in ascending order
     const int64_t tail0 = nvec << 3;
-    if (width > 0 && tail0 + tid < width) raw_push1(st, __bfloat162float(L[tail0 + tid]), c2);
+    if (width > 0 && tail0 + tid < width) raw_push1(st, __bfloat162float(L[tail0 + tid]), c2, span);
 
     Stat loc = raw_to_stat(st);
 #pragma unroll
@@ -188,53 +179,39 @@ __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_l
                    __shfl_down_sync(0xffffffffu, loc.a, off)};
       if (lane < off) stat_merge(loc, o);
     }
-    if (lane == 0) red[warp] = loc;
-    __syncthreads();
-    if (tid == 0) {
-      Stat sh = red[0];
-      for (int w = 1; w < kStreamWarps; ++w) stat_merge(sh, red[w]);
-      const bool own = y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k];
-      float tk = 0.f;
-      if (own) {
-        tk = __fmul_rn(__bfloat162float(L[yv - p.shard_start[k]]), p.inv_tau);
-        t_val = tk;
-      }
-      if (p.shard_stats != nullptr) {
-        float* ss = p.shard_stats + size_t(k) * 3 * T;
-        ss[row] = stat_lse(sh);
-        ss[T + row] = tk;
-        ss[2 * T + row] = stat_mean(sh);
-      }
-      stat_merge(tot, sh);
-    }
-    __syncthreads();
+    if (lane == 0) red[k][warp] = loc;
   }
-  if (tid == 0) {
-    const float lse = stat_lse(tot);
-    if (!ok) {
-      p.lse[row] = -INFINITY;
-      p.logp[row] = -INFINITY;
-      if (p.entropy != nullptr) p.entropy[row] = 0.f;
-      return;
+  __syncthreads();
+  if (tid != 0) return;
+  Stat tot = stat_empty();
+  float t_val = 0.f;
+  for (int k = 0; k < p.n_shards; ++k) {
+    Stat sh = red[k][0];
+    for (int w = 1; w < kStreamWarps; ++w) stat_merge(sh, red[k][w]);
+    const bool own = y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k];
+    float tk = 0.f;
+    if (own) {
+      const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
+      tk = __fmul_rn(__bfloat162float(L[yv - p.shard_start[k]]), p.inv_tau);
+      t_val = tk;
     }
-    p.lse[row] = lse;
-    if (p.entropy != nullptr) p.entropy[row] = stat_entropy(tot);
-    if (!y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
-    p.logp[row] = (y_ok && tot.m != -INFINITY) ? __fsub_rn(t_val, lse) : -INFINITY;
+    if (p.shard_stats != nullptr) {
+      float* ss = p.shard_stats + size_t(k) * 3 * T;
+      ss[row] = stat_lse(sh);
+      ss[T + row] = tk;
+      ss[2 * T + row] = stat_mean(sh);
+    }
+    stat_merge(tot, sh);
   }
+  const float lse = stat_lse(tot);
+  p.lse[row] = lse;
+  if (p.entropy != nullptr) p.entropy[row] = stat_entropy(tot);
+  if (!y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
+  p.logp[row] = (y_ok && tot.m != -INFINITY) ? __fsub_rn(t_val, lse) : -INFINITY;
 }
 
 cudaError_t launch_stream_logits(const StreamParams& p, cudaStream_t s) {
-  const int smem = kStages * kChunkVecs * int(sizeof(uint4));
-  static std::atomic<bool> ready[64];  // shared-memory opt-in done on this device
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!ready[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(stream_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    ready[dev].store(true, std::memory_order_release);
-  }
-  stream_logits_kernel<<<p.T, kStreamThreads, smem, s>>>(p);
+  stream_logits_kernel<<<p.T, kStreamThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

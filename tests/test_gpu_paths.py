@@ -29,6 +29,17 @@ def _np(t):
 
 # ----------------------------------------------------------------- logits reuse
 
+def _strided_rows(a):
+    """A [T, w] device view of bf16 bits `a` whose row stride is a multiple of 8 elements
+    (16 bytes, as the library requires) with 8 elements to spare."""
+    import torch
+    T, w = a.shape
+    ld = (w + 7) // 8 * 8 + 8
+    buf = torch.zeros((T, ld), dtype=torch.bfloat16, device="cuda")
+    buf[:, :w] = dev_bf16(a)
+    return buf[:, :w]
+
+
 @pytest.mark.parametrize("T,bounds,real", [
     (37, [0, 1000], 1000),
     (64, [0, 4099, 4099, 9000, 12301], 12290),     # ragged widths, empty shard, padding
@@ -74,6 +85,72 @@ def test_logits_reuse_bitwise_and_batch_invariant(lp):
     for k in ("logp", "lse", "entropy"):
         assert torch.equal(a[k], b[k])
         assert torch.equal(a[k][40:], c[k])
+
+
+@pytest.mark.parametrize("tau", [0.05, 0.7, 20.0])
+def test_logits_reuse_masked_and_extreme_rows(lp, tau):
+    """Rows built to stress the streaming fold: entries masked out with -inf (also a whole
+    shard, and all but the target), large offsets, a far-below-the-rest half of the row, a
+    single dominant logit, and rows whose maximum rises (or falls) with every element.
+    A -inf logit and a finite one so low that exp underflows to exactly 0 in fp64 are the
+    same to the definition, so the oracle sees -1e30 where the kernel sees -inf."""
+    bounds, real = [0, 4101, 8203, 12000], 11990
+    part = synth.ranges_partition(real, bounds[-1], bounds)
+    T = 40
+    tau = float(np.float32(tau))
+    L, y, _ = synth.logits_inputs(T, part, tau, seed=17)
+    full = np.concatenate(L, axis=1).view(np.uint16)
+    x = (full.astype(np.uint32) << np.uint32(16)).view(np.float32).copy()
+    rng = np.random.Generator(np.random.PCG64(99))
+    y = y.astype(np.int64)
+    mask = np.zeros(x.shape, bool)
+    # row 0: 30 % of the real ids masked (never the target)
+    mask[0, rng.choice(real, size=int(0.3 * real), replace=False)] = True
+    # row 1: shard 1 masked entirely, target elsewhere
+    mask[1, bounds[1]:bounds[2]] = True
+    y[1] = 17
+    # row 2: everything masked but the target
+    mask[2, :real] = True
+    y[2] = 9000
+    mask[2, y[2]] = False
+    mask[0, y[0]] = False
+    # rows 3, 4: all logits shifted by +-300
+    x[3] += 300.0
+    x[4] -= 300.0
+    # row 5: half of the ids at -1e30 (finite, far below every other logit)
+    x[5, rng.choice(real, size=real // 2, replace=False)] = -1e30
+    # row 6: one dominant logit
+    x[6, 5000] = 200.0
+    # rows 7, 8: maximum rising with every element / falling
+    x[7, :real] = np.linspace(-50.0, 50.0, real)
+    x[8, :real] = np.linspace(50.0, -50.0, real)
+    bits = synth.bf16_bits(x.astype(np.float32))
+    gpu_bits = bits.copy()
+    gpu_bits[mask] = 0xFF80                        # bf16 -inf
+    ora_bits = bits.copy()
+    ora_bits[mask] = synth.bf16_bits(np.array([-1e30], np.float32))[0]
+    split = lambda b: [np.ascontiguousarray(b[:, s:e]) for s, e in part.ranges]
+    y32 = y.astype(np.int32)
+    out = lp.lp_forward_from_logits([_strided_rows(a) for a in split(gpu_bits)], part_of(part), dev_i32(y32), tau,
+                                    shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.forward_from_logits(split(ora_bits), part, y32, tau)
+    lg, ls, en = _np(out["logp"]), _np(out["lse"]), _np(out["entropy"])
+    assert np.all(np.isfinite(lg)) and np.all(np.isfinite(ls)) and np.all(np.isfinite(en))
+    assert max_abs(lg, ref.logp) <= TOL_LOGP
+    assert max_abs(ls, ref.lse) <= TOL_LSE
+    assert max_abs(en, ref.entropy) <= TOL_ENT
+    assert abs(lg[2]) <= 1e-5 and abs(en[2]) <= 1e-5   # one live id: p = 1
+    ss = _np(out["shard_stats"])
+    assert not np.isnan(ss).any()
+    empty = np.stack([mask[:, s:min(e, real)].all(axis=1) for s, e in part.ranges])   # [K, T]
+    assert empty[1, 1] and empty[0, 2] and empty[1, 2] and not empty[2, 2]
+    for k in range(part.n_shards):
+        live = ~empty[k]
+        assert max_abs(ss[k, 0, live], ref.shards[k].lse[live]) <= TOL_LSE
+        assert max_abs(ss[k, 2, live], ref.shards[k].mu[live]) <= TOL_ENT
+        # a shard whose ids are all masked is empty: LSE -inf, mean 0
+        assert np.all(np.isneginf(ss[k, 0, empty[k]])) and np.all(ss[k, 2, empty[k]] == 0.0)
 
 
 # ----------------------------------------------------------------------- replay
