@@ -57,10 +57,6 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -112,10 +108,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 
 // -------------------------------------------------------------------- TMA
 
-__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
-}
-
 // 2-D tiled bulk tensor copy global -> shared, completing on `bar` (tx bytes).
 // (x, y) = (innermost, outer) element coordinates of the box origin; x is always a
 // multiple of the 64-element box width here, so x * 2 bytes is 16-byte aligned.
@@ -149,23 +141,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 // All threads of every CTA of the cluster: release/acquire barrier.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// 1-D bulk copy global -> shared of `bytes` (multiple of 16; both addresses 16-byte
-// aligned), completing on `bar` (tx bytes), with an L2 eviction-policy hint.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                          uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
