@@ -7,7 +7,9 @@
 // logits and LSE reduced over shards in rank order; a shard without candidates
 // contributes zero probability (LSE -inf, target logit 0) and never a NaN.
 //
-// One CTA (256 threads) per row:
+// One CTA (256 threads) per row, six rows resident per SM (a launch-shape sweep: 4-16
+// rows per SM, 128-512 threads, 2-8 vectors per lane in flight; 4.6 % faster than four
+// rows with eight vectors, and every variant gives the same bits):
 //   1. warp 0 reads the 64 slots, checks every id, and writes the distinct ids in
 //      ascending order (rank of each first occurrence among the distinct values);
 //   2. the row of X is staged in shared memory;
@@ -30,7 +32,14 @@ namespace lp {
 
 namespace {
 
+#ifndef LP_REPLAY_MIN_BLOCKS
+#define LP_REPLAY_MIN_BLOCKS 6  // rows resident per SM (40 registers a thread)
+#endif
+#ifndef LP_REPLAY_UNROLL
+#define LP_REPLAY_UNROLL 4      // 16-byte vectors of a W row per lane in flight
+#endif
 constexpr int kReplayThreads = 256;
+constexpr int kDotUnroll = LP_REPLAY_UNROLL;
 constexpr int kReplayWarps = kReplayThreads / 32;
 
 __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
@@ -57,15 +66,15 @@ __device__ __forceinline__ float fma8(float acc, const uint4 x, const uint4 w) {
 // row of W; every lane returns the same value.
 __device__ __forceinline__ float warp_dot(const uint4* __restrict__ w, const uint4* xs, int nvec, int lane) {
   float acc = 0.f;
-  for (int base = 0; base < nvec; base += 32 * 8) {
-    uint4 wv[8];
+  for (int base = 0; base < nvec; base += 32 * kDotUnroll) {
+    uint4 wv[kDotUnroll];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kDotUnroll; ++u) {
       const int v = base + u * 32 + lane;
       wv[u] = v < nvec ? ld_nc(w + v) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kDotUnroll; ++u) {
       const int v = base + u * 32 + lane;
       if (v < nvec) acc = fma8(acc, xs[v], wv[u]);
     }
@@ -87,7 +96,7 @@ __device__ __forceinline__ int shard_of(const ReplayParams& p, int64_t v) {
 }  // namespace
 
 template <bool kFromLogits>
-__global__ void __launch_bounds__(kReplayThreads) replay_kernel(const __grid_constant__ ReplayParams p) {
+__global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_kernel(const __grid_constant__ ReplayParams p) {
   extern __shared__ uint4 xs[];  // the row of X, H / 8 vectors
   __shared__ int32_t slots[LP_REPLAY_SLOTS];
   __shared__ uint8_t dup[LP_REPLAY_SLOTS];

@@ -4,7 +4,8 @@ sampled rows the oracle computes one by one (plus properties that hold at any si
 * Qwen3-8B-shaped forward: T=4096, H=4096, V=151936, tau=0.7; 1 x 4096 vs 8 x 512 bitwise;
 * vocabulary-sharded forward + backward: V=151936 padded to 152064 in 4 shards of 38016,
   bias; dX on sampled rows at T=4096, dW/db on sampled vocabulary rows at T'=256;
-* logits reuse: T=8192 x 151936 bf16 logits, 1 % peaked rows;
+* logits reuse: T=8192 x 151936 bf16 logits, 1 % peaked rows (and T=2048 in the 4 padded
+  shards of the sharded layout);
 * compact top-p replay: T=8192, 4 shards of 37984, 1-64 ids per row, 25 % of rows with an
   empty shard; dense keep-mask route bitwise equal.
 """
@@ -143,6 +144,33 @@ def test_logits_reuse_full_size_sampled_rows(lp):
     assert max_abs(_np(out["entropy"])[rows], ref.entropy) <= TOL_ENT
     again = lp.lp_forward_from_logits(Ld, part_of(part), dev_i32(y), tau)
     assert torch.equal(again["lse"], out["lse"]) and torch.equal(again["entropy"], out["entropy"])
+
+
+def test_logits_reuse_full_width_four_padded_shards(lp):
+    """The sharded layout (4 x 38016 ids, the last 128 of them padding) at full width: every
+    shard ends in a partial batch of vectors, and per-shard results are merged at the end of
+    the row. Sampled rows against the oracle, shard statistics included; rows computed in a
+    smaller batch keep their bits."""
+    import torch
+    part = _sharded()
+    T = 2048
+    L, y, tau = synth.logits_inputs(T, part, TAU, seed=44)
+    Ld = [dev_bf16(a) for a in L]
+    out = lp.lp_forward_from_logits(Ld, part_of(part), dev_i32(y), tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    rows = _sample_rows(T, 256, 5)
+    ref = oracle.forward_from_logits(L, part, y, tau, rows=rows)
+    assert max_abs(_np(out["logp"])[rows], ref.logp) <= TOL_LOGP
+    assert max_abs(_np(out["lse"])[rows], ref.lse) <= TOL_LSE
+    assert max_abs(_np(out["entropy"])[rows], ref.entropy) <= TOL_ENT
+    ss = _np(out["shard_stats"])
+    for k, s in enumerate(ref.shards):
+        assert max_abs(ss[k, 0][rows], s.lse) <= TOL_LSE
+        assert max_abs(ss[k, 1][rows], s.t) <= TOL_LOGP
+        assert max_abs(ss[k, 2][rows], s.mu) <= TOL_ENT
+    sub = lp.lp_forward_from_logits([x[1000:1100] for x in Ld], part_of(part), dev_i32(y[1000:1100]), tau)
+    for key in ("logp", "lse", "entropy"):
+        assert torch.equal(sub[key], out[key][1000:1100])
 
 
 def test_replay_full_size_and_dense_mask(lp):
