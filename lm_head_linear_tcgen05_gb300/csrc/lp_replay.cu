@@ -10,14 +10,15 @@
 // One CTA (256 threads) per row, six rows resident per SM (a launch-shape sweep: 4-16
 // rows per SM, 128-512 threads, 2-8 vectors per lane in flight; 4.6 % faster than four
 // rows with eight vectors, and every variant gives the same bits):
-//   1. warp 0 reads the 64 slots, checks every id, and writes the distinct ids in
-//      ascending order (rank of each first occurrence among the distinct values);
+//   1. warp 0 reads the 64 slots, checks every id, sorts them with a bitonic network
+//      across its lanes (two per lane) and writes the distinct ids in ascending order;
 //   2. the row of X is staged in shared memory;
 //   3. each warp scores ids i = warp, warp+8, ...: a canonical fp32 dot product
 //      (lane l accumulates 16-byte vectors l, l+32, ... in order, then a fixed
 //      shuffle tree) of x with the gathered row W[id] - a gather GEMV;
-//   4. thread 0 folds the scores in ascending id order, shard by shard, and merges
-//      the shards in ascending order.
+//   4. warp 0 folds the scores shard by shard - each lane the two adjacent ids it holds,
+//      then a fixed shuffle tree - and lane 0 merges the shards in ascending order. The
+//      order depends only on the row's id set.
 // The dense keep-mask route compacts each mask row into the same canonical slots
 // and runs this very kernel, so both routes produce identical bits for equal sets.
 // The logits-gather variant (reused unscaled logits instead of x . W) replaces step 3
@@ -87,6 +88,32 @@ __device__ __forceinline__ float warp_dot(const uint4* __restrict__ w, const uin
   return __shfl_sync(0xffffffffu, acc, 0);
 }
 
+// Warp-wide bitonic sort of 64 unsigned keys, two per lane: element e = 2 * lane + j
+// holds k[j]; on return the keys ascend with e. Stage (size, d) compare-exchanges e with
+// e ^ d, keeping the smaller key at the lower index inside blocks of `size` whose index
+// has bit `size` clear and the larger one elsewhere.
+__device__ __forceinline__ void warp_sort64(uint32_t& k0, uint32_t& k1, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 64; size <<= 1) {
+    const bool asc = ((2 * lane) & size) == 0;  // bit 0 (the j of e) never reaches `size`
+#pragma unroll
+    for (int d = size >> 1; d >= 1; d >>= 1) {
+      if (d == 1) {  // both elements in this lane
+        const uint32_t lo = min(k0, k1), hi = max(k0, k1);
+        k0 = asc ? lo : hi;
+        k1 = asc ? hi : lo;
+      } else {  // partner lane = lane ^ (d / 2), same j
+        const int ld = d >> 1;
+        const uint32_t p0 = __shfl_xor_sync(0xffffffffu, k0, ld);
+        const uint32_t p1 = __shfl_xor_sync(0xffffffffu, k1, ld);
+        const bool take_min = ((lane & ld) == 0) == asc;
+        k0 = take_min ? min(k0, p0) : max(k0, p0);
+        k1 = take_min ? min(k1, p1) : max(k1, p1);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ int shard_of(const ReplayParams& p, int64_t v) {
   int k = 0;
   while (k + 1 < p.n_shards && v >= p.shard_end[k]) ++k;
@@ -98,8 +125,6 @@ __device__ __forceinline__ int shard_of(const ReplayParams& p, int64_t v) {
 template <bool kFromLogits>
 __global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_kernel(const __grid_constant__ ReplayParams p) {
   extern __shared__ uint4 xs[];  // the row of X, H / 8 vectors
-  __shared__ int32_t slots[LP_REPLAY_SLOTS];
-  __shared__ uint8_t dup[LP_REPLAY_SLOTS];
   __shared__ int32_t uniq[LP_REPLAY_SLOTS];
   __shared__ float zs[LP_REPLAY_SLOTS];
   __shared__ int n_uniq;
@@ -112,41 +137,28 @@ __global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_k
   const size_t T = size_t(p.T);
   const int nvec = p.H >> 3;
 
-  // 1. validate, sort ascending, deduplicate
+  // 1. validate, sort ascending, deduplicate (warp 0): unused and invalid slots become the
+  // key 0xFFFFFFFF, above every id; after the sort a key is kept if it differs from its
+  // predecessor, and its rank is the number of kept keys before it
   if (warp == 0) {
     const int32_t* ids = p.ids + size_t(row) * LP_REPLAY_SLOTS;
-    const int32_t v0 = __ldg(ids + lane), v1 = __ldg(ids + 32 + lane);
+    const int32_t v0 = __ldg(ids + 2 * lane), v1 = __ldg(ids + 2 * lane + 1);
     const bool bad0 = v0 != -1 && (v0 < 0 || int64_t(v0) >= p.vocab_real);
     const bool bad1 = v1 != -1 && (v1 < 0 || int64_t(v1) >= p.vocab_real);
     const unsigned any_bad = __ballot_sync(0xffffffffu, bad0 || bad1);
-    slots[lane] = (bad0 || v0 < 0) ? -1 : v0;
-    slots[32 + lane] = (bad1 || v1 < 0) ? -1 : v1;
-    __syncwarp();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int i = lane + 32 * h;
-      const int32_t v = slots[i];
-      bool d = v == -1;
-      for (int j = 0; j < i && !d; ++j) d = slots[j] == v;
-      dup[i] = d ? 1 : 0;
-    }
-    __syncwarp();
-    int kept = 0;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int i = lane + 32 * h;
-      const int32_t v = slots[i];
-      if (!dup[i]) {
-        int rank = 0;
-        for (int j = 0; j < LP_REPLAY_SLOTS; ++j) rank += (!dup[j] && slots[j] < v) ? 1 : 0;
-        uniq[rank] = v;
-        ++kept;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, off);
+    uint32_t k0 = (bad0 || v0 < 0) ? 0xFFFFFFFFu : uint32_t(v0);
+    uint32_t k1 = (bad1 || v1 < 0) ? 0xFFFFFFFFu : uint32_t(v1);
+    warp_sort64(k0, k1, lane);
+    const uint32_t prev0 = __shfl_up_sync(0xffffffffu, k1, 1);
+    const bool keep0 = k0 != 0xFFFFFFFFu && (lane == 0 || k0 != prev0);
+    const bool keep1 = k1 != 0xFFFFFFFFu && k1 != k0;
+    const unsigned b0 = __ballot_sync(0xffffffffu, keep0), b1 = __ballot_sync(0xffffffffu, keep1);
+    const unsigned lower = (1u << lane) - 1u;
+    const int before = __popc(b0 & lower) + __popc(b1 & lower);
+    if (keep0) uniq[before] = int32_t(k0);
+    if (keep1) uniq[before + (keep0 ? 1 : 0)] = int32_t(k1);
     if (lane == 0) {
-      n_uniq = kept;
+      n_uniq = __popc(b0) + __popc(b1);
       bad_row = any_bad != 0u;
       if (any_bad) record_error(p.err, LP_ERR_REPLAY_ID_OUT_OF_RANGE);
     }
@@ -183,38 +195,52 @@ __global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_k
   }
   __syncthreads();
 
-  // 4. fold in ascending id order, shard by shard, shards in ascending order
-  if (tid == 0) {
+  // 4. fold (warp 0): lane l takes ids 2l and 2l + 1 (ascending) of each shard, the lanes'
+  // statistics combine by a fixed shuffle tree, and lane 0 merges the shards in ascending
+  // order - an order fixed by the row's id set alone
+  if (warp == 0) {
     const int yv = __ldg(p.y + row);
     const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
-    if (!y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
+    if (lane == 0 && !y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
+    const int i0 = 2 * lane, i1 = 2 * lane + 1;
+    const bool h0 = i0 < n, h1 = i1 < n;
+    const int64_t id0 = h0 ? int64_t(uniq[i0]) : -1, id1 = h1 ? int64_t(uniq[i1]) : -1;
+    const float z0 = h0 ? zs[i0] : 0.f, z1 = h1 ? zs[i1] : 0.f;
+    const bool own0 = y_ok && id0 == yv, own1 = y_ok && id1 == yv;
+    const unsigned tb = __ballot_sync(0xffffffffu, own0 || own1);
+    const bool t_found = tb != 0u;
+    const float t_val = __shfl_sync(0xffffffffu, own1 ? z1 : z0, t_found ? __ffs(tb) - 1 : 0);
     Stat tot = stat_empty();
-    float t_val = 0.f;
-    bool t_found = false;
-    int i = 0;
     for (int k = 0; k < p.n_shards; ++k) {
+      const bool in0 = h0 && id0 >= p.shard_start[k] && id0 < p.shard_end[k];
+      const bool in1 = h1 && id1 >= p.shard_start[k] && id1 < p.shard_end[k];
       Stat loc = stat_empty();
-      float tk = 0.f;
-      for (; i < n && uniq[i] < p.shard_end[k]; ++i) {
-        const float z = zs[i];
-        stat_push(loc, __fmul_rn(z, kLog2e));
-        if (uniq[i] == yv) {
-          tk = z;
-          t_val = z;
-          t_found = true;
+      if (__ballot_sync(0xffffffffu, in0 || in1) != 0u) {
+        if (in0) stat_push(loc, __fmul_rn(z0, kLog2e));
+        if (in1) stat_push(loc, __fmul_rn(z1, kLog2e));
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const Stat o{__shfl_down_sync(0xffffffffu, loc.m, off), __shfl_down_sync(0xffffffffu, loc.s, off),
+                       __shfl_down_sync(0xffffffffu, loc.a, off)};
+          if (lane < off) stat_merge(loc, o);
         }
       }
-      if (p.shard_stats != nullptr) {
-        float* ss = p.shard_stats + size_t(k) * 3 * T;
-        ss[row] = stat_lse(loc);
-        ss[T + row] = tk;
-        ss[2 * T + row] = 0.f;
+      if (lane == 0) {
+        const bool own_k = t_found && yv >= p.shard_start[k] && yv < p.shard_end[k];
+        if (p.shard_stats != nullptr) {
+          float* ss = p.shard_stats + size_t(k) * 3 * T;
+          ss[row] = stat_lse(loc);
+          ss[T + row] = own_k ? t_val : 0.f;
+          ss[2 * T + row] = 0.f;
+        }
+        stat_merge(tot, loc);
       }
-      stat_merge(tot, loc);
     }
-    const float lse = stat_lse(tot);
-    p.lse[row] = bad_row ? -INFINITY : lse;
-    p.logp[row] = (!bad_row && y_ok && t_found) ? __fsub_rn(t_val, lse) : -INFINITY;
+    if (lane == 0) {
+      const float lse = stat_lse(tot);
+      p.lse[row] = bad_row ? -INFINITY : lse;
+      p.logp[row] = (!bad_row && y_ok && t_found) ? __fsub_rn(t_val, lse) : -INFINITY;
+    }
   }
 }
 
