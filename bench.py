@@ -561,7 +561,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true", help="time only the fused forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per reference step")
+    ap.add_argument("--ref-rows", type=int, default=256,
+                    help="oracle rows per reference step (each call also decodes all of W, which a larger "
+                         "sample amortises as the full 4096-row workload would)")
     ap.add_argument("--rows", type=int, default=T_FWD, help="headline rows T (profiling of smaller cases)")
     ap.add_argument("--path-rows", type=int, default=8192,
                     help="rows of the logits-reuse and replay workloads (profiling of smaller cases)")
