@@ -209,6 +209,50 @@ def test_replay_parity_and_dense_mask_bitwise(lp, T, H, bounds, real, bias):
     assert torch.equal(o3["logp"], out["logp"][10:]) and torch.equal(o3["lse"], out["lse"][10:])
 
 
+def test_replay_adversarial_slot_patterns(lp):
+    """Slot patterns that stress the in-warp sort and deduplication: 64 distinct ids in
+    descending and in ascending order, one id 64 times, the two ends of the vocabulary,
+    ids alternating between the first and last shard, one id among 63 empty slots (first
+    or last slot), and pairs of equal ids at every other slot."""
+    import torch
+    bounds, real = [0, 1000, 2000, 3000, 4096], 4090
+    part = synth.ranges_partition(real, bounds[-1], bounds)
+    T, H = 10, 128
+    inp = synth.forward_inputs(T, H, part, tau=0.6, seed=31, w_std=0.2, bias_std=0.1)
+    ids = np.full((T, 64), -1, np.int32)
+    ids[0] = np.arange(4000, 3936, -1)
+    ids[1] = np.arange(100, 164)
+    ids[2] = 777
+    ids[3, :2] = [0, real - 1]
+    ids[4] = np.where(np.arange(64) % 2 == 0, np.arange(64) * 7, real - 1 - np.arange(64) * 5)
+    ids[5, 0] = 2500
+    ids[6, 63] = 2500
+    ids[7] = np.repeat(np.arange(3000, 3032), 2)
+    ids[8, ::2] = np.arange(32) * 100
+    ids[9] = np.random.default_rng(5).permutation(np.arange(1990, 2054))
+    y = np.array([3937, 163, 777, real - 1, 0, 2500, 2500, 3031, 3150, 2000], np.int32)
+    X, W, b, _ = dev_inputs(inp)
+    P = part_of(part)
+    out = lp.lp_top_p_replay(X, W, b, P, dev_i32(ids), dev_i32(y), inp.tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.top_p_replay(inp.X, inp.W, inp.bias, part, ids, y, inp.tau)
+    lg, ls = _np(out["logp"]), _np(out["lse"])
+    fin = np.isfinite(ref.logp)
+    assert np.array_equal(np.isfinite(lg), fin) and np.array_equal(np.isfinite(ls), np.isfinite(ref.lse))
+    assert max_abs(lg[fin], ref.logp[fin]) <= TOL_LOGP
+    assert max_abs(ls, ref.lse) <= TOL_LSE
+    assert not fin[8] and np.all(fin[[0, 1, 2, 3, 4, 5, 6, 7, 9]])   # row 8: target not in its set
+    assert abs(lg[2]) <= 1e-5 and abs(lg[5]) <= 1e-5                  # a single id: p = 1
+    ss = _np(out["shard_stats"])
+    for k in range(part.n_shards):
+        assert max_abs(ss[k, 0], ref.shard_lse[k]) <= TOL_LSE
+        assert max_abs(ss[k, 1], ref.shard_t[k]) <= TOL_LOGP
+    # the same rows with their slots reversed give the same bits
+    rev = lp.lp_top_p_replay(X, W, b, P, dev_i32(ids[:, ::-1].copy()), dev_i32(y), inp.tau, shard_stats=True)
+    for key in ("logp", "lse", "shard_stats"):
+        assert torch.equal(rev[key], out[key]), key
+
+
 def test_replay_whole_vocab_matches_dense_forward(lp):
     part = synth.ranges_partition(60, 64, [0, 16, 32, 48, 64])
     inp = synth.forward_inputs(9, 64, part, tau=0.7, seed=4, w_std=0.3, bias_std=0.2)
@@ -410,6 +454,13 @@ def test_many_row_blocks_forward_replay_logits_backward(lp):
     # the first 4096 rows alone give the same forward bits (batch invariance at this size)
     head = lp.lp_forward(X[:4096].contiguous(), W, b, P, y[:4096].contiguous(), inp.tau)
     assert torch.equal(head["logp"], fwd["logp"][:4096]) and torch.equal(head["lse"], fwd["lse"][:4096])
+    # the logits-reuse route over the same 70000 rows (one CTA per row)
+    L, yl, tau = synth.logits_inputs(T, part, 0.8, seed=81)
+    lf = lp.lp_forward_from_logits([dev_bf16(a) for a in L], P, dev_i32(yl), tau)
+    assert lp.lp_get_device_error() == 0
+    lref = oracle.forward_from_logits(L, part, yl, tau, rows=rows)
+    assert max_abs(_np(lf["logp"])[rows], lref.logp) <= TOL_LOGP
+    assert max_abs(_np(lf["entropy"])[rows], lref.entropy) <= TOL_ENT
 
 
 def test_projection_row_chunks_forward_and_backward(lp):
