@@ -72,7 +72,9 @@ typedef enum {
   LP_ERR_REPLAY_ID_OUT_OF_RANGE = 6, /* device: a replay id not in {-1} U [0, vocab_real) */
   LP_ERR_DEVICE_TIMEOUT = 7,       /* device: a pipeline wait ran past its limit */
   LP_ERR_CUDA = 8,                 /* a CUDA runtime call failed */
-  LP_ERR_REPLAY_TOO_MANY_IDS = 9   /* device: a keep-mask row kept more than 64 ids (row fails closed) */
+  LP_ERR_REPLAY_TOO_MANY_IDS = 9,  /* device: a keep-mask row kept more than 64 ids (row fails closed) */
+  LP_ERR_BOUNDS = 10               /* device, bounds-checked builds only: an index failed its check and
+                                      the access was skipped (see lp_debug_bounds_build) */
 } lp_status;
 
 typedef enum {
@@ -317,6 +319,20 @@ LP_API lp_status lp_get_device_error(lp_stream_t stream);
  * device error word and the kernel exits cleanly, leaving the context usable. Read the
  * result with lp_get_device_error(). Nothing hangs and nothing faults. */
 LP_API lp_status lp_selftest_wait_timeout(uint64_t limit_ns, lp_stream_t stream);
+
+/* 1 if this library was built with device-side bounds checks (LP_DEBUG_BOUNDS=1), else 0.
+ * The compute sanitizer is not available on every machine; such a build stands in for its
+ * out-of-bounds checks: every global index a kernel computes (from the grid, the partition,
+ * the targets or the replay ids) is compared with the extent of its buffer before the
+ * access, and a failed comparison records LP_ERR_BOUNDS in the device error word and skips
+ * the access instead of touching memory. Results are otherwise bitwise those of the
+ * regular build, which compiles the checks away. */
+LP_API int lp_debug_bounds_build(void);
+
+/* Self-test of the bounds checks: one thread checks an index equal to its extent. A
+ * bounds-checked build records LP_ERR_BOUNDS (read it with lp_get_device_error()); the
+ * regular build records nothing. No memory is accessed either way. */
+LP_API lp_status lp_selftest_bounds(lp_stream_t stream);
 
 /* 1 if the current device can run this library (sm_100 family, e.g. GB300), else 0. */
 LP_API int lp_device_supported(void);

@@ -41,6 +41,7 @@ STATUS_NAMES = {
     7: "LP_ERR_DEVICE_TIMEOUT",
     8: "LP_ERR_CUDA",
     9: "LP_ERR_REPLAY_TOO_MANY_IDS",
+    10: "LP_ERR_BOUNDS",
 }
 
 LP_OP_FORWARD = 0
@@ -59,7 +60,7 @@ _LP_DTYPES = {torch.float32: LP_DTYPE_F32, torch.bfloat16: LP_DTYPE_BF16}
 EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward_host", "lp_forward_from_logits",
             "lp_top_p_replay", "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward",
             "lp_backward_ex", "lp_backward_from_logits", "lp_get_device_error", "lp_selftest_wait_timeout",
-            "lp_device_supported", "lp_status_string")
+            "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported", "lp_status_string")
 
 
 class LPError(RuntimeError):
@@ -134,16 +135,27 @@ def lib() -> ctypes.CDLL:
     L.lp_forward_host.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, P(_Outputs), vp, sz, vp]
     L.lp_get_device_error.argtypes = [vp]
     L.lp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    L.lp_selftest_bounds.argtypes = [vp]
+    L.lp_debug_bounds_build.argtypes = []
     L.lp_device_supported.argtypes = []
     L.lp_status_string.argtypes = [ctypes.c_int]
     L.lp_status_string.restype = ctypes.c_char_p
     for name in ("lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
                  "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask",
                  "lp_backward", "lp_backward_ex", "lp_backward_from_logits", "lp_forward_host", "lp_get_device_error",
-                 "lp_selftest_wait_timeout", "lp_device_supported"):
+                 "lp_selftest_wait_timeout", "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
+
+
+def use_library(path: str) -> ctypes.CDLL:
+    """Load the library at `path` (e.g. the bounds-checked liblp_debug.so) for every later
+    call of this module, in place of the one loaded so far."""
+    global _lib, LIB_PATH
+    LIB_PATH = path
+    _lib = None
+    return lib()
 
 
 # ------------------------------------------------------------------ marshalling
@@ -202,6 +214,18 @@ def lp_get_device_error(stream: Optional[int] = None) -> int:
     """Synchronise the stream and return (and clear) the sticky device error code."""
     s = _stream(torch.cuda.current_device()) if stream is None else stream
     return int(lib().lp_get_device_error(s))
+
+
+def lp_debug_bounds_build() -> bool:
+    """True if the loaded library was built with device-side bounds checks."""
+    return bool(lib().lp_debug_bounds_build())
+
+
+def lp_selftest_bounds(stream: Optional[int] = None) -> None:
+    """Run the bounds-check self-test (LP_ERR_BOUNDS in the device error word of a
+    bounds-checked build, nothing in the regular one)."""
+    s = _stream(torch.cuda.current_device()) if stream is None else stream
+    _raise(lib().lp_selftest_bounds(s), "lp_selftest_bounds")
 
 
 def lp_selftest_wait_timeout(limit_ns: int, stream: Optional[int] = None) -> None:

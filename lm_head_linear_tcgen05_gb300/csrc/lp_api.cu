@@ -35,6 +35,12 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, unsigned int* er
   __syncthreads();
 }
 
+// One thread checks an index equal to its extent: a bounds-checked build records
+// LP_ERR_BOUNDS, the regular build nothing. No memory is read or written.
+__global__ void bounds_selftest_kernel(int64_t extent, unsigned int* err) {
+  if (threadIdx.x == 0) (void)in_bounds(extent < extent, err);
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -198,6 +204,7 @@ const char* lp_status_string(lp_status s) {
     case LP_ERR_DEVICE_TIMEOUT: return "LP_ERR_DEVICE_TIMEOUT: a pipeline wait exceeded its time limit";
     case LP_ERR_CUDA: return "LP_ERR_CUDA: a CUDA runtime call failed";
     case LP_ERR_REPLAY_TOO_MANY_IDS: return "LP_ERR_REPLAY_TOO_MANY_IDS: a keep-mask row keeps more than 64 ids";
+    case LP_ERR_BOUNDS: return "LP_ERR_BOUNDS: a device bounds check failed (bounds-checked build)";
   }
   return "unknown lp_status";
 }
@@ -701,10 +708,21 @@ lp_status lp_backward_from_logits(const void* const* logits, const int64_t* ld, 
   p.n_shards = sh.n;
   p.T = int32_t(T);
   p.out_bf16 = bf16 ? 1 : 0;
+  p.err = dev->err;
   p.scale_log2 = float(1.4426950408889634 / double(tau));
   p.inv_tau = float(1.0 / double(tau));
   if (launch_logits_backward(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
   return LP_OK;
+}
+
+int lp_debug_bounds_build(void) { return LP_DEBUG_BOUNDS ? 1 : 0; }
+
+lp_status lp_selftest_bounds(lp_stream_t stream) {
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+  bounds_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(int64_t(1), dev->err);
+  return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
 lp_status lp_selftest_wait_timeout(uint64_t limit_ns, lp_stream_t stream) {

@@ -44,6 +44,23 @@ __device__ __forceinline__ void record_error(unsigned int* err, unsigned int cod
   if (err) atomicCAS(err, 0u, code);  // first error wins
 }
 
+// Device-side bounds checks of the bounds-checked build (LP_DEBUG_BOUNDS=1): in_bounds(ok,
+// err) returns ok and, when ok is false, records LP_ERR_BOUNDS, so that the caller skips the
+// access. In the regular build it returns true and the comparison compiles away.
+#ifndef LP_DEBUG_BOUNDS
+#define LP_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned int* err) {
+#if LP_DEBUG_BOUNDS
+  if (!ok) record_error(err, LP_ERR_BOUNDS);
+  return ok;
+#else
+  (void)ok;
+  (void)err;
+  return true;
+#endif
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

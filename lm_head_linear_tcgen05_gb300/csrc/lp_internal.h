@@ -135,6 +135,7 @@ struct LogitsGradParams {
   int32_t out_bf16;
   float scale_log2;                      // log2(e) / tau
   float inv_tau;
+  unsigned int* err;                     // device error word (bounds-checked builds)
 };
 
 // Compact top-p replay, one CTA per row. Scores come from x . W[v] + b[v] (X, W, bias)

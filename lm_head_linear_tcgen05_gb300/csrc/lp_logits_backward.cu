@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kLgThreads) logits_backward_kernel(const __gri
 #pragma unroll
       for (int u = 0; u < kLgUnroll; ++u) {
         const int64_t j = j0 + int64_t(u) * kLgThreads;
-        if (j < nfull) v[u] = __ldcs(reinterpret_cast<const uint4*>(L) + j);
+        if (j < nfull && in_bounds(8 * (j + 1) <= real && real <= width && width <= p.ld[k], p.err))
+          v[u] = __ldcs(reinterpret_cast<const uint4*>(L) + j);
       }
 #pragma unroll
       for (int u = 0; u < kLgUnroll; ++u) {
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(kLgThreads) logits_backward_kernel(const __gri
           for (int e = 0; e < 8; ++e)
             if (e == d) gv[e] = __fadd_rn(gv[e], r.gi);
         }
-        store8(O, bf16, j << 3, gv);
+        if (in_bounds(8 * (j + 1) <= width && width <= p.ld_out[k], p.err)) store8(O, bf16, j << 3, gv);
       }
     }
     // the rest of the row: the vector holding the last real ids, vectors of padded ids,

@@ -177,6 +177,11 @@ __global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_k
       const int64_t v = uniq[i];
       const int k = shard_of(p, v);
       const int64_t local = v - p.shard_start[k];
+      // the gathered row lies inside shard k's weight (the same for every lane)
+      if (!in_bounds(local >= 0 && v < p.shard_end[k] && v < p.vocab_real, p.err)) {
+        if (lane == 0) zs[i] = 0.f;
+        continue;
+      }
       const uint4* wrow = reinterpret_cast<const uint4*>(p.W[k]) + size_t(local) * size_t(nvec);
       const float dot = warp_dot(wrow, xs, nvec, lane);
       if (lane == 0) {
@@ -189,7 +194,9 @@ __global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_k
     if (tid < n) {
       const int64_t v = uniq[tid];
       const int k = shard_of(p, v);
-      const float l = __bfloat162float(p.logits[k][size_t(row) * size_t(p.ld[k]) + size_t(v - p.shard_start[k])]);
+      const int64_t col = v - p.shard_start[k];
+      const bool ok = in_bounds(col >= 0 && v < p.shard_end[k] && col < p.ld[k] && v < p.vocab_real, p.err);
+      const float l = ok ? __bfloat162float(p.logits[k][size_t(row) * size_t(p.ld[k]) + size_t(col)]) : 0.f;
       zs[tid] = __fmul_rn(l, p.inv_tau);
     }
   }

@@ -154,6 +154,8 @@ __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_l
     RawStat st{-INFINITY, -INFINITY, 0ull, 0ull, 0u};
     int64_t j0 = tid;  // this thread's vectors: j0, j0 + 256, ...
     for (; j0 + kBatch - kStreamThreads < nvec; j0 += kBatch) {
+      // the batch's last vector ends inside the shard's real columns
+      if (!in_bounds(8 * (j0 + kBatch - kStreamThreads + 1) <= width, p.err)) break;
       uint4 v[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) v[u] = __ldcs(src + j0 + int64_t(u) * kStreamThreads);
@@ -164,13 +166,16 @@ __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_l
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int64_t j = j0 + int64_t(u) * kStreamThreads;
-        v[u] = j < nvec ? __ldcs(src + j) : make_uint4(kNegInfPair, kNegInfPair, kNegInfPair, kNegInfPair);
+        v[u] = j < nvec && in_bounds(8 * (j + 1) <= width, p.err)
+                   ? __ldcs(src + j)
+                   : make_uint4(kNegInfPair, kNegInfPair, kNegInfPair, kNegInfPair);
       }
       raw_fold_batch(st, v, int((nvec - j0 + kStreamThreads - 1) / kStreamThreads), c2, span);
     }
     // ragged tail (width % 8 elements) by the first threads, in ascending order
     const int64_t tail0 = nvec << 3;
-    if (width > 0 && tail0 + tid < width) raw_push1(st, __bfloat162float(L[tail0 + tid]), c2, span);
+    if (width > 0 && tail0 + tid < width && in_bounds(tail0 + tid < p.ld[k], p.err))
+      raw_push1(st, __bfloat162float(L[tail0 + tid]), c2, span);
 
     Stat loc = raw_to_stat(st);
 #pragma unroll
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_l
     for (int w = 1; w < kStreamWarps; ++w) stat_merge(sh, red[k][w]);
     const bool own = y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k];
     float tk = 0.f;
-    if (own) {
+    if (own && in_bounds(yv - p.shard_start[k] < p.shard_width[k], p.err)) {
       const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
       tk = __fmul_rn(__bfloat162float(L[yv - p.shard_start[k]]), p.inv_tau);
       t_val = tk;
