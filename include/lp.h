@@ -35,8 +35,9 @@
  *    depends only on the partition and compile-time tile sizes.
  *  - Host-side validation errors are returned before anything is launched.
  *    Errors found on the device (a target or replay id out of range, a
- *    pipeline wait that timed out) are recorded in a sticky per-device error
- *    word read by lp_get_device_error(); the affected rows get logp = -inf.
+ *    pipeline wait that timed out, a failed bounds check of a bounds-checked
+ *    build) are recorded in a sticky per-device error word read by
+ *    lp_get_device_error(); the affected rows get logp = -inf.
  *  - A call made while the current device is not sm_100-family (GB300 is
  *    sm_103) returns LP_ERR_UNSUPPORTED_DEVICE. There is no CPU fallback.
  */
