@@ -262,7 +262,9 @@ struct GradEpi : GemmEpiBase {
           const float oh = (int64_t(col) == ycol) ? 1.f : 0.f;
           // logp term g (1[v = y] - p) / tau, entropy term - h p (z - mu) / tau
           float gval = __fmul_rn(gi, __fsub_rn(oh, pr));
-          if (hi != 0.f) gval = __fsub_rn(gval, __fmul_rn(__fmul_rn(hi, pr), __fsub_rn(__fmul_rn(v, p.inv_tau), mu)));
+          // (p = 0 adds nothing; skipping it keeps a -inf-biased id from forming 0 * -inf)
+          if (hi != 0.f && pr != 0.f)
+            gval = __fsub_rn(gval, __fmul_rn(__fmul_rn(hi, pr), __fsub_rn(__fmul_rn(v, p.inv_tau), mu)));
           gv[j] = (col < valid && live) ? gval : 0.f;
         }
       } else {

@@ -63,12 +63,15 @@ __device__ __forceinline__ void chunk_sums_full(const uint32_t (&r)[32], float c
   }
 }
 
+// A bias of -inf masks its id out (p = 0). The scaled difference is clamped at -256, where
+// 2^d is 0 either way, so such an id never forms 0 * -inf (nor -inf - -inf when a whole
+// block is masked); for every finite d below -256 the sums are unchanged.
 __device__ __forceinline__ void chunk_sums_masked(const uint32_t (&r)[32], float bl, int lim, float c2, float m_u,
                                                   Sums4& acc) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const float v = __fadd_rn(f32(r[j]), __shfl_sync(0xffffffffu, bl, j));
-    const float d = __fmaf_rn(v, c2, -m_u);
+    const float d = fmaxf(__fmaf_rn(v, c2, -m_u), -256.f);
     const float e = hw_ex2(d);
     const bool in = j < lim;
     acc.s[j & 3] = in ? __fadd_rn(acc.s[j & 3], e) : acc.s[j & 3];

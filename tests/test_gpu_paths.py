@@ -290,6 +290,60 @@ def test_replay_errors_and_empty_rows(lp):
 
 # --------------------------------------------------------------------- backward
 
+def test_minus_inf_bias_masks_ids_forward_and_backward(lp):
+    """A bias of -inf masks an id out of the softmax (p = 0): forward statistics and every
+    gradient stay finite, and masked ids get exactly zero dW and db. As in the logits-reuse
+    test, the oracle sees -1e30, whose exponential is exactly 0 in fp64 as well. Masked: a
+    whole 256-id vocabulary block and 15 % of the other ids (never a target)."""
+    import torch
+    bounds, real = [0, 600, 1200], 1190
+    part = synth.ranges_partition(real, bounds[-1], bounds)
+    T, H = 70, 96
+    inp = synth.forward_inputs(T, H, part, tau=0.7, seed=61, w_std=0.1, bias_std=0.2)
+    rng = np.random.default_rng(62)
+    masked = np.zeros(bounds[-1], bool)
+    masked[256:512] = True
+    masked[rng.choice(real, size=int(0.15 * real), replace=False)] = True
+    masked[real:] = False
+    live = np.flatnonzero(~masked[:real])
+    y = rng.choice(live, size=T).astype(np.int32)
+    neg_inf = np.uint16(0xFF80)
+    very_low = synth.bf16_bits(np.array([-1e30], np.float32))[0]
+    b_gpu, b_ora = [], []
+    for (s, e), bk in zip(part.ranges, inp.bias):
+        m = masked[s:e]
+        b_gpu.append(np.where(m, neg_inf, bk).astype(np.uint16))
+        b_ora.append(np.where(m, very_low, bk).astype(np.uint16))
+    X, W, _, _ = dev_inputs(inp)
+    b = [dev_bf16(x) for x in b_gpu]
+    P = part_of(part)
+    yd = dev_i32(y)
+    fwd = lp.lp_forward(X, W, b, P, yd, inp.tau, shard_stats=True)
+    assert lp.lp_get_device_error() == 0
+    ref = oracle.forward(inp.X, inp.W, b_ora, part, y, inp.tau)
+    lg, ls, en = _np(fwd["logp"]), _np(fwd["lse"]), _np(fwd["entropy"])
+    assert np.all(np.isfinite(lg)) and np.all(np.isfinite(ls)) and np.all(np.isfinite(en))
+    assert max_abs(lg, ref.logp) <= TOL_LOGP
+    assert max_abs(ls, ref.lse) <= TOL_LSE
+    assert max_abs(en, ref.entropy) <= TOL_ENT
+    assert not np.isnan(_np(fwd["shard_stats"])).any()
+    g = synth.upstream_grad(T, seed=63)
+    h = synth.upstream_grad(T, seed=64)
+    bw = lp.lp_backward(X, W, b, P, yd, inp.tau, fwd["lse"], dev_f32(g), entropy=fwd["entropy"],
+                        grad_entropy=dev_f32(h))
+    assert lp.lp_get_device_error() == 0
+    bref = oracle.backward(inp.X, inp.W, b_ora, part, y, inp.tau, g, h=h)
+    assert rel_fro(_np(bw["dX"]), bref.dX) <= TOL_GRAD_REL
+    for k, (s, e) in enumerate(part.ranges):
+        dw, db = _np(bw["dW"][k]), _np(bw["db"][k])
+        assert np.all(np.isfinite(dw)) and np.all(np.isfinite(db))
+        assert rel_fro(dw, bref.dW[k]) <= TOL_GRAD_REL, k
+        assert rel_fro(db, bref.db[k]) <= TOL_GRAD_REL, k
+        m = masked[s:e]
+        assert np.all(dw[m] == 0) and np.all(db[m] == 0), k
+
+
+
 @pytest.mark.parametrize("T,H,bounds,real,bias", [
     (64, 256, [0, 1000], 1000, None),
     (200, 192, [0, 700, 700, 1500, 2048], 2000, 0.3),    # empty shard, padding, ragged rows
