@@ -52,6 +52,20 @@ def test_status_strings(lp):
         assert lp.lp_status_string(code).startswith(name)
 
 
+def test_bounds_checked_build_builds_and_says_so(lp):
+    # the regular library reports no checks; the bounds-checked one (built from the same
+    # sources with LP_DEBUG_BOUNDS=1) exports the same C ABI and reports them
+    from lm_head_linear_tcgen05_gb300 import _build
+    path = _build.build(debug_bounds=True)
+    assert lp.lib().lp_debug_bounds_build() == 0
+    D = ctypes.CDLL(path)
+    assert D.lp_debug_bounds_build() == 1
+    for name in _declared():
+        assert hasattr(D, name), name
+    if not _has_gpu():
+        assert D.lp_selftest_bounds(None) == 3     # LP_ERR_UNSUPPORTED_DEVICE without a GPU
+
+
 def _part(lp, real, padded, bounds):
     return lp.VocabPartition(real, padded, tuple((bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1)))
 
