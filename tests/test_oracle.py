@@ -24,6 +24,25 @@ def _dec(bits):
     return struct.unpack("<f", struct.pack("<I", (int(bits) & 0xFFFF) << 16))[0]
 
 
+def test_bf16_decode_against_the_format_definition():
+    # bf16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits; value written out from
+    # the definition for every one of the 65536 codes (normal, subnormal, zero, inf, NaN)
+    codes = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):          # signalling NaN codes widen with a warning
+        got = oracle.bf16_to_f64(codes)
+    for c in range(1 << 16):
+        s, e, f = c >> 15, (c >> 7) & 0xFF, c & 0x7F
+        sign = -1.0 if s else 1.0
+        if e == 0xFF:
+            if f == 0:
+                assert got[c] == sign * math.inf, hex(c)
+            else:
+                assert math.isnan(got[c]), hex(c)
+            continue
+        want = sign * (math.ldexp(f, -126 - 7) if e == 0 else math.ldexp(128 + f, e - 127 - 7))
+        assert got[c] == want and math.copysign(1.0, got[c]) == sign, hex(c)
+
+
 def _zeros_like_W(part, H):
     return [np.zeros((e - s, H), np.uint16) for s, e in part.ranges]
 
