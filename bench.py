@@ -12,9 +12,12 @@ vocabulary-sharded forward + backward
 
 Every input is synthetic and seeded; the weights and logits are larger than the
 129 MB L2, so no flush is needed between timed steps. --impl reference times the fp64
-CPU oracle on the host cores on a bounded row sample of the same workload.
-N > 1 (torchrun): every rank runs the same workload on its own GPU (replicas, no
-collective on the data path); the value is all rows over the slowest rank's time.
+CPU oracle on the host cores on a bounded row sample of the same workload (under
+torchrun, rank 0 alone runs it).
+
+One GPU only: the projection GEMMs share each W tile between the two CTAs of a cluster
+with TMA multicast loads, which this library runs on single-GPU calls only, so the GPU arm
+refuses a run with more than one rank (or --gpus > 1) before it touches a GPU.
 """
 from __future__ import annotations
 
@@ -227,19 +230,19 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def reduce_max_ms(ms: float, dist, device) -> float:
-    """Slowest rank's time: the only collective of the multi-GPU run (no data exchange)."""
-    if dist is None:
-        return ms
-    import torch
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+ONE_GPU_ONLY = ("one-GPU library: its projection GEMMs load each W tile once per pair of SMs with TMA "
+                "cluster multicast, which this build runs on single-GPU calls only; run bench.py with one rank "
+                "and --gpus 1")
 
 
-def whole_job_rate(rows_per_rank: int, world: int, ms_max: float) -> float:
-    """Rows processed by all ranks per second of the slowest rank (weak scaling)."""
-    return world * rows_per_rank / (ms_max * 1e-3)
+def refuse_multi_gpu(args, world: int) -> bool:
+    """The GPU arm runs on one GPU only: with more than one rank (or --gpus > 1) it prints one
+    JSON line saying why and returns True, before any GPU or process-group work."""
+    if args.impl == "ours" and (world > 1 or args.gpus > 1):
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps({"impl": "ours", "n_gpus": max(world, args.gpus), "error": ONE_GPU_ONLY}), flush=True)
+        return True
+    return False
 
 
 def time_steps(fn, steps, warmup, stream, sampler=None):
@@ -263,7 +266,7 @@ def time_steps(fn, steps, warmup, stream, sampler=None):
 
 # -------------------------------------------------------------- our GPU arm
 
-def run_ours(args, rank, world, dist):
+def run_ours(args):
     import numpy as np
     import torch
 
@@ -272,9 +275,8 @@ def run_ours(args, rank, world, dist):
 
     from lm_head_linear_tcgen05_gb300 import _build
     _build.build()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     if not lp.lp_device_supported():
         raise RuntimeError("this GPU cannot run liblp.so (sm_103a build)")
     stream = torch.cuda.current_stream(dev)
@@ -282,8 +284,7 @@ def run_ours(args, rank, world, dist):
 
     if args.skip_headline:
         paths = time_other_paths(args, lp, synth, dev, stream, peaks)
-        if rank == 0:
-            print(json.dumps({"paths": paths}), flush=True)
+        print(json.dumps({"paths": paths}), flush=True)
         return
 
     # ---- headline: fused forward, T=4096, H=4096, V=151936, tau=0.7, no bias
@@ -293,16 +294,13 @@ def run_ours(args, rank, world, dist):
     X, W, _, y = synth.device_forward_inputs(T_FWD, H, part, TAU, dev, seed=0)
     ws = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD, T_FWD, H, P), dtype=torch.uint8, device=dev)
     step = lambda: lp.lp_forward(X, W, None, P, y, TAU, workspace=ws)
-    if dist is not None:
-        dist.barrier()
     clk = clock_sampler(dev)
     ms = time_steps(step, args.steps, args.warmup, stream, sampler=clk)
     if lp.lp_get_device_error() != 0:
         raise RuntimeError("device error during the timed forward")
-    ms = reduce_max_ms(ms, dist, dev)
     flops = 2.0 * T_FWD * H * V
     tflops = flops / (ms * 1e-3) / 1e12
-    value = whole_job_rate(T_FWD, world, ms)
+    value = T_FWD / (ms * 1e-3)
 
     # ---- end to end through the C entry point lp_forward_host: pinned host X, y in; host logp,
     # lse, entropy out. The call copies the inputs in, runs the forward and copies the outputs
@@ -320,7 +318,6 @@ def run_ours(args, rank, world, dist):
     for _ in range(args.steps):
         lp.lp_forward_host(hX, W, None, P, hy, TAU, workspace=ws_host, out=host_out)
     ms_e2e = (time.perf_counter() - t0) * 1e3 / args.steps
-    ms_e2e = reduce_max_ms(ms_e2e, dist, dev)
     ref = lp.lp_forward(X, W, None, P, y, TAU, workspace=ws)
     if not torch.equal(host_out["logp"], ref["logp"].cpu()):
         raise RuntimeError("host-staged forward differs from the device forward")
@@ -345,20 +342,18 @@ def run_ours(args, rank, world, dist):
     clk_sus = clock_sampler(dev)
     ms_sus = time_steps(step, sus_steps, 0, stream, sampler=clk_sus)
 
-    if rank != 0:
-        return
     traffic = stored_traffic("fused_forward")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"Qwen3-8B-shaped LM-head fused forward, T={T_FWD} rows, H={H}, V={V}, "
                                "tau=0.7, no bias, logp+LSE+entropy",
                    "T": T_FWD, "H": H, "V": V, "tau": TAU, "shards": 1,
                    "l2": "inputs larger than L2 (W 1.245 GB > 129 MB); no flush",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": "one GPU"},
         "clocks": clk.summary(),
-        "e2e": {"value": whole_job_rate(T_FWD, world, ms_e2e), "unit": UNIT,
+        "e2e": {"value": T_FWD / (ms_e2e * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": T_FWD * H * 2 + T_FWD * 4, "d2h_bytes_per_step": 3 * T_FWD * 4,
                 "ms_per_step": ms_e2e, "timed": "host clock around the C entry point lp_forward_host (H2D, "
                                                   "forward, D2H, synchronised every step)"},
@@ -374,18 +369,35 @@ def run_ours(args, rank, world, dist):
                                    "clocks": clk_sus.summary()}},
         "paths": paths,
         "bitwise": {"repeat": bit_repeat, f"1x{T_FWD}_vs_{-(-T_FWD // chunk)}x{chunk}": bit_batch},
+        "build": lp.build_info(),
     }
-    if not args.no_cpu_baseline and world == 1:  # the host-core oracle runs at N = 1 only
+    if not args.no_cpu_baseline:
         line["cpu_baseline"], line["parity"] = cpu_baseline_forward(X, W, y, base, rows=1536)
     print(json.dumps(line), flush=True)
 
 
 def time_other_paths(args, lp, synth, dev, stream, peaks):
-    """The other hot-path rows, each on its own workload (vocabulary args.vocab)."""
+    """The other hot-path rows, each on its own workload (vocabulary args.vocab), each timed
+    with its own clock record."""
     import torch
     out = {}
     Vp = args.vocab
     TP = args.path_rows  # rows of the logits and replay workloads
+
+    def timed(fn, steps):
+        clk = clock_sampler(dev)
+        ms = time_steps(fn, steps, args.warmup, stream, sampler=clk)
+        return ms, clk.summary()
+
+    def hbm_roofline(nbytes, ms, kernel, **extra):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        r = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes}
+        if kernel is not None:
+            r["traffic"] = stored_traffic(kernel)
+        r.update(extra)
+        return r
+
     wanted = set(args.paths.split(","))
     if wanted & {"logits", "replay"}:
         part = synth.even_partition(Vp, 1)
@@ -399,57 +411,53 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
         uniq = sum(len(set(r[r >= 0].tolist())) for r in ids)
         if "logits" in wanted:
             # logits reuse: T=TP x V bf16 logits
-            ms = time_steps(lambda: lp.lp_forward_from_logits(L, P, y, TAU), args.steps, args.warmup, stream)
+            ms, clk = timed(lambda: lp.lp_forward_from_logits(L, P, y, TAU), args.steps)
             nbytes = TP * Vp * 2
-            gbs = nbytes / (ms * 1e-3) / 1e9
             out["logits_reuse"] = {
                 "workload": f"T={TP}, V={Vp} bf16 logits N(0,9), 1% peaked, tau=0.7",
-                "tokens_per_s": TP / (ms * 1e-3), "ms": ms,
-                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
-                             "traffic": stored_traffic("stream_logits")}}
+                "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "steps": args.steps, "clocks": clk,
+                "roofline": hbm_roofline(nbytes, ms, "stream_logits",
+                                         frac_of_8tbs=nbytes / (ms * 1e-3) / 1e9 / 8000.0)}
             # its backward: the gradient with respect to those logits, bf16, out of place
             fl = lp.lp_forward_from_logits(L, P, y, TAU)
             gl = torch.randn(TP, generator=torch.Generator(device=dev).manual_seed(4), device=dev)
             dL = [torch.empty_like(L[0])]
-            ms = time_steps(lambda: lp.lp_backward_from_logits(L, P, y, TAU, fl["lse"], gl, entropy=fl["entropy"],
-                                                               grad_entropy=gl, out=dL),
-                            args.steps, args.warmup, stream)
-            nbytes = 2 * TP * Vp * 2
-            gbs = nbytes / (ms * 1e-3) / 1e9
+            ms, clk = timed(lambda: lp.lp_backward_from_logits(L, P, y, TAU, fl["lse"], gl, entropy=fl["entropy"],
+                                                               grad_entropy=gl, out=dL), args.steps)
             out["logits_backward"] = {
                 "workload": f"gradient w.r.t. the T={TP} x V={Vp} logits above (logp + entropy terms), bf16 out",
-                "tokens_per_s": TP / (ms * 1e-3), "ms": ms,
-                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
-                             "traffic": stored_traffic("logits_backward")}}
+                "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "steps": args.steps, "clocks": clk,
+                "roofline": hbm_roofline(2 * TP * Vp * 2, ms, "logits_backward")}
             del dL, fl
         if "replay" in wanted:
-            # the compact replay scored from the reused logits above (one 2-byte gather per id)
+            # the compact replay scored from the reused logits above: per row its 64 id slots
+            # and one logit per distinct id, each logit alone in a 32-byte DRAM sector
             L4 = [L[0][:, s:e] for s, e in part4.ranges]
-            ms = time_steps(lambda: lp.lp_top_p_replay_from_logits(L4, P4, ids_d, yr_d, TAU), args.steps,
-                            args.warmup, stream)
+            ms, clk = timed(lambda: lp.lp_top_p_replay_from_logits(L4, P4, ids_d, yr_d, TAU), args.steps)
+            sector_bytes = TP * (64 * 4 + 4) + uniq * 32
             out["top_p_replay_from_logits"] = {
                 "workload": f"T={TP} rows of the logits above in 4 shards, 1-64 ids/row",
-                "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "ids_scored": uniq}
+                "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "steps": args.steps, "clocks": clk,
+                "ids_scored": uniq,
+                "roofline": hbm_roofline(sector_bytes, ms, None,
+                                         note="bytes counted at DRAM sector granularity (32 B per gathered logit, "
+                                              "plus the id slots and targets); bound by the latency of each row's "
+                                              "dependent loads (ids, then the gathered logits), not by bandwidth")}
         del L
         torch.cuda.empty_cache()
         if "replay" in wanted:
             # compact top-p replay: T=TP, 4 shards, ids as the nucleus recipe
             X, W, _, _ = synth.device_forward_inputs(TP, H, part4, TAU, dev, seed=5)
-            ms = time_steps(lambda: lp.lp_top_p_replay(X, W, None, P4, ids_d, yr_d, TAU), args.steps, args.warmup,
-                            stream)
+            ms, clk = timed(lambda: lp.lp_top_p_replay(X, W, None, P4, ids_d, yr_d, TAU), args.steps)
             distinct = len(set(ids[ids >= 0].tolist()))
             gathered = TP * H * 2 + uniq * H * 2
             distinct_b = TP * H * 2 + distinct * H * 2
             out["top_p_replay"] = {
                 "workload": f"T={TP}, H=4096, V={Vp} in 4 shards, 1-64 ids/row (+10% dups), tau=0.7",
-                "tokens_per_s": TP / (ms * 1e-3), "ms": ms,
+                "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "steps": args.steps, "clocks": clk,
                 "gathered_bytes": gathered, "distinct_bytes": distinct_b,
-                "roofline": {"bound": "hbm", "achieved": gathered / (ms * 1e-3) / 1e9,
-                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": gathered / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                             "traffic": stored_traffic("replay")}}
+                "roofline": hbm_roofline(gathered, ms, "replay",
+                                         frac_distinct=distinct_b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"])}
             del X, W
             torch.cuda.empty_cache()
 
@@ -464,22 +472,25 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
         wsf = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
         wsb = torch.empty(lp.lp_workspace_size(lp.LP_OP_BACKWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
         fwd = lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf)
-        ms_f = time_steps(lambda: lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf), args.steps, args.warmup,
-                          stream)
-        ms_b = time_steps(lambda: lp.lp_backward(X, W, b, P3, y, TAU, fwd["lse"], g, workspace=wsb),
-                          max(3, args.steps // 2), args.warmup, stream)
+        ms_f, clk_f = timed(lambda: lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf), args.steps)
+        bsteps = max(20, args.steps)
+        ms_b, clk_b = timed(lambda: lp.lp_backward(X, W, b, P3, y, TAU, fwd["lse"], g, workspace=wsb), bsteps)
         f_fl = 2.0 * T_FWD * H * Vp
+        b_tf = 3 * f_fl / (ms_b * 1e-3) / 1e12
         out["sharded_fwd_bwd"] = {
             "workload": f"T=4096, H=4096, V={Vp} padded to {Vpad}, 4 shards, bias, tau=0.7",
-            "fwd_tokens_per_s": T_FWD / (ms_f * 1e-3), "fwd_ms": ms_f,
-            "bwd_tokens_per_s": T_FWD / (ms_b * 1e-3), "bwd_ms": ms_b,
+            "fwd_tokens_per_s": T_FWD / (ms_f * 1e-3), "fwd_ms": ms_f, "fwd_steps": args.steps, "fwd_clocks": clk_f,
+            "bwd_tokens_per_s": T_FWD / (ms_b * 1e-3), "bwd_ms": ms_b, "bwd_steps": bsteps, "bwd_clocks": clk_b,
             "fwd_bwd_tokens_per_s": T_FWD / ((ms_f + ms_b) * 1e-3),
-            "fwd_tflops": f_fl / (ms_f * 1e-3) / 1e12,
-            "bwd_tflops_3gemm": 3 * f_fl / (ms_b * 1e-3) / 1e12,
-            "bwd_frac_3gemm": 3 * f_fl / (ms_b * 1e-3) / 1e12 / peaks["bf16_tflops"],
-            # ~0.1 s of back-to-back GEMMs runs into the power cap: the sustained peak is the
-            # matching denominator
-            "bwd_frac_3gemm_of_sustained": 3 * f_fl / (ms_b * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"]}
+            "fwd_roofline": {"bound": "tensor", "achieved": f_fl / (ms_f * 1e-3) / 1e12,
+                             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": f_fl / (ms_f * 1e-3) / 1e12 / peaks["bf16_tflops"]},
+            # three GEMMs of 2 T H V each (G recomputed, dW, dX); ~0.2 s of back-to-back GEMMs
+            # runs into the power cap, so the sustained peak is reported beside the burst one
+            "bwd_roofline": {"bound": "tensor", "achieved": b_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": b_tf / peaks["bf16_tflops"],
+                             "frac_of_sustained": b_tf / peaks["bf16_tflops_sustained"],
+                             "flops_per_call": 3 * f_fl}}
     if lp.lp_get_device_error() != 0:
         raise RuntimeError("device error in the path timings")
     return out
@@ -526,9 +537,7 @@ def cpu_baseline_forward(X, W, y, gpu_out, rows: int):
     return base, parity
 
 
-def run_reference(args, rank, world):
-    if rank != 0:
-        return
+def run_reference(args, world):
     import oracle
     import synth
     rows = args.ref_rows
@@ -576,20 +585,15 @@ def main(argv=None):
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        backend = "gloo" if args.impl == "reference" else "nccl"
-        dist.init_process_group(backend)
-    try:
-        if args.impl == "reference":
-            run_reference(args, rank, world)
-        else:
-            run_ours(args, rank, world, dist)
-    finally:
-        if dist is not None:
-            dist.destroy_process_group()
+    if refuse_multi_gpu(args, world):
+        return 2
+    if args.impl == "reference":
+        if rank == 0:  # under torchrun the other ranks exit without work
+            run_reference(args, world)
+    else:
+        run_ours(args)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -297,10 +297,16 @@ LP_API lp_status lp_backward_from_logits(const void* const* logits, const int64_
  * outputs are still the caller's device memory. The call allocates nothing (no
  * cudaMalloc, no allocating library routine) and frees nothing.
  *  - Limit: lp_workspace_size(LP_OP_FORWARD, T, H, part) must not exceed
- *    LP_NOALLOC_SCRATCH_BYTES (32 MiB: e.g. T <= 4705 rows at V = 151936 in one
- *    shard); larger problems return LP_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *    LP_NOALLOC_SCRATCH_BYTES (32 MiB). That size is 3 * align256(4 T nb) +
+ *    align256(4 T) bytes, nb = the number of 256-id vocabulary blocks (594 at
+ *    V = 151936 in one shard), so at that vocabulary T <= 4704 rows fit and
+ *    T = 4705 does not. Larger problems return LP_ERR_WORKSPACE_TOO_SMALL before
+ *    any launch.
  *  - The first call on each device looks up that device's address of the array
  *    (with the device current); make that first call before any stream capture.
+ *    The address is kept for the life of the process, so the device must not be
+ *    reset (cudaDeviceReset) between calls: the array could move and later calls
+ *    would write through a stale address.
  *  - Every call shares the one array and it keeps the previous call's contents.
  *    Nothing in it needs to start at zero (each call writes every slot it reads),
  *    but calls whose kernels overlap on the GPU - on different streams, or from
@@ -334,6 +340,11 @@ LP_API int lp_debug_bounds_build(void);
  * bounds-checked build records LP_ERR_BOUNDS (read it with lp_get_device_error()); the
  * regular build records nothing. No memory is accessed either way. */
 LP_API lp_status lp_selftest_bounds(lp_stream_t stream);
+
+/* Identity of this build: a hash of the sources and code flags it was compiled from (a
+ * static string; "unknown" for a build made without the in-tree build script). Lets a
+ * caller check that the library it loaded was built from the sources it expects. */
+LP_API const char* lp_build_id(void);
 
 /* 1 if the current device can run this library (sm_100 family, e.g. GB300), else 0. */
 LP_API int lp_device_supported(void);

@@ -19,6 +19,8 @@ from typing import Optional, Sequence, Tuple
 
 import torch
 
+from . import _build
+from ._build import DEBUG_LIB as _BUILT_DEBUG_LIB
 from ._build import LIB as _BUILT_LIB
 
 # The in-tree build by default; LP_LIBRARY points the binding at another build of the
@@ -60,7 +62,8 @@ _LP_DTYPES = {torch.float32: LP_DTYPE_F32, torch.bfloat16: LP_DTYPE_BF16}
 EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward_host", "lp_forward_from_logits",
             "lp_top_p_replay", "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward",
             "lp_backward_ex", "lp_backward_from_logits", "lp_get_device_error", "lp_selftest_wait_timeout",
-            "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported", "lp_status_string")
+            "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported", "lp_status_string",
+            "lp_build_id")
 
 
 class LPError(RuntimeError):
@@ -106,7 +109,8 @@ _lib = None
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded liblp.so (raises ImportError if it has not been built)."""
+    """The loaded liblp.so (raises ImportError if it has not been built, or if an in-tree
+    build was compiled from other sources than the ones beside it)."""
     global _lib
     if _lib is not None:
         return _lib
@@ -114,6 +118,16 @@ def lib() -> ctypes.CDLL:
         raise ImportError(f"liblp.so is not built ({LIB_PATH}); run "
                           "`python -m lm_head_linear_tcgen05_gb300._build` or __graft_entry__.build()")
     L = ctypes.CDLL(LIB_PATH)
+    L.lp_build_id.argtypes = []
+    L.lp_build_id.restype = ctypes.c_char_p
+    built = L.lp_build_id().decode()
+    in_tree = {os.path.realpath(_BUILT_LIB): False, os.path.realpath(_BUILT_DEBUG_LIB): True}
+    debug = in_tree.get(os.path.realpath(LIB_PATH))
+    if debug is not None:
+        want = _build.source_hash(debug_bounds=debug)
+        if built != want:
+            raise ImportError(f"{LIB_PATH} was built from sources {built}, but the sources here hash to {want}: "
+                              "rebuild it (`python -m lm_head_linear_tcgen05_gb300._build`)")
     vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     P = ctypes.POINTER
     L.lp_workspace_size.argtypes = [ctypes.c_int, i64, i64, P(_Partition)]
@@ -199,6 +213,21 @@ def _raise(st: int, where: str):
 
 def lp_status_string(status: int) -> str:
     return lib().lp_status_string(int(status)).decode()
+
+
+def lp_build_id() -> str:
+    """Hash of the sources and code flags the loaded library was compiled from."""
+    return lib().lp_build_id().decode()
+
+
+def build_info() -> dict:
+    """Which library is loaded, its build id, and whether this process compiled it."""
+    info = {"library": LIB_PATH, "build_id": lp_build_id()}
+    for rec in _build.BUILDS.values():
+        if os.path.realpath(rec["lib"]) == os.path.realpath(LIB_PATH):
+            info["compiled_in_this_process"] = bool(rec["compiled"])
+            info["machine"] = rec["machine"]
+    return info
 
 
 def lp_device_supported() -> bool:

@@ -9,12 +9,21 @@ liblp_debug.so, a stand-in for a sanitizer's out-of-bounds checks. The CUDA runt
 statically and the driver API is reached through cudaGetDriverEntryPointByVersion,
 so the library loads on a machine without a GPU driver (every call then returns
 LP_ERR_UNSUPPORTED_DEVICE).
+
+Provenance: the library embeds a hash of the sources and flags it was compiled from
+(`lp_build_id()`), and a stamp file beside it records that hash and the machine it was
+built on. A library is reused only when its stamp matches the current sources on this
+machine; otherwise it is compiled again. `LAST_BUILD` says which happened, and the
+binding refuses to load an in-tree library whose embedded hash differs from the sources.
 """
 from __future__ import annotations
 
 import argparse
 import glob
+import hashlib
+import json
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -30,8 +39,14 @@ DEBUG_OBJDIR = os.path.join(PKG, "_build_debug")
 DEBUG_LIB = os.path.join(PKG, "liblp_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-                     "-I" + INCLUDE, "-I" + CSRC]
+CODE_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden"]
+NVCC_FLAGS = CODE_FLAGS + ["-I" + INCLUDE, "-I" + CSRC]
+DEBUG_FLAGS = ["-DLP_DEBUG_BOUNDS=1"]
+
+# the most recent build() of this process: {"lib", "compiled", "source_hash", "machine"},
+# and the latest such record of every library this process built or reused
+LAST_BUILD: dict = {}
+BUILDS: dict = {}
 
 
 def _nvcc() -> str:
@@ -48,24 +63,54 @@ def _inputs():
     return srcs, headers
 
 
-def up_to_date(lib: str = LIB) -> bool:
-    if not os.path.exists(lib):
-        return False
+def source_hash(debug_bounds: bool = False) -> str:
+    """Hash of every source and header (by path relative to the repository) and of the code
+    flags: the identity of a build, the same on every machine."""
     srcs, headers = _inputs()
-    t = os.path.getmtime(lib)
-    return all(os.path.getmtime(f) <= t for f in srcs + headers + [__file__])
+    h = hashlib.sha256()
+    for f in srcs + headers:
+        h.update(os.path.relpath(f, ROOT).replace(os.sep, "/").encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+        h.update(b"\0")
+    h.update(" ".join(CODE_FLAGS + (DEBUG_FLAGS if debug_bounds else [])).encode())
+    return h.hexdigest()[:16]
+
+
+def _stamp_path(lib_path: str) -> str:
+    return lib_path + ".stamp"
+
+
+def _stamp(src_hash: str) -> dict:
+    return {"source_hash": src_hash, "machine": platform.machine()}
+
+
+def up_to_date(lib_path: str = LIB, debug_bounds: bool = False) -> bool:
+    """True if lib_path exists and its stamp names the current sources and this machine."""
+    if not os.path.exists(lib_path):
+        return False
+    try:
+        with open(_stamp_path(lib_path)) as f:
+            return json.load(f) == _stamp(source_hash(debug_bounds))
+    except (OSError, ValueError):
+        return False
 
 
 def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False) -> str:
-    """Compile and link liblp.so (liblp_debug.so with debug_bounds) unless it is newer than
-    every source; return its path."""
+    """Compile and link liblp.so (liblp_debug.so with debug_bounds) unless an up-to-date build
+    of the current sources for this machine exists; return its path. LAST_BUILD records
+    whether it compiled."""
     lib_path, objdir = (DEBUG_LIB, DEBUG_OBJDIR) if debug_bounds else (LIB, OBJDIR)
-    if not force and up_to_date(lib_path):
+    h = source_hash(debug_bounds)
+    if not force and up_to_date(lib_path, debug_bounds):
+        LAST_BUILD.clear()
+        LAST_BUILD.update(lib=lib_path, compiled=False, **_stamp(h))
+        BUILDS[lib_path] = dict(LAST_BUILD)
         return lib_path
     nvcc = _nvcc()
     os.makedirs(objdir, exist_ok=True)
     srcs, _ = _inputs()
-    extra = ["-DLP_DEBUG_BOUNDS=1"] if debug_bounds else []
+    extra = (DEBUG_FLAGS if debug_bounds else []) + [f'-DLP_SOURCE_HASH="{h}"']
 
     def compile_one(src):
         obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
@@ -85,6 +130,12 @@ def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, lib_path)
+    with open(_stamp_path(lib_path), "w") as f:
+        json.dump(_stamp(h), f)
+    LAST_BUILD.clear()
+    LAST_BUILD.update(lib=lib_path, compiled=True, **_stamp(h))
+    BUILDS[lib_path] = dict(LAST_BUILD)
+    sys.stderr.write(f"{os.path.basename(lib_path)}: compiled from sources {h} on {platform.machine()}\n")
     return lib_path
 
 
@@ -95,3 +146,4 @@ if __name__ == "__main__":
     ap.add_argument("--debug-bounds", action="store_true", help="build liblp_debug.so with device bounds checks")
     a = ap.parse_args()
     print(build(force=a.force, verbose=a.verbose, debug_bounds=a.debug_bounds))
+    print(json.dumps(LAST_BUILD))

@@ -717,6 +717,11 @@ lp_status lp_backward_from_logits(const void* const* logits, const int64_t* ld, 
 
 int lp_debug_bounds_build(void) { return LP_DEBUG_BOUNDS ? 1 : 0; }
 
+#ifndef LP_SOURCE_HASH
+#define LP_SOURCE_HASH "unknown"
+#endif
+const char* lp_build_id(void) { return LP_SOURCE_HASH; }
+
 lp_status lp_selftest_bounds(lp_stream_t stream) {
   DeviceState* dev = nullptr;
   lp_status st = device_state(&dev);

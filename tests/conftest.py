@@ -12,6 +12,24 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103) GPU and the built CUDA library")
 
 
+def pytest_report_header(config):
+    try:
+        from lm_head_linear_tcgen05_gb300 import _build
+        state = "up to date" if _build.up_to_date() else "missing or stale (compiled by the first test that needs it)"
+        return f"liblp.so: sources {_build.source_hash()}, in-tree build {state}"
+    except Exception as e:  # the header must never stop a run
+        return f"liblp.so: build state unknown ({e})"
+
+
+def pytest_terminal_summary(terminalreporter):
+    try:
+        from lm_head_linear_tcgen05_gb300 import _build
+        for rec in _build.BUILDS.values():
+            terminalreporter.write_line(f"liblp build used by this run: {rec}")
+    except Exception:
+        pass
+
+
 def _has_gpu():
     try:
         import torch

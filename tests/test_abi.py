@@ -47,6 +47,20 @@ def test_library_exports_every_declared_symbol(lp):
     assert exported == _declared()
 
 
+def test_build_provenance(lp):
+    # the loaded library carries the hash of the sources beside it; a second build() of
+    # unchanged sources reuses it and says so
+    from lm_head_linear_tcgen05_gb300 import _build
+    assert lp.lp_build_id() == _build.source_hash()
+    _build.build()
+    assert _build.LAST_BUILD["compiled"] is False
+    assert _build.LAST_BUILD["source_hash"] == lp.lp_build_id()
+    info = lp.build_info()
+    assert info["build_id"] == _build.source_hash() and info["compiled_in_this_process"] is False
+    # the bounds-checked build hashes differently (its flags differ)
+    assert _build.source_hash(debug_bounds=True) != _build.source_hash()
+
+
 def test_status_strings(lp):
     for code, name in lp.STATUS_NAMES.items():
         assert lp.lp_status_string(code).startswith(name)

@@ -1,49 +1,33 @@
-"""Host logic of the multi-GPU benchmark run (replicas, weak scaling), on CPU with two
-gloo ranks: the only collective is the max of the per-rank step times, and the
-whole-job rate counts every rank's rows over the slowest rank's time."""
-import os
-import socket
+"""The benchmark's GPU arm is one-GPU only (its projection GEMMs use TMA cluster multicast,
+which this library runs on single-GPU calls only): with more than one rank, or --gpus > 1,
+it refuses before any GPU or process-group work. The reference arm (the CPU oracle) runs on
+rank 0 alone under torchrun; the other ranks exit without work. CPU only."""
+import json
 
-import pytest
-
-torch = pytest.importorskip("torch")
-import torch.distributed as dist  # noqa: E402
-import torch.multiprocessing as mp  # noqa: E402
+import bench
 
 
-def _free_port():
-    s = socket.socket()
-    s.bind(("127.0.0.1", 0))
-    port = s.getsockname()[1]
-    s.close()
-    return port
+def test_gpu_arm_refuses_more_than_one_gpu_flag(monkeypatch, capsys):
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    assert bench.main(["--gpus", "2"]) == 2
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["impl"] == "ours" and line["n_gpus"] == 2 and "one-GPU" in line["error"]
 
 
-def _worker(rank, world, port, out):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
-    import bench
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    try:
-        ms = bench.reduce_max_ms(1.0 + 0.5 * rank, dist, "cpu")
-        out[rank] = (ms, bench.whole_job_rate(4096, world, ms))
-    finally:
-        dist.destroy_process_group()
+def test_gpu_arm_refuses_torchrun_ranks(monkeypatch, capsys):
+    for rank, prints in ((0, True), (1, False)):
+        monkeypatch.setenv("WORLD_SIZE", "2")
+        monkeypatch.setenv("RANK", str(rank))
+        assert bench.main(["--gpus", "2"]) == 2
+        out = capsys.readouterr().out.strip()
+        assert bool(out) == prints          # rank 0 alone says why
+        if prints:
+            assert "one-GPU" in json.loads(out)["error"]
 
 
-def test_two_gloo_ranks_take_the_slowest_time():
-    world = 2
-    port = _free_port()
-    with mp.Manager() as m:
-        out = m.dict()
-        mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
-        res = dict(out)
-    for r in range(world):
-        ms, rate = res[r]
-        assert ms == 1.5
-        assert rate == pytest.approx(2 * 4096 / 1.5e-3)
-
-
-def test_single_rank_needs_no_collective():
-    import bench
-    assert bench.reduce_max_ms(2.5, None, "cpu") == 2.5
-    assert bench.whole_job_rate(4096, 1, 2.0) == pytest.approx(4096 / 2e-3)
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--impl", "reference", "--gpus", "2", "--steps", "1"]) == 0
+    assert capsys.readouterr().out == ""
