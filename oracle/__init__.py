@@ -37,6 +37,12 @@ Readings where the pages are silent (each one is also listed in the design notes
   mu_t)) / tau with mu_t = sum_v p_tv z_tv; dX = G W, dW = G^T X, db = sum_t G.
 * The logits-gather replay scores the replay set from reused unscaled logits
   (z_v = L[t, v] / tau) instead of x . W[v]; everything else as the replay.
+* What a shard reports for the rank-ordered reduction: its local LSE, its target
+  logit and its own entropy. A replay target inside a non-empty shard's range but
+  outside the replay set is an excluded id, whose logit is -inf (page "Perf/cuda
+  compact top p replay", Walkthrough: the keep-mask route applies -inf to excluded
+  entries); an empty shard keeps the page's target logit 0 and its LSE of -inf
+  makes the row's logp -inf when the target falls in it.
 
 Pins (tests/test_oracle.py, CPU only): closed forms (W = 0, constant bias,
 two-level logits, one dominant logit), torch.log_softmax in float64 on random
@@ -123,16 +129,17 @@ class ShardStats:
     """Local statistics of one vocabulary shard, per row.
 
     lse: log sum over the shard's real ids of exp z (-inf if the shard has none);
-    mu:  sum over those ids of softmax_local(z) * z, the local mean logit (0 if empty);
+    h:   the shard's own entropy, lse - sum over those ids of softmax_local(z) * z
+         (0 if the shard is empty);
     t:   z[y] if y lies in the shard, else 0.
     """
     lse: np.ndarray
-    mu: np.ndarray
+    h: np.ndarray
     t: np.ndarray
 
 
 def shard_stats(z: np.ndarray, y: np.ndarray, ranges, vocab_real: int) -> List[ShardStats]:
-    """Local statistics of each shard (empty shard: lse = -inf, mu = 0, t = 0)."""
+    """Local statistics of each shard (empty shard: lse = -inf, h = 0, t = 0)."""
     T = z.shape[0]
     out = []
     for vs, ve in ranges:
@@ -146,45 +153,55 @@ def shard_stats(z: np.ndarray, y: np.ndarray, ranges, vocab_real: int) -> List[S
         M = zk.max(axis=1)
         S = np.exp(zk - M[:, None]).sum(axis=1)
         lse = M + np.log(S)
-        mu = (np.exp(zk - lse[:, None]) * zk).sum(axis=1)
-        out.append(ShardStats(lse, mu, t))
+        h = lse - (np.exp(zk - lse[:, None]) * zk).sum(axis=1)
+        out.append(ShardStats(lse, h, t))
     return out
 
 
-def merge_shards(stats: List[ShardStats], y: np.ndarray, ranges):
-    """Combine per-shard statistics in ascending shard order (the rank-ordered reduction).
+def merge_shard_stats(lse: np.ndarray, t: np.ndarray, h: np.ndarray, y: np.ndarray, ranges, vocab_real: int):
+    """Combine per-shard statistics [K, T] of the shards `ranges` (ascending, the
+    rank-ordered reduction) into per-row (logp, lse, entropy).
 
-    LSE = M + log sum_k exp(lse_k - M) with M = max_k lse_k, skipping empty shards;
-    entropy = LSE - sum_k exp(lse_k - LSE) mu_k; logp = t_owner - LSE. A row whose
-    shards are all empty gets LSE = -inf, logp = -inf, entropy = 0.
+    LSE = log sum_k exp(lse_k) (an empty shard, lse_k = -inf, adds nothing);
+    entropy = -sum_v p_v log p_v = sum_k w_k (h_k + LSE - lse_k) with w_k = exp(lse_k - LSE),
+    the share of shard k in the softmax; logp = t_o - LSE where o is the shard holding y,
+    and -inf when no shard holds y, when that shard is empty (the page's empty-shard rule)
+    or when its target logit is -inf (an excluded id). A row whose shards are all empty
+    gets LSE = -inf, logp = -inf, entropy = 0.
     """
-    T = y.shape[0]
-    lse_all = np.stack([s.lse for s in stats])          # [K, T]
-    M = lse_all.max(axis=0)
-    lse = np.full(T, -np.inf)
+    lse = np.asarray(lse, dtype=np.float64)
+    t = np.asarray(t, dtype=np.float64)
+    h = np.asarray(h, dtype=np.float64)
+    y = np.asarray(y, dtype=np.int64)
+    K, T = lse.shape
+    M = lse.max(axis=0)
+    out_lse = np.full(T, -np.inf)
     ent = np.zeros(T)
     logp = np.full(T, -np.inf)
     live = np.isfinite(M)
     Ml = M[live]
     acc = np.zeros(Ml.shape)
-    for s in stats:                                      # ascending shard order
-        l = s.lse[live]
+    for k in range(K):                                   # ascending shard order
+        l = lse[k, live]
         acc += np.where(np.isfinite(l), np.exp(np.where(np.isfinite(l), l, 0.0) - Ml), 0.0)
-    lse[live] = Ml + np.log(acc)
-    mean = np.zeros(Ml.shape)
-    for s in stats:
-        l = s.lse[live]
-        w = np.where(np.isfinite(l), np.exp(np.where(np.isfinite(l), l, 0.0) - lse[live]), 0.0)
-        mean += w * s.mu[live]
-    ent[live] = lse[live] - mean
-    t = np.zeros(T)
-    found = np.zeros(T, dtype=bool)
-    for (vs, ve), s in zip(ranges, stats):
-        own = (y >= vs) & (y < ve)
-        t = np.where(own, s.t, t)
-        found |= own
-    logp[live & found] = (t - lse)[live & found]
-    return logp, lse, ent
+    out_lse[live] = Ml + np.log(acc)
+    L = out_lse[live]
+    for k in range(K):
+        l = lse[k, live]
+        fin = np.isfinite(l)
+        w = np.where(fin, np.exp(np.where(fin, l, 0.0) - L), 0.0)
+        ent[live] += w * (h[k, live] + np.where(fin, L - np.where(fin, l, 0.0), 0.0))
+    for k, (vs, ve) in enumerate(ranges):
+        own = live & (y >= vs) & (y < ve) & (y < vocab_real) & np.isfinite(lse[k])
+        logp[own] = t[k, own] - out_lse[own]
+    return logp, out_lse, ent
+
+
+def merge_shards(stats: List[ShardStats], y: np.ndarray, ranges, vocab_real: Optional[int] = None):
+    """``merge_shard_stats`` on a list of ShardStats (ascending shard order)."""
+    vr = int(ranges[-1][1]) if vocab_real is None else vocab_real
+    return merge_shard_stats(np.stack([s.lse for s in stats]), np.stack([s.t for s in stats]),
+                             np.stack([s.h for s in stats]), y, ranges, vr)
 
 
 # ------------------------------------------------------------------------- forward
@@ -247,7 +264,9 @@ def top_p_replay(X_bits, W_bits, b_bits, part, ids, y, tau: float, rows=None) ->
     For row t with set R (sorted, distinct): z_v = (x_t . W[v] + b[v]) / tau for
     v in R; LSE_R = log sum_{v in R} exp z_v; logp = z_y - LSE_R if y in R else
     -inf. Per shard k: the same over R restricted to the shard, with the empty
-    shard convention (lse -inf, t 0) when that restriction is empty.
+    shard convention (lse -inf, t 0) when that restriction is empty; a target that lies
+    in a non-empty shard's range but not in R is an excluded id, whose logit the
+    keep-mask route sets to -inf, so that shard's t is -inf.
     """
     rows = np.arange(np.asarray(ids).shape[0]) if rows is None else np.asarray(rows)
     K = part.n_shards
@@ -283,8 +302,8 @@ def top_p_replay(X_bits, W_bits, b_bits, part, ids, y, tau: float, rows=None) ->
             zk = zs[m]
             Mk = zk.max()
             sh_lse[k, i] = Mk + np.log(np.exp(zk - Mk).sum())
-            if vs <= yi < ve and hit.size:
-                sh_t[k, i] = zs[hit[0]]
+            if vs <= yi < ve:
+                sh_t[k, i] = zs[hit[0]] if hit.size else -np.inf
     return ReplayResult(logp, lse, sh_lse, sh_t)
 
 
@@ -322,8 +341,8 @@ def top_p_replay_from_logits(L_bits, part, ids, y, tau: float, rows=None) -> Rep
             zk = zs[m]
             Mk = zk.max()
             sh_lse[k, i] = Mk + np.log(np.exp(zk - Mk).sum())
-            if vs <= yi < ve and hit.size:
-                sh_t[k, i] = zs[hit[0]]
+            if vs <= yi < ve:
+                sh_t[k, i] = zs[hit[0]] if hit.size else -np.inf
     return ReplayResult(logp, lse, sh_lse, sh_t)
 
 

@@ -234,13 +234,69 @@ def test_merge_of_shards_equals_unsharded():
     np.testing.assert_allclose(ent, r.entropy, atol=1e-12)
     # the empty shard [100,100) and the all-padding shard [499..512) minus id 499
     assert np.all(np.isneginf(r.shards[1].lse))
-    assert np.all(r.shards[1].t == 0) and np.all(r.shards[1].mu == 0)
+    assert np.all(r.shards[1].t == 0) and np.all(r.shards[1].h == 0)
 
 
 def test_merge_all_empty_row_convention():
     st = [oracle.ShardStats(np.array([-np.inf]), np.zeros(1), np.zeros(1)) for _ in range(3)]
     logp, lse, ent = oracle.merge_shards(st, np.array([5]), ((0, 4), (4, 8), (8, 12)))
     assert np.isneginf(lse[0]) and np.isneginf(logp[0]) and ent[0] == 0.0
+
+
+def test_merged_replay_statistics_reproduce_the_replay():
+    # the replay's per-shard (lse, t) exchanged and merged give the replay's own logp and
+    # LSE, computed directly over each row's set: target found, target excluded from a
+    # non-empty shard (t = -inf), target in an empty shard (lse = -inf, t = 0)
+    part = synth.ranges_partition(60, 64, [0, 20, 40, 64])
+    inp = synth.forward_inputs(4, 16, part, tau=0.7, seed=6, w_std=0.3, bias_std=0.1)
+    ids = np.full((4, 64), -1, np.int32)
+    ids[0, :4] = [3, 25, 41, 59]
+    ids[1, :3] = [3, 25, 41]
+    ids[2, :2] = [25, 41]
+    ids[3, :2] = [1, 2]
+    y = np.array([25, 5, 7, 45], np.int32)   # found; excluded from shard 0; shard 0 empty; shard 2 empty
+    rep = oracle.top_p_replay(inp.X, inp.W, inp.bias, part, ids, y, inp.tau)
+    assert rep.shard_t[0, 1] == -np.inf and np.isfinite(rep.shard_lse[0, 1])
+    assert rep.shard_t[0, 2] == 0.0 and np.isneginf(rep.shard_lse[0, 2])
+    logp, lse, _ = oracle.merge_shard_stats(rep.shard_lse, rep.shard_t, np.zeros_like(rep.shard_t), y,
+                                            part.ranges, part.vocab_real)
+    np.testing.assert_array_equal(np.isneginf(logp), [False, True, True, True])
+    assert abs(logp[0] - rep.logp[0]) < 1e-12
+    np.testing.assert_allclose(lse, rep.lse, atol=1e-12)
+
+
+def test_shard_entropy_two_level_closed_form():
+    # inside one shard of n real ids (padding excluded), k ids at alpha and the rest at 0:
+    # h = log(k e^a + n - k) - k a e^a / (k e^a + n - k)
+    part = synth.ranges_partition(30, 32, [0, 10, 32])
+    n, k, alpha = 20, 3, 1.7                             # shard 1 holds real ids [10, 30)
+    z = np.zeros((1, 30))
+    z[0, 10:10 + k] = alpha
+    st = oracle.shard_stats(z, np.array([12]), part.ranges, 30)
+    Z = k * math.exp(alpha) + n - k
+    assert abs(st[1].h[0] - (math.log(Z) - k * alpha * math.exp(alpha) / Z)) < 1e-12
+    assert abs(st[0].h[0] - math.log(10)) < 1e-12      # uniform shard: log n
+
+
+def test_merge_of_a_subset_of_shards_is_the_subsets_own_softmax():
+    # what one tensor-parallel rank sees: the merge of its own shards only is the softmax
+    # over its ids; a target held by another rank gives logp = -inf there
+    part = synth.ranges_partition(500, 512, [0, 100, 250, 380, 512])
+    inp = synth.forward_inputs(6, 32, part, tau=0.6, seed=9, w_std=0.2, bias_std=0.2)
+    z = oracle.logits_from_bits(inp.X, inp.W, inp.bias, part, inp.tau)
+    y = inp.y.astype(np.int64)
+    y[:3] = [120, 300, 10]
+    st = oracle.shard_stats(z, y, part.ranges, part.vocab_real)
+    sub = [1, 2]                                         # this rank holds [100, 380)
+    logp, lse, ent = oracle.merge_shard_stats(np.stack([st[k].lse for k in sub]), np.stack([st[k].t for k in sub]),
+                                              np.stack([st[k].h for k in sub]), y,
+                                              [part.ranges[k] for k in sub], part.vocab_real)
+    lz, ll, le = oracle.dense_stats(z[:, 100:380], np.clip(y - 100, 0, 279))
+    np.testing.assert_allclose(lse, ll, atol=1e-12)
+    np.testing.assert_allclose(ent, le, atol=1e-12)
+    local = (y >= 100) & (y < 380)
+    np.testing.assert_allclose(logp[local], lz[local], atol=1e-12)
+    assert np.all(np.isneginf(logp[~local]))
 
 
 def test_shard_stats_match_local_closed_form():
