@@ -22,9 +22,11 @@
  *  - bf16 tensors are row-major; rows of X, W and logits must start on a
  *    16-byte boundary (pointer % 16 == 0 and row stride % 8 elements == 0).
  *  - Vocabulary ids are GLOBAL ids. A partition lists n_shards (1..LP_MAX_SHARDS)
- *    contiguous ranges in ascending order that tile [0, vocab_padded) exactly;
- *    ids in [vocab_real, vocab_padded) are padding and excluded from the softmax.
- *    A shard may be empty (vocab_start == vocab_end).
+ *    contiguous ranges in ascending order that tile [0, vocab_padded) exactly, or,
+ *    in a rank-local partition (local = 1), only this tensor-parallel rank's range
+ *    [shards[0].vocab_start, shards[n_shards-1].vocab_end); ids in
+ *    [vocab_real, vocab_padded) are padding and excluded from the softmax. A shard
+ *    may be empty (vocab_start == vocab_end).
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and never synchronises, except lp_get_device_error().
  *  - T = 0 (an empty batch) succeeds without work and without reading any tensor
@@ -102,22 +104,39 @@ typedef struct {
 
 /* Tensor-parallel vocabulary partition: the real and padded vocabulary sizes and
  * the shards in rank order (page "feat(rl-kernel): add CUDA linear logp provider
- * integration", Changes / Megatron integration). `shards` is a host array. */
+ * integration", Changes / Megatron integration: the provider is given the
+ * tensor-parallel vocabulary range, and tensor parallelism is the vocabulary
+ * reduction group). `shards` is a host array.
+ *   local = 0  the shards tile [0, vocab_padded): every id of the vocabulary is here;
+ *   local = 1  the shards tile only this rank's range [lo, hi) =
+ *              [shards[0].vocab_start, shards[n_shards-1].vocab_end) within
+ *              [0, vocab_padded). Every entry point then works on those ids alone:
+ *              LSE and entropy are over the rank's real ids; a target outside [lo, hi)
+ *              is another rank's (logp = -inf here, no error; a target outside
+ *              [0, vocab_real) is still a device error); replay ids of other ranks are
+ *              skipped; the backward takes the merged LSE and entropy and returns this
+ *              rank's share of dX. The per-shard statistics (lp_outputs.shard_stats)
+ *              are what the ranks exchange, merged by lp_merge_shard_stats.
+ * A C caller that initialises the first four members leaves local = 0. */
 typedef struct {
   int64_t vocab_real;
   int64_t vocab_padded;
   int32_t n_shards;
   const lp_shard_range* shards;
+  int32_t local;
 } lp_vocab_partition;
 
 /* Per-row outputs, fp32 device arrays of length T.
  *   logp        z[y] - LSE (or -inf: target outside the support or device error)
  *   lse         log sum over the support of exp z (-inf when the support is empty)
  *   entropy     LSE - sum p z in nats; may be NULL; must be NULL for replay
- *   shard_stats optional [n_shards][3][T]: per shard its local LSE, its local
- *               target logit (z[y] if y lies in the shard, else 0) and its local
- *               mean logit sum_{v in shard} softmax_local(z)_v z_v (0 for replay).
- *               An empty shard reports (-inf, 0, 0). */
+ *   shard_stats optional [n_shards][3][T]: what each shard contributes to the
+ *               rank-ordered reduction - its local LSE, its target logit (z[y] if y
+ *               lies in the shard, else 0) and its own entropy
+ *               -sum_{v in shard} p_v log p_v with p = softmax over the shard's ids
+ *               (0 for replay). An empty shard reports (-inf, 0, 0). In replay, a
+ *               target inside a shard that keeps other ids but not y is an excluded
+ *               id: that shard's target logit is -inf. */
 typedef struct {
   float* logp;
   float* lse;
@@ -315,6 +334,41 @@ LP_API lp_status lp_forward_noalloc(const void* X, int64_t T, int64_t H,
                                     const void* const* W, const void* const* bias,
                                     const lp_vocab_partition* part, const int32_t* y, float tau,
                                     const lp_outputs* out, lp_stream_t stream);
+
+/* The rank-ordered reduction of per-shard statistics (page "Perf/cuda compact top p
+ * replay", Summary: rank-ordered reductions, and tensor-parallel shards with no replay
+ * candidates handled without NaN). After each tensor-parallel rank has run an entry
+ * point on its own shards (a rank-local partition) with out->shard_stats, and the ranks
+ * have gathered those statistics in rank order, every rank calls this to fold them:
+ *   shard_stats  device fp32 [n_shards][3][T], the shards of `part` in ascending order,
+ *                each (local LSE, target logit, own entropy) as lp_outputs describes
+ *   part         the partition those shards form (usually the whole vocabulary)
+ *   y            device int32 [T] global target ids in [0, vocab_real)
+ *   out          logp and lse required, entropy optional, shard_stats must be NULL
+ * Per row: LSE = log sum_k exp(lse_k); entropy = sum_k w_k (h_k + LSE - lse_k) with
+ * w_k = exp(lse_k - LSE); logp = t_o - LSE for the shard o holding y, and -inf when no
+ * shard of `part` holds y, when o is empty or when t_o is -inf. A row whose shards are
+ * all empty gets LSE = -inf, logp = -inf, entropy = 0. The fold is the one every entry
+ * point applies to its own shards, so merging the statistics of K rank-local calls gives
+ * bit for bit what one call over all K shards returns (for replay statistics the
+ * entropy output is meaningless: replay reports no entropy). A target outside
+ * [0, vocab_real) records LP_ERR_TARGET_OUT_OF_RANGE. Needs no workspace. */
+LP_API lp_status lp_merge_shard_stats(const float* shard_stats, int64_t T, const lp_vocab_partition* part,
+                                      const int32_t* y, const lp_outputs* out, lp_stream_t stream);
+
+#define LP_MAX_PARTS 64  /* partial sums per lp_sum_partials call */
+
+/* out[i] = ((parts[0][i] + parts[1][i]) + parts[2][i]) + ... in exactly that order, for
+ * i < count: the rank-ordered sum of per-rank partial results, such as each rank's share
+ * of dX in the vocabulary-parallel backward (page "Perf/cuda compact top p replay",
+ * Summary: rank-ordered reductions; a sum whose order varies would not be deterministic).
+ *   parts     host array of n_parts (1..LP_MAX_PARTS) device pointers to fp32 [count],
+ *             16-byte aligned
+ *   out       device [count] fp32, or bf16 (the fp32 sum rounded once) per out_dtype,
+ *             16-byte aligned; may be parts[0] itself (fp32), must not overlap any other
+ * Needs no workspace. */
+LP_API lp_status lp_sum_partials(const float* const* parts, int32_t n_parts, int64_t count, void* out,
+                                 lp_dtype out_dtype, lp_stream_t stream);
 
 /* Synchronises `stream`, returns the first device-side error recorded on the
  * current device since the last call (LP_OK if none) and clears it. */

@@ -30,6 +30,7 @@ LIB_PATH = os.environ.get("LP_LIBRARY", _BUILT_LIB)
 LP_MAX_SHARDS = 8
 LP_REPLAY_SLOTS = 64
 LP_NOALLOC_SCRATCH_BYTES = 32 << 20
+LP_MAX_PARTS = 64
 
 LP_OK = 0
 STATUS_NAMES = {
@@ -63,7 +64,7 @@ EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward
             "lp_top_p_replay", "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward",
             "lp_backward_ex", "lp_backward_from_logits", "lp_get_device_error", "lp_selftest_wait_timeout",
             "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported", "lp_status_string",
-            "lp_build_id")
+            "lp_build_id", "lp_merge_shard_stats", "lp_sum_partials")
 
 
 class LPError(RuntimeError):
@@ -77,10 +78,12 @@ class LPError(RuntimeError):
 @dataclass(frozen=True)
 class VocabPartition:
     """Tensor-parallel vocabulary partition: contiguous ascending global-id ranges
-    covering [0, vocab_padded); ids >= vocab_real are padding."""
+    covering [0, vocab_padded), or, with local=True, only one rank's range
+    [ranges[0][0], ranges[-1][1]); ids >= vocab_real are padding."""
     vocab_real: int
     vocab_padded: int
     ranges: Tuple[Tuple[int, int], ...]
+    local: bool = False
 
     @property
     def n_shards(self) -> int:
@@ -93,7 +96,7 @@ class _ShardRange(ctypes.Structure):
 
 class _Partition(ctypes.Structure):
     _fields_ = [("vocab_real", ctypes.c_int64), ("vocab_padded", ctypes.c_int64),
-                ("n_shards", ctypes.c_int32), ("shards", ctypes.POINTER(_ShardRange))]
+                ("n_shards", ctypes.c_int32), ("shards", ctypes.POINTER(_ShardRange)), ("local", ctypes.c_int32)]
 
 
 class _Outputs(ctypes.Structure):
@@ -147,6 +150,8 @@ def lib() -> ctypes.CDLL:
     L.lp_backward_from_logits.argtypes = [P(vp), P(i64), i64, P(_Partition), vp, f32, vp, vp, vp, vp, P(vp),
                                           P(i64), ctypes.c_int, vp]
     L.lp_forward_host.argtypes = [vp, i64, i64, P(vp), P(vp), P(_Partition), vp, f32, P(_Outputs), vp, sz, vp]
+    L.lp_merge_shard_stats.argtypes = [vp, i64, P(_Partition), vp, P(_Outputs), vp]
+    L.lp_sum_partials.argtypes = [P(vp), i32, i64, vp, ctypes.c_int, vp]
     L.lp_get_device_error.argtypes = [vp]
     L.lp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     L.lp_selftest_bounds.argtypes = [vp]
@@ -157,7 +162,8 @@ def lib() -> ctypes.CDLL:
     for name in ("lp_forward", "lp_forward_noalloc", "lp_forward_from_logits", "lp_top_p_replay",
                  "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask",
                  "lp_backward", "lp_backward_ex", "lp_backward_from_logits", "lp_forward_host", "lp_get_device_error",
-                 "lp_selftest_wait_timeout", "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported"):
+                 "lp_selftest_wait_timeout", "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported",
+                 "lp_merge_shard_stats", "lp_sum_partials"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -177,7 +183,8 @@ def use_library(path: str) -> ctypes.CDLL:
 def _c_partition(part) -> Tuple[_Partition, object]:
     n = len(part.ranges)
     arr = (_ShardRange * max(n, 1))(*[_ShardRange(int(s), int(e)) for s, e in part.ranges])
-    cp = _Partition(int(part.vocab_real), int(part.vocab_padded), n, ctypes.cast(arr, ctypes.POINTER(_ShardRange)))
+    cp = _Partition(int(part.vocab_real), int(part.vocab_padded), n, ctypes.cast(arr, ctypes.POINTER(_ShardRange)),
+                    1 if getattr(part, "local", False) else 0)
     return cp, arr
 
 
@@ -293,6 +300,11 @@ def _outputs(T: int, n_shards: int, device, entropy: bool, shard_stats: bool, ou
             _shape(o["shard_stats"], "out['shard_stats']", (n_shards, 3, T))
     co = _Outputs(_ptr(o["logp"]), _ptr(o["lse"]), _ptr(o["entropy"]), _ptr(o["shard_stats"]))
     return o, co
+
+
+def _same_device(a: torch.Tensor, b: torch.Tensor):
+    if a.device != b.device:
+        raise ValueError(f"tensors on different devices ({a.device}, {b.device})")
 
 
 def _shape(t: Optional[torch.Tensor], name: str, shape: tuple):
@@ -665,3 +677,49 @@ def lp_forward_host(hX: torch.Tensor, W: Sequence[torch.Tensor], bias, part, hy:
         stream.synchronize()
     return {k: out.get(k) for k in ("logp", "lse", "entropy", "shard_stats")}
 
+
+def lp_merge_shard_stats(shard_stats: torch.Tensor, y: torch.Tensor, part, entropy: bool = True,
+                         out: Optional[dict] = None) -> dict:
+    """Rank-ordered reduction of per-shard statistics: shard_stats fp32 [n_shards, 3, T]
+    (the shards of ``part`` in ascending order, e.g. gathered from the ranks of a
+    vocabulary-parallel group), y int32 [T]. Returns fp32 logp, lse and entropy [T]."""
+    _check(shard_stats, "shard_stats", torch.float32, 3)
+    _check(y, "y", torch.int32, 1)
+    n = len(part.ranges)
+    T = y.shape[0]
+    _shape(shard_stats, "shard_stats", (n, 3, T))
+    _same_device(shard_stats, y)
+    cp, _keep = _c_partition(part)
+    with torch.cuda.device(y.device):
+        o, co = _outputs(T, n, y.device, entropy, False, out)
+        if o["shard_stats"] is not None:
+            raise ValueError("out must not hold shard_stats")
+        st = lib().lp_merge_shard_stats(shard_stats.data_ptr(), T, ctypes.byref(cp), y.data_ptr(), ctypes.byref(co),
+                                        _stream(y.device))
+    _raise(st, "lp_merge_shard_stats")
+    return o
+
+
+def lp_sum_partials(parts: Sequence[torch.Tensor], out_dtype=torch.float32,
+                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """((parts[0] + parts[1]) + parts[2]) + ... elementwise, in exactly that order: the
+    rank-ordered sum of per-rank partial results (fp32 tensors of one shape). The sum is
+    returned as fp32, or rounded once to bf16."""
+    if len(parts) < 1 or len(parts) > LP_MAX_PARTS:
+        raise ValueError(f"between 1 and {LP_MAX_PARTS} parts")
+    shape = tuple(parts[0].shape)
+    for i, t in enumerate(parts):
+        _check(t, f"parts[{i}]", torch.float32, len(shape))
+        _shape(t, f"parts[{i}]", shape)
+        _same_device(parts[0], t)
+    if out_dtype not in _LP_DTYPES:
+        raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+    if out is None:
+        out = torch.empty(shape, dtype=out_dtype, device=parts[0].device)
+    _check(out, "out", out_dtype, len(shape))
+    _shape(out, "out", shape)
+    with torch.cuda.device(parts[0].device):
+        st = lib().lp_sum_partials(_ptr_array(list(parts)), len(parts), parts[0].numel(), out.data_ptr(),
+                                   _LP_DTYPES[out_dtype], _stream(parts[0].device))
+    _raise(st, "lp_sum_partials")
+    return out

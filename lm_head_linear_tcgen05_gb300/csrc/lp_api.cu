@@ -124,13 +124,20 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+// A partition is valid when its shards are contiguous and ascending and tile
+// [0, vocab_padded) (local = 0) or a range [lo, hi) inside it (local = 1, one
+// tensor-parallel rank's ids). The kernels need no mode of their own: an id outside the
+// shards is simply not here (another rank's target or replay id).
 lp_status check_partition(const lp_vocab_partition* part, Shards* sh) {
   if (part == nullptr || part->shards == nullptr) return LP_ERR_INVALID_ARG;
   const int n = part->n_shards;
   if (n < 1 || n > LP_MAX_SHARDS) return LP_ERR_INVALID_ARG;
   if (part->vocab_real < 1 || part->vocab_real > part->vocab_padded || part->vocab_padded > INT32_MAX)
     return LP_ERR_INVALID_ARG;
-  int64_t expect = 0;
+  if (part->local != 0 && part->local != 1) return LP_ERR_INVALID_ARG;
+  const bool local = part->local == 1;
+  int64_t expect = local ? part->shards[0].vocab_start : 0;
+  if (expect < 0) return LP_ERR_INVALID_ARG;
   for (int k = 0; k < n; ++k) {
     const int64_t s = part->shards[k].vocab_start, e = part->shards[k].vocab_end;
     if (s != expect || e < s) return LP_ERR_INVALID_ARG;
@@ -141,7 +148,7 @@ lp_status check_partition(const lp_vocab_partition* part, Shards* sh) {
     const int64_t r = (e < part->vocab_real ? e : part->vocab_real) - s;
     sh->real[k] = r > 0 ? r : 0;
   }
-  if (expect != part->vocab_padded) return LP_ERR_INVALID_ARG;
+  if (local ? expect > part->vocab_padded : expect != part->vocab_padded) return LP_ERR_INVALID_ARG;
   sh->n = n;
   sh->vocab_real = part->vocab_real;
   sh->vocab_padded = part->vocab_padded;
@@ -712,6 +719,66 @@ lp_status lp_backward_from_logits(const void* const* logits, const int64_t* ld, 
   p.scale_log2 = float(1.4426950408889634 / double(tau));
   p.inv_tau = float(1.0 / double(tau));
   if (launch_logits_backward(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
+}
+
+lp_status lp_merge_shard_stats(const float* shard_stats, int64_t T, const lp_vocab_partition* part,
+                               const int32_t* y, const lp_outputs* out, lp_stream_t stream) {
+  Shards sh;
+  if (check_partition(part, &sh) != LP_OK) return LP_ERR_INVALID_ARG;
+  if (!valid_rows(T)) return LP_ERR_INVALID_ARG;
+  if (T == 0) return LP_OK;
+  if (shard_stats == nullptr || y == nullptr || out == nullptr || out->logp == nullptr || out->lse == nullptr ||
+      out->shard_stats != nullptr)
+    return LP_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+  MergeStatsParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.stats = shard_stats;
+  p.y = y;
+  p.logp = out->logp;
+  p.lse = out->lse;
+  p.entropy = out->entropy;
+  p.err = dev->err;
+  p.vocab_real = sh.vocab_real;
+  for (int k = 0; k < sh.n; ++k) {
+    p.shard_start[k] = sh.start[k];
+    p.shard_end[k] = sh.end[k];
+  }
+  p.n_shards = sh.n;
+  p.T = int32_t(T);
+  if (launch_merge_stats(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
+  return LP_OK;
+}
+
+lp_status lp_sum_partials(const float* const* parts, int32_t n_parts, int64_t count, void* out, lp_dtype out_dtype,
+                          lp_stream_t stream) {
+  if (n_parts < 1 || n_parts > LP_MAX_PARTS || count < 0 || parts == nullptr) return LP_ERR_INVALID_ARG;
+  if (out_dtype != LP_DTYPE_F32 && out_dtype != LP_DTYPE_BF16) return LP_ERR_INVALID_ARG;
+  if (count == 0) return LP_OK;
+  if (out == nullptr) return LP_ERR_INVALID_ARG;
+  const int64_t esz = out_dtype == LP_DTYPE_BF16 ? 2 : 4;
+  const Span o = row_span(out, 1, count, count, esz);
+  for (int i = 0; i < n_parts; ++i) {
+    if (parts[i] == nullptr) return LP_ERR_INVALID_ARG;
+    if (!aligned16(parts[i])) return LP_ERR_ALIGNMENT;
+    const bool in_place = i == 0 && parts[0] == out && out_dtype == LP_DTYPE_F32;
+    if (!in_place && overlap(o, row_span(parts[i], 1, count, count, 4))) return LP_ERR_INVALID_ARG;
+  }
+  if (!aligned16(out)) return LP_ERR_ALIGNMENT;
+  DeviceState* dev = nullptr;
+  lp_status st = device_state(&dev);
+  if (st != LP_OK) return st;
+  SumPartsParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int i = 0; i < n_parts; ++i) p.parts[i] = parts[i];
+  p.out = out;
+  p.count = count;
+  p.n_parts = n_parts;
+  p.out_bf16 = out_dtype == LP_DTYPE_BF16 ? 1 : 0;
+  if (launch_sum_partials(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LP_ERR_CUDA;
   return LP_OK;
 }
 

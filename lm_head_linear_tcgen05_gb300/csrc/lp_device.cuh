@@ -7,8 +7,8 @@
 //  * the per-row statistics fold used by every path. Statistics are kept in base-2
 //    units of the scaled logit, u = z * log2(e), z = (x.w + b) / tau:
 //        m = max u,  s = sum 2^(u - m),  a = sum 2^(u - m) (u - m)
-//    so that LSE = ln2 (m + log2 s), entropy = ln2 (log2 s - a / s) and the local
-//    mean logit sum p z = ln2 (m + a / s). An empty set is (m, s, a) = (-inf, 0, 0)
+//    so that LSE = ln2 (m + log2 s) and entropy = ln2 (log2 s - a / s). An empty set
+//    is (m, s, a) = (-inf, 0, 0)
 //    and is skipped by every merge, so no -inf - -inf is ever formed (the
 //    empty-shard rule of page "Perf/cuda compact top p replay", Walkthrough).
 #pragma once
@@ -347,10 +347,53 @@ __device__ __forceinline__ float stat_entropy(const Stat& A) {
   return __fmul_rn(kLn2, __fsub_rn(log2f(A.s), __fdiv_rn(A.a, A.s)));
 }
 
-// Mean logit sum p z in nats (0 for the empty set).
-__device__ __forceinline__ float stat_mean(const Stat& A) {
-  if (A.m == -INFINITY) return 0.f;
-  return __fmul_rn(kLn2, __fadd_rn(A.m, __fdiv_rn(A.a, A.s)));
+// ------------------------------------------------- rank-ordered shard reduction
+// What a vocabulary shard reports for the rank-ordered reduction (page "Perf/cuda
+// compact top p replay", Summary), in nats: its local LSE (-inf when it holds no id of
+// the support), its own entropy h (0 when empty) and its target logit t. The merged row
+// follows from these alone:
+//     LSE     = M + ln sum_k e^(lse_k - M),             M = max_k lse_k
+//     entropy = sum_k w_k (h_k + LSE - lse_k),          w_k = e^(lse_k - LSE)
+//     logp    = t_o - LSE, o the shard holding y; -inf when no shard holds y or o is
+//               empty (the empty-shard rule), and -inf when t_o is (an excluded id).
+// Every path folds its shards through row_finish, and lp_merge_shard_stats folds
+// statistics exchanged between ranks through it as well, so one call over K shards and
+// K rank-local calls merged afterwards give the same bits. With a single shard the
+// result is that shard's own (LSE, h) exactly.
+
+struct RowOut {
+  float logp, lse, entropy;
+};
+
+// e^d for d <= 0; exactly 1 at d = 0
+__device__ __forceinline__ float nat_exp(float d) { return d == 0.f ? 1.f : hw_ex2(__fmul_rn(d, kLog2e)); }
+
+// lse, h, t: [n] per-shard statistics in ascending shard order (n <= LP_MAX_SHARDS);
+// owner: index of the shard holding the row's target, or -1.
+__device__ __forceinline__ RowOut row_finish(const float* lse, const float* h, const float* t, int n, int owner) {
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < LP_MAX_SHARDS; ++k)
+    if (k < n) M = fmaxf(M, lse[k]);
+  if (M == -INFINITY) return RowOut{-INFINITY, -INFINITY, 0.f};
+  float S = 0.f;
+#pragma unroll
+  for (int k = 0; k < LP_MAX_SHARDS; ++k)
+    if (k < n && lse[k] != -INFINITY) S = __fadd_rn(S, nat_exp(__fsub_rn(lse[k], M)));
+  const float L = S == 1.f ? M : __fadd_rn(M, __fmul_rn(kLn2, log2f(S)));
+  float E = 0.f;
+#pragma unroll
+  for (int k = 0; k < LP_MAX_SHARDS; ++k) {
+    if (k < n && lse[k] != -INFINITY) {
+      const float gap = __fsub_rn(L, lse[k]);
+      E = __fmaf_rn(nat_exp(-gap), __fadd_rn(h[k], gap), E);
+    }
+  }
+  float lp = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < LP_MAX_SHARDS; ++k)
+    if (k == owner && lse[k] != -INFINITY) lp = __fsub_rn(t[k], L);
+  return RowOut{lp, L, E};
 }
 
 }  // namespace lp

@@ -207,9 +207,10 @@ struct LogpEpi : GemmEpiBase {
 // and g = tid / 8 folds, for row r, the blocks nb = g, g + 32, ... of each shard in
 // ascending order, so every load instruction of a warp reads whole 32-byte sectors (4
 // groups x 8 adjacent rows). The 32 partials of a row are then combined in a fixed order:
-// a shuffle tree over the warp's 4 groups, then the 8 warps in ascending order; shards are
-// folded in ascending order (the rank-ordered reduction of page "Perf/cuda compact top p
-// replay", Summary). The order depends only on the vocabulary layout, never on T.
+// a shuffle tree over the warp's 4 groups, then the 8 warps in ascending order, giving
+// the shard's own (LSE, entropy); the shards are then reduced in ascending order by
+// row_finish (the rank-ordered reduction of page "Perf/cuda compact top p replay",
+// Summary). The order depends only on the vocabulary layout, never on T.
 constexpr int kMergeRows = 8;
 constexpr int kMergeThreads = 256;
 constexpr int kMergeGroups = kMergeThreads / kMergeRows;  // 32
@@ -218,6 +219,8 @@ constexpr int kMergeBatch = 8;                            // blocks per thread l
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeParams p) {
   __shared__ Stat part[kMergeWarps][kMergeRows];
+  __shared__ float sh_lse[LP_MAX_SHARDS][kMergeRows];
+  __shared__ float sh_h[LP_MAX_SHARDS][kMergeRows];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -226,7 +229,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   const int row = int(blockIdx.x) * kMergeRows + r;
   const bool in_rows = row < p.T;
   const size_t T = size_t(p.T);
-  Stat tot = stat_empty();  // meaningful in threads tid < kMergeRows
   for (int k = 0; k < p.n_shards; ++k) {
     Stat loc = stat_empty();
     if (in_rows) {
@@ -256,29 +258,44 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     }
     if (lane < kMergeRows) part[warp][lane] = loc;
     __syncthreads();
-    if (tid < kMergeRows && in_rows) {
+    if (tid < kMergeRows) {
       Stat sh = part[0][tid];
       for (int w = 1; w < kMergeWarps; ++w) stat_merge(sh, part[w][tid]);
-      if (p.shard_stats != nullptr) {
-        const int yv = __ldg(p.y + row);
-        const bool own = yv >= 0 && int64_t(yv) < p.vocab_real && yv >= p.shard_start[k] && yv < p.shard_end[k];
-        float* ss = p.shard_stats + size_t(k) * 3 * T;
-        ss[row] = stat_lse(sh);
-        ss[T + row] = own ? p.ws_t[row] : 0.f;
-        ss[2 * T + row] = stat_mean(sh);
-      }
-      stat_merge(tot, sh);
+      sh_lse[k][tid] = stat_lse(sh);
+      sh_h[k][tid] = stat_entropy(sh);
     }
     __syncthreads();  // part is rewritten for the next shard
   }
   if (tid < kMergeRows && in_rows) {
     const int yv = __ldg(p.y + row);
     const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
-    const float lse = stat_lse(tot);
-    p.lse[row] = lse;
-    if (p.entropy != nullptr) p.entropy[row] = stat_entropy(tot);
+    int owner = -1;  // the shard holding y (none: y belongs to another rank's range)
+    for (int k = 0; k < p.n_shards; ++k)
+      if (y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k]) owner = k;
+    const float tv = owner >= 0 ? p.ws_t[row] : 0.f;
+    float lse[LP_MAX_SHARDS], h[LP_MAX_SHARDS], t[LP_MAX_SHARDS];
+#pragma unroll
+    for (int k = 0; k < LP_MAX_SHARDS; ++k) {
+      lse[k] = k < p.n_shards ? sh_lse[k][tid] : -INFINITY;
+      h[k] = k < p.n_shards ? sh_h[k][tid] : 0.f;
+      t[k] = k == owner ? tv : 0.f;
+    }
+    if (p.shard_stats != nullptr) {
+#pragma unroll
+      for (int k = 0; k < LP_MAX_SHARDS; ++k) {
+        if (k < p.n_shards) {
+          float* ss = p.shard_stats + size_t(k) * 3 * T;
+          ss[row] = lse[k];
+          ss[T + row] = t[k];
+          ss[2 * T + row] = h[k];
+        }
+      }
+    }
+    const RowOut o = row_finish(lse, h, t, p.n_shards, owner);
+    p.lse[row] = o.lse;
+    if (p.entropy != nullptr) p.entropy[row] = o.entropy;
     if (!y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
-    p.logp[row] = (y_ok && tot.m != -INFINITY) ? __fsub_rn(p.ws_t[row], lse) : -INFINITY;
+    p.logp[row] = o.logp;
   }
 }
 

@@ -173,6 +173,30 @@ struct MaskParams {
   int32_t T;
 };
 
+// Rank-ordered reduction of exchanged per-shard statistics, one thread per row.
+struct MergeStatsParams {
+  const float* stats;                   // [n_shards][3][T]: lse, t, h
+  const int32_t* y;
+  float* logp;
+  float* lse;
+  float* entropy;                       // or NULL
+  unsigned int* err;
+  int64_t vocab_real;
+  int64_t shard_start[LP_MAX_SHARDS];
+  int64_t shard_end[LP_MAX_SHARDS];
+  int32_t n_shards;
+  int32_t T;
+};
+
+// Ordered elementwise sum of partial results.
+struct SumPartsParams {
+  const float* parts[LP_MAX_PARTS];
+  void* out;
+  int64_t count;
+  int32_t n_parts;
+  int32_t out_bf16;
+};
+
 // Backward: everything lp_backward validated, handed to the backward translation unit.
 struct BackwardArgs {
   const void* X;
@@ -211,5 +235,7 @@ cudaError_t launch_replay(const ReplayParams& p, cudaStream_t s);
 cudaError_t launch_replay_from_logits(const ReplayParams& p, cudaStream_t s);
 cudaError_t launch_mask_compact(const MaskParams& p, cudaStream_t s);
 cudaError_t launch_logits_backward(const LogitsGradParams& p, cudaStream_t s);
+cudaError_t launch_merge_stats(const MergeStatsParams& p, cudaStream_t s);
+cudaError_t launch_sum_partials(const SumPartsParams& p, cudaStream_t s);
 
 }  // namespace lp

@@ -16,9 +16,9 @@
 //   3. each warp scores ids i = warp, warp+8, ...: a canonical fp32 dot product
 //      (lane l accumulates 16-byte vectors l, l+32, ... in order, then a fixed
 //      shuffle tree) of x with the gathered row W[id] - a gather GEMV;
-//   4. warp 0 folds the scores shard by shard - each lane the two adjacent ids it holds,
-//      then a fixed shuffle tree - and lane 0 merges the shards in ascending order. The
-//      order depends only on the row's id set.
+//   4. warp 0 folds the scores shard by shard - each lane two adjacent ids of the shard's
+//      run of the ascending list, then a fixed shuffle tree - and the shards are reduced
+//      in ascending order. The order depends only on each shard's own ids.
 // The dense keep-mask route compacts each mask row into the same canonical slots
 // and runs this very kernel, so both routes produce identical bits for equal sets.
 // The logits-gather variant (reused unscaled logits instead of x . W) replaces step 3
@@ -137,17 +137,20 @@ __global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_k
   const size_t T = size_t(p.T);
   const int nvec = p.H >> 3;
 
-  // 1. validate, sort ascending, deduplicate (warp 0): unused and invalid slots become the
-  // key 0xFFFFFFFF, above every id; after the sort a key is kept if it differs from its
-  // predecessor, and its rank is the number of kept keys before it
+  // 1. validate, sort ascending, deduplicate (warp 0): unused and invalid slots, and valid
+  // ids outside this call's range [lo, hi) (another rank's ids in a rank-local partition),
+  // become the key 0xFFFFFFFF, above every id; after the sort a key is kept if it differs
+  // from its predecessor, and its rank is the number of kept keys before it
   if (warp == 0) {
     const int32_t* ids = p.ids + size_t(row) * LP_REPLAY_SLOTS;
     const int32_t v0 = __ldg(ids + 2 * lane), v1 = __ldg(ids + 2 * lane + 1);
     const bool bad0 = v0 != -1 && (v0 < 0 || int64_t(v0) >= p.vocab_real);
     const bool bad1 = v1 != -1 && (v1 < 0 || int64_t(v1) >= p.vocab_real);
     const unsigned any_bad = __ballot_sync(0xffffffffu, bad0 || bad1);
-    uint32_t k0 = (bad0 || v0 < 0) ? 0xFFFFFFFFu : uint32_t(v0);
-    uint32_t k1 = (bad1 || v1 < 0) ? 0xFFFFFFFFu : uint32_t(v1);
+    const int64_t lo = p.shard_start[0], hi = p.shard_end[p.n_shards - 1];
+    const bool here0 = int64_t(v0) >= lo && int64_t(v0) < hi, here1 = int64_t(v1) >= lo && int64_t(v1) < hi;
+    uint32_t k0 = (bad0 || v0 < 0 || !here0) ? 0xFFFFFFFFu : uint32_t(v0);
+    uint32_t k1 = (bad1 || v1 < 0 || !here1) ? 0xFFFFFFFFu : uint32_t(v1);
     warp_sort64(k0, k1, lane);
     const uint32_t prev0 = __shfl_up_sync(0xffffffffu, k1, 1);
     const bool keep0 = k0 != 0xFFFFFFFFu && (lane == 0 || k0 != prev0);
@@ -202,51 +205,71 @@ __global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_k
   }
   __syncthreads();
 
-  // 4. fold (warp 0): lane l takes ids 2l and 2l + 1 (ascending) of each shard, the lanes'
-  // statistics combine by a fixed shuffle tree, and lane 0 merges the shards in ascending
-  // order - an order fixed by the row's id set alone
+  // 4. fold (warp 0), shard by shard: the shard's ids are a contiguous run [i0, i1) of the
+  // ascending list; lane l takes its ids i0 + 2l and i0 + 2l + 1, the lanes' statistics
+  // combine by a fixed shuffle tree, and the shards are reduced in ascending order by
+  // row_finish - an order fixed by the shard's own ids alone, so a rank-local call that
+  // holds only some of the shards folds each of them exactly as a call holding all does
   if (warp == 0) {
     const int yv = __ldg(p.y + row);
     const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
     if (lane == 0 && !y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
-    const int i0 = 2 * lane, i1 = 2 * lane + 1;
-    const bool h0 = i0 < n, h1 = i1 < n;
-    const int64_t id0 = h0 ? int64_t(uniq[i0]) : -1, id1 = h1 ? int64_t(uniq[i1]) : -1;
-    const float z0 = h0 ? zs[i0] : 0.f, z1 = h1 ? zs[i1] : 0.f;
+    const int64_t id0 = 2 * lane < n ? int64_t(uniq[2 * lane]) : INT64_MAX;
+    const int64_t id1 = 2 * lane + 1 < n ? int64_t(uniq[2 * lane + 1]) : INT64_MAX;
+    // the target logit, if y is in the set: the lane holding it says which of its two ids
     const bool own0 = y_ok && id0 == yv, own1 = y_ok && id1 == yv;
     const unsigned tb = __ballot_sync(0xffffffffu, own0 || own1);
     const bool t_found = tb != 0u;
-    const float t_val = __shfl_sync(0xffffffffu, own1 ? z1 : z0, t_found ? __ffs(tb) - 1 : 0);
-    Stat tot = stat_empty();
-    for (int k = 0; k < p.n_shards; ++k) {
-      const bool in0 = h0 && id0 >= p.shard_start[k] && id0 < p.shard_end[k];
-      const bool in1 = h1 && id1 >= p.shard_start[k] && id1 < p.shard_end[k];
-      Stat loc = stat_empty();
-      if (__ballot_sync(0xffffffffu, in0 || in1) != 0u) {
-        if (in0) stat_push(loc, __fmul_rn(z0, kLog2e));
-        if (in1) stat_push(loc, __fmul_rn(z1, kLog2e));
+    const int src = t_found ? __ffs(tb) - 1 : 0;
+    const int t_idx = 2 * src + __shfl_sync(0xffffffffu, own0 ? 0 : 1, src);
+    const float t_val = t_found ? zs[t_idx] : 0.f;
+    int owner = -1;
+    float lse[LP_MAX_SHARDS], hz[LP_MAX_SHARDS], t[LP_MAX_SHARDS];
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          const Stat o{__shfl_down_sync(0xffffffffu, loc.m, off), __shfl_down_sync(0xffffffffu, loc.s, off),
-                       __shfl_down_sync(0xffffffffu, loc.a, off)};
-          if (lane < off) stat_merge(loc, o);
+    for (int k = 0; k < LP_MAX_SHARDS; ++k) {
+      lse[k] = -INFINITY;
+      hz[k] = 0.f;
+      t[k] = 0.f;
+      if (k < p.n_shards) {
+        const int64_t s0 = p.shard_start[k], s1 = p.shard_end[k];
+        const int i0 = __popc(__ballot_sync(0xffffffffu, id0 < s0)) + __popc(__ballot_sync(0xffffffffu, id1 < s0));
+        const int i1 = __popc(__ballot_sync(0xffffffffu, id0 < s1)) + __popc(__ballot_sync(0xffffffffu, id1 < s1));
+        Stat loc = stat_empty();
+        if (i1 > i0) {
+          const int j0 = i0 + 2 * lane, j1 = j0 + 1;
+          if (j0 < i1) stat_push(loc, __fmul_rn(zs[j0], kLog2e));
+          if (j1 < i1) stat_push(loc, __fmul_rn(zs[j1], kLog2e));
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            const Stat o{__shfl_down_sync(0xffffffffu, loc.m, off), __shfl_down_sync(0xffffffffu, loc.s, off),
+                         __shfl_down_sync(0xffffffffu, loc.a, off)};
+            if (lane < off) stat_merge(loc, o);
+          }
         }
-      }
-      if (lane == 0) {
-        const bool own_k = t_found && yv >= p.shard_start[k] && yv < p.shard_end[k];
-        if (p.shard_stats != nullptr) {
-          float* ss = p.shard_stats + size_t(k) * 3 * T;
-          ss[row] = stat_lse(loc);
-          ss[T + row] = own_k ? t_val : 0.f;
-          ss[2 * T + row] = 0.f;
+        lse[k] = stat_lse(loc);
+        if (y_ok && yv >= s0 && yv < s1) {
+          owner = k;
+          // the target's logit over the support: z_y if kept, -inf if the shard keeps
+          // other ids but not y (an excluded id), 0 if the shard keeps none (empty shard)
+          t[k] = t_found ? t_val : (i1 > i0 ? -INFINITY : 0.f);
         }
-        stat_merge(tot, loc);
       }
     }
     if (lane == 0) {
-      const float lse = stat_lse(tot);
-      p.lse[row] = bad_row ? -INFINITY : lse;
-      p.logp[row] = (!bad_row && y_ok && t_found) ? __fsub_rn(t_val, lse) : -INFINITY;
+      if (p.shard_stats != nullptr) {
+#pragma unroll
+        for (int k = 0; k < LP_MAX_SHARDS; ++k) {
+          if (k < p.n_shards) {
+            float* ss = p.shard_stats + size_t(k) * 3 * T;
+            ss[row] = bad_row ? -INFINITY : lse[k];
+            ss[T + row] = bad_row ? 0.f : t[k];
+            ss[2 * T + row] = 0.f;
+          }
+        }
+      }
+      const RowOut o = row_finish(lse, hz, t, p.n_shards, owner);
+      p.lse[row] = bad_row ? -INFINITY : o.lse;
+      p.logp[row] = bad_row ? -INFINITY : o.logp;
     }
   }
 }

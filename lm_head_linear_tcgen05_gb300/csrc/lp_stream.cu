@@ -16,9 +16,10 @@
 // 2^d flushes to 0 there exactly as it would for the original logit, and a -inf logit
 // (an entry the caller masked out) never forms 0 * inf. The threads of a shard are
 // combined by a fixed shuffle tree per warp; the per-warp results of every shard wait in
-// shared memory until the row is done, and thread 0 then merges warp after warp and
-// shard after shard in ascending order. The work split depends only on the shard width,
-// so a row's result never depends on T. No thread waits on another while streaming.
+// shared memory until the row is done, and thread 0 then merges warp after warp into each
+// shard's own (LSE, entropy) and reduces the shards in ascending order (row_finish). The
+// work split depends only on the shard width, so a row's result never depends on T. No
+// thread waits on another while streaming.
 #include <cuda_bf16.h>
 
 #include "lp_device.cuh"
@@ -188,31 +189,40 @@ __global__ void __launch_bounds__(kStreamThreads, LP_STREAM_MIN_BLOCKS) stream_l
   }
   __syncthreads();
   if (tid != 0) return;
-  Stat tot = stat_empty();
-  float t_val = 0.f;
-  for (int k = 0; k < p.n_shards; ++k) {
-    Stat sh = red[k][0];
-    for (int w = 1; w < kStreamWarps; ++w) stat_merge(sh, red[k][w]);
-    const bool own = y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k];
-    float tk = 0.f;
-    if (own && in_bounds(yv - p.shard_start[k] < p.shard_width[k], p.err)) {
-      const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
-      tk = __fmul_rn(__bfloat162float(L[yv - p.shard_start[k]]), p.inv_tau);
-      t_val = tk;
+  // shard by shard: the warps' statistics merged in ascending order, then the shards
+  // reduced in ascending order by row_finish
+  int owner = -1;  // the shard holding y (none: y belongs to another rank's range)
+  float lse[LP_MAX_SHARDS], h[LP_MAX_SHARDS], t[LP_MAX_SHARDS];
+#pragma unroll
+  for (int k = 0; k < LP_MAX_SHARDS; ++k) {
+    lse[k] = -INFINITY;
+    h[k] = 0.f;
+    t[k] = 0.f;
+    if (k < p.n_shards) {
+      Stat sh = red[k][0];
+      for (int w = 1; w < kStreamWarps; ++w) stat_merge(sh, red[k][w]);
+      lse[k] = stat_lse(sh);
+      h[k] = stat_entropy(sh);
+      if (y_ok && yv >= p.shard_start[k] && yv < p.shard_end[k]) {
+        owner = k;
+        if (in_bounds(yv - p.shard_start[k] < p.shard_width[k], p.err)) {
+          const __nv_bfloat16* L = p.logits[k] + size_t(row) * size_t(p.ld[k]);
+          t[k] = __fmul_rn(__bfloat162float(L[yv - p.shard_start[k]]), p.inv_tau);
+        }
+      }
+      if (p.shard_stats != nullptr) {
+        float* ss = p.shard_stats + size_t(k) * 3 * T;
+        ss[row] = lse[k];
+        ss[T + row] = t[k];
+        ss[2 * T + row] = h[k];
+      }
     }
-    if (p.shard_stats != nullptr) {
-      float* ss = p.shard_stats + size_t(k) * 3 * T;
-      ss[row] = stat_lse(sh);
-      ss[T + row] = tk;
-      ss[2 * T + row] = stat_mean(sh);
-    }
-    stat_merge(tot, sh);
   }
-  const float lse = stat_lse(tot);
-  p.lse[row] = lse;
-  if (p.entropy != nullptr) p.entropy[row] = stat_entropy(tot);
+  const RowOut o = row_finish(lse, h, t, p.n_shards, owner);
+  p.lse[row] = o.lse;
+  if (p.entropy != nullptr) p.entropy[row] = o.entropy;
   if (!y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
-  p.logp[row] = (y_ok && tot.m != -INFINITY) ? __fsub_rn(t_val, lse) : -INFINITY;
+  p.logp[row] = o.logp;
 }
 
 cudaError_t launch_stream_logits(const StreamParams& p, cudaStream_t s) {

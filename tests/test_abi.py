@@ -248,3 +248,65 @@ def test_forward_host_validation(lp):
     assert call(ws=A + 8) == 2
     assert call(T=0, X=None, y=None, logp=None, lse=None, ws=None, wsb=0) == 0
     assert call() == 3                       # valid: fails only for want of a GPU, before any copy
+
+
+def _local(lp, real, padded, bounds):
+    return lp.VocabPartition(real, padded, tuple((bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1)),
+                             local=True)
+
+
+def test_rank_local_partitions_validate(lp):
+    # a rank-local partition tiles one rank's range [lo, hi) inside [0, vocab_padded)
+    ok = _local(lp, 151936, 152064, [38016, 76032])
+    nb = 149
+    assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 64, 256, ok) == 3 * nb * 64 * 4 + 256
+    assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 64, 256, _local(lp, 151936, 152064, [114048, 152064])) > 0
+    assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 64, 256, _local(lp, 151936, 152064, [0, 152064])) > 0
+    # beyond the padded vocabulary, a negative start, a gap: rejected (size 0)
+    assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 64, 256, _local(lp, 151936, 152064, [114048, 152065])) == 0
+    assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 64, 256, _local(lp, 1000, 1000, [-8, 500])) == 0
+    bad = lp.VocabPartition(1000, 1000, ((0, 400), (500, 1000)), local=True)
+    assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 64, 256, bad) == 0
+    # the same ranges without the flag do not cover the vocabulary
+    assert lp.lp_workspace_size(lp.LP_OP_FORWARD, 64, 256,
+                                lp.VocabPartition(151936, 152064, ((38016, 76032),))) == 0
+    # a flag other than 0 / 1 is rejected
+    cp, keep = lp._c_partition(ok)
+    cp.local = 2
+    assert lp.lib().lp_workspace_size(lp.LP_OP_FORWARD, 64, 256, ctypes.byref(cp)) == 0
+
+
+@pytest.mark.skipif(_has_gpu(), reason="uses fake device pointers; only safe without a GPU")
+def test_merge_and_sum_host_validation(lp):
+    L = lp.lib()
+    A, B = 0x100000, 0x900000            # fake, 16-byte aligned, far apart; never dereferenced on the host
+    p = _part(lp, 1000, 1000, [0, 400, 1000])
+    cp, keep = lp._c_partition(p)
+
+    def merge(stats=A, T=8, y=A, logp=B, lse=B + 64, ent=None, ss=None):
+        out = lp._Outputs(logp, lse, ent, ss)
+        return L.lp_merge_shard_stats(stats, T, ctypes.byref(cp), y, ctypes.byref(out), None)
+
+    assert merge(stats=None) == 1
+    assert merge(y=None) == 1
+    assert merge(lse=None) == 1
+    assert merge(ss=B + 128) == 1                 # shard statistics are an input here, not an output
+    assert merge(T=0, stats=None, y=None) == 0    # empty batch: no work
+    assert merge() == 3                           # valid: fails only for want of a GPU
+
+    def psum(parts=(A, A + 4096), n=None, count=1000, out=B, dtype=lp.LP_DTYPE_F32):
+        P = (ctypes.c_void_p * max(len(parts), 1))(*parts)
+        return L.lp_sum_partials(P, len(parts) if n is None else n, count, out, dtype, None)
+
+    assert psum(n=0) == 1
+    assert psum(n=65, parts=[A + 4096 * i for i in range(65)]) == 1
+    assert psum(dtype=2) == 1
+    assert psum(out=None) == 1
+    assert psum(parts=(A + 4, A + 4096)) == 2     # misaligned part
+    assert psum(out=B + 8) == 2                   # misaligned output
+    assert psum(out=A + 4096) == 1                # output over a later part
+    assert psum(out=A + 16) == 1                  # output over part 0, not exactly in place
+    assert psum(out=A, dtype=lp.LP_DTYPE_BF16) == 1   # bf16 over fp32 part 0 is not in place
+    assert psum(count=0, parts=(None,), out=None) == 0
+    assert psum(out=A) == 3                       # in place into part 0: valid
+    assert psum() == 3

@@ -75,6 +75,15 @@ def _every_entry_point(lp, case):
     for k, d in enumerate(dL):
         if d is not None:
             out[f"dL{k}"] = d
+    # the vocabulary-parallel steps: a rank-local replay (other ranks' ids skipped), the
+    # rank-ordered merge of statistics and the ordered sum of partials
+    ranges = P.ranges
+    Pl = lp.VocabPartition(P.vocab_real, P.vocab_padded, ranges[2:], local=True)
+    rloc = lp.lp_top_p_replay(X, W[2:], None if b is None else b[2:], Pl, ids, y, tau, shard_stats=True)
+    out.update({f"replay_local_{k}": v for k, v in rloc.items() if v is not None})
+    m = lp.lp_merge_shard_stats(f["shard_stats"], y, P)
+    out.update({f"merge_{k}": v for k, v in m.items() if v is not None})
+    out["sum"] = lp.lp_sum_partials([bw["dX"], bw["dX"].flip(0).contiguous(), bw["dX"]])
     torch.cuda.synchronize()
     return out
 

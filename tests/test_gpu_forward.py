@@ -43,7 +43,7 @@ def _compare(out, ref, shard_stats=False):
         for k, s in enumerate(ref.shards):
             assert max_abs(ss[k, 0], s.lse) <= TOL_LSE
             assert max_abs(ss[k, 1], s.t) <= TOL_LOGP
-            assert max_abs(ss[k, 2], s.mu) <= TOL_ENT
+            assert max_abs(ss[k, 2], s.h) <= TOL_ENT
 
 
 def test_tiny_config_parity(lp):

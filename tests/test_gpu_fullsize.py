@@ -167,7 +167,7 @@ def test_logits_reuse_full_width_four_padded_shards(lp):
     for k, s in enumerate(ref.shards):
         assert max_abs(ss[k, 0][rows], s.lse) <= TOL_LSE
         assert max_abs(ss[k, 1][rows], s.t) <= TOL_LOGP
-        assert max_abs(ss[k, 2][rows], s.mu) <= TOL_ENT
+        assert max_abs(ss[k, 2][rows], s.h) <= TOL_ENT
     sub = lp.lp_forward_from_logits([x[1000:1100] for x in Ld], part_of(part), dev_i32(y[1000:1100]), tau)
     for key in ("logp", "lse", "entropy"):
         assert torch.equal(sub[key], out[key][1000:1100])

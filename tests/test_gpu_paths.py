@@ -70,7 +70,7 @@ def test_logits_reuse_parity(lp, T, bounds, real):
     for k, s in enumerate(ref.shards):
         assert max_abs(ss[k, 0], s.lse) <= TOL_LSE
         assert max_abs(ss[k, 1], s.t) <= TOL_LOGP
-        assert max_abs(ss[k, 2], s.mu) <= TOL_ENT
+        assert max_abs(ss[k, 2], s.h) <= TOL_ENT
 
 
 def test_logits_reuse_bitwise_and_batch_invariant(lp):
@@ -148,8 +148,8 @@ def test_logits_reuse_masked_and_extreme_rows(lp, tau):
     for k in range(part.n_shards):
         live = ~empty[k]
         assert max_abs(ss[k, 0, live], ref.shards[k].lse[live]) <= TOL_LSE
-        assert max_abs(ss[k, 2, live], ref.shards[k].mu[live]) <= TOL_ENT
-        # a shard whose ids are all masked is empty: LSE -inf, mean 0
+        assert max_abs(ss[k, 2, live], ref.shards[k].h[live]) <= TOL_ENT
+        # a shard whose ids are all masked is empty: LSE -inf, entropy 0
         assert np.all(np.isneginf(ss[k, 0, empty[k]])) and np.all(ss[k, 2, empty[k]] == 0.0)
 
 
