@@ -192,10 +192,11 @@ def test_merge_entry_point_edge_rows(lp):
 def test_sum_partials_adds_in_rank_order(lp, n, count):
     import torch
     rng = np.random.default_rng(n * 1000 + count)
-    parts = [rng.standard_normal(count).astype(np.float32) * (10.0 ** rng.integers(-3, 4)) for _ in range(n)]
+    parts = [(rng.standard_normal(count) * 10.0 ** float(rng.integers(-3, 4))).astype(np.float32) for _ in range(n)]
     expect = parts[0].copy()
     for q in parts[1:]:
         expect += q                                      # fp32, round to nearest, in order
+    assert expect.dtype == np.float32
     d = [dev_f32(q) for q in parts]
     got = lp.lp_sum_partials(d)
     assert np.array_equal(_np(got), expect)
