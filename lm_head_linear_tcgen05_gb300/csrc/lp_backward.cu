@@ -10,10 +10,10 @@
 //
 // Steps (all in the caller's workspace; nothing is allocated):
 //   1. the G kernel: the forward's projection X W_k^T recomputed tile by tile on the
-//      tensor core (2-CTA clusters, W tile multicast); its epilogue forms G from the
+//      tensor core (CTA pairs on the paired-SM MMA); its epilogue forms G from the
 //      accumulator and the saved LSE and writes it once, bf16 [T, Vc];
 //   2. dW_k^T = X^T G_k: tcgen05 GEMM with both operands read MN-major straight from
-//      X [T, H] and G [T, Vc] (K = T), 2-CTA clusters sharing the G tile; the
+//      X [T, H] and G [T, Vc] (K = T), CTA pairs each holding half of the G tile; the
 //      epilogue stores each accumulator row h as column h of dW_k;
 //   3. dX = G W: tcgen05 GEMM, A = G (K-major), B = W_k read MN-major from each
 //      shard's own weight (K = every shard's columns in ascending order), split into

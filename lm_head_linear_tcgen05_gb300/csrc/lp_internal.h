@@ -15,14 +15,15 @@ namespace lp {
 constexpr int kFwdBlockM = 128;
 constexpr int kFwdBlockN = 256;
 constexpr int kFwdBlockK = 64;
-// CTAs per cluster along M in the projection GEMMs (forward and the backward's G):
-// the two row blocks of one vocabulary block share its W box through TMA multicast,
-// so row blocks are counted in pairs and W maps have boxes of kFwdBlockN / 2 rows.
-// (Four also works - a quarter box each - but fewer four-CTA clusters fit on the chip.)
+// CTAs per cluster along M in the projection GEMMs (forward and backward): a CTA pair
+// on the paired-SM MMA, which takes the two row blocks of one vocabulary block and holds
+// half of its W box in each CTA, so row blocks are counted in pairs and W maps have boxes
+// of kFwdBlockN / 2 rows. 1 runs every tile on one CTA.
 #ifndef LP_CLUSTER_M
 #define LP_CLUSTER_M 2
 #endif
 constexpr int kFwdClusterM = LP_CLUSTER_M;
+static_assert(kFwdClusterM == 1 || kFwdClusterM == 2, "one CTA or a CTA pair per tile pair");
 
 // Validated vocabulary partition (host side).
 struct Shards {

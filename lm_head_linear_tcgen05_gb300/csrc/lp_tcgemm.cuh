@@ -1,34 +1,38 @@
 // lp_tcgemm.cuh - persistent warp-specialised bf16 GEMM pipeline on tcgen05/TMEM.
 //
-// C_tile[128 x 256] = sum_k A[rows, k] * B[cols, k]  (both operands K-major bf16,
-// fp32 accumulation in tensor memory), followed by an epilogue supplied by the
-// caller that reads the accumulator straight out of TMEM. The kernel is persistent
-// (one CTA per SM, tiles handed out round-robin) and warp specialised:
+// C_tile[128 x 256] = sum_k A[rows, k] * B[cols, k]  (K-major or MN-major bf16 operands,
+// fp32 accumulation in tensor memory), followed by an epilogue supplied by the caller
+// that reads the accumulator straight out of TMEM. The kernel is persistent (one CTA per
+// SM, tiles handed out round-robin) and warp specialised:
 //
 //   warp 0      TMA producer: A and B boxes (64 K-elements wide, 128-byte swizzle)
-//               into a kGemmStages-deep shared-memory ring (mbarrier full/empty);
+//               into a shared-memory ring of S::kStages stages (mbarrier full/empty);
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
-//               issues tcgen05.mma kind::f16 (M=128, N=256, K=16) from one thread,
-//               committing each stage back to the producer and each finished tile
-//               to the epilogue;
+//               issues tcgen05.mma kind::f16 (K=16) from one thread, committing each
+//               stage back to the producers and each finished tile to the epilogue;
 //   warps 2..5  epilogue: warp w may read TMEM lanes 32*(w%4)..+31, so each thread
 //               owns one row of the tile; the callback runs while the MMA warp
 //               fills the other accumulator.
 //
-// With kClusterM = 2 the CTAs run in clusters of two that take the two row blocks of
-// the same column block (tiles 2j and 2j+1): each CTA fetches half of the shared B
-// box (128 of its 256 rows) and multicasts it into both CTAs' shared memory, so every
-// SM pulls 32 KB instead of 48 KB per K step through L2. A stage may then be refilled
-// only when both CTAs' MMAs are done with it: each MMA commit arrives on the empty
-// barrier of both CTAs (count 2). kClusterM = 4 generalises this to quarter boxes.
+// kClusterM = 2 runs the CTAs as pairs on the paired-SM MMA (tcgen05 .cta_group::2). The
+// two CTAs of a pair take the two row blocks of one column block (tiles 2j and 2j+1):
+// each loads its own 128 rows of A and one half (128 rows) of the shared B box into its
+// own shared memory, and the pair's even CTA issues M = 256, N = 256 MMAs that read A and
+// B from both CTAs' shared memory and leave each CTA's 128 rows in its own TMEM. Every SM
+// thus receives 32 KB of operands per 64-deep K step instead of 48 KB, and no operand is
+// copied to more than one SM. Both CTAs' copies complete on the even CTA's full barrier
+// (it expects the pair's bytes); each MMA commit arrives on the empty barrier of both
+// CTAs, each finished tile on both CTAs' accumulator barriers, and all eight epilogue
+// warps of the pair release an accumulator on the even CTA's barrier.
 //
 // Every mbarrier wait is bounded in time (see lp_device.cuh): a wait that runs past
 // the limit records LP_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag and every
 // role leaves its loop; the producer then waits (bounded) for its copies in flight,
-// the MMA warp for its MMAs, and TMEM is freed before the CTA exits.
+// the MMA thread for its MMAs, a cluster barrier keeps both CTAs of a pair alive until
+// neither can touch the other, and TMEM is freed before the CTA exits.
 //
 // An epilogue type E derives from GemmEpiBase and provides
-//   static constexpr int kClusterM;       1, or 2 for the multicast pairing above
+//   static constexpr int kClusterM;       1, or 2 for the CTA pairs above
 //   kAMN / kBMN                           operand major-ness (default K-major)
 //   a_k / b_k                             per-k-block map and K coordinate (default above)
 //   struct E::Params           with members `CUtensorMap maps[kGemmMaps]`,
@@ -41,9 +45,9 @@
 //   static void E::run(const Params&, int tile, int half, uint32_t tmem_row_base, int quarter, int lane);
 // `tmem_row_base` addresses column 0 of the accumulator of rows [128 half, 128 half + 128)
 // of the tile at this warp's first lane; column c of this thread's row is at
-// tmem_row_base + c. Boxes: K-major A 64 x 128,
-// K-major B 64 x 256 (64 x 128 with kClusterM = 2: each CTA loads half), MN-major
-// operands 64 x 64 atoms (with kClusterM = 2 each CTA loads half of B's atoms).
+// tmem_row_base + c. Boxes: K-major A 64 x 128, K-major B 64 x 256 (64 x 128 in a pair:
+// each CTA loads its half), MN-major operands 64 x 64 atoms (a pair's CTAs load half of
+// B's atoms each).
 #pragma once
 
 #include <atomic>
@@ -55,7 +59,6 @@ namespace lp {
 constexpr int kGemmBlockM = kFwdBlockM;
 constexpr int kGemmBlockN = kFwdBlockN;
 constexpr int kGemmBlockK = kFwdBlockK;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int kGemmMaxStages = 4;
 constexpr int kGemmThreads = 192;
 constexpr int kGemmTmemCols = 512;
 constexpr int kGemmMaps = LP_MAX_SHARDS + 1;
@@ -107,9 +110,13 @@ struct GemmEpiBase {
   }
 };
 
+#ifndef LP_GEMM_MAX_STAGES
+#define LP_GEMM_MAX_STAGES 8
+#endif
+
 struct GemmSync {
-  uint64_t full[kGemmMaxStages];
-  uint64_t empty[kGemmMaxStages];
+  uint64_t full[LP_GEMM_MAX_STAGES];
+  uint64_t empty[LP_GEMM_MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t done;
@@ -117,64 +124,70 @@ struct GemmSync {
   int abort;
 };
 
-// Ring geometry of an epilogue type: 4 stages of 48 KB for 128-row tiles (two TMEM
-// accumulators, so the epilogue of one tile overlaps the MMAs of the next), or 3 stages
-// of 64 KB for 256-row tiles (both halves fill all 512 TMEM columns: meant for tiles
-// whose K loop is long enough that the epilogue gap does not matter).
+// Ring geometry of an epilogue type: a stage holds kMHalves 128-row halves of A and this
+// CTA's rows of B (all 256, or 128 in a CTA pair); as many stages as fit the shared memory
+// (up to LP_GEMM_MAX_STAGES). 128-row tiles keep two TMEM accumulators, so the epilogue of
+// one tile overlaps the MMAs of the next; 256-row tiles fill all 512 TMEM columns with
+// their two halves (meant for tiles whose K loop is long enough that the epilogue gap does
+// not matter).
 template <class E>
 struct GemmShape {
+  static constexpr int kCG = E::kClusterM;
+  static_assert(kCG == 1 || kCG == 2, "one CTA, or a CTA pair");
   static constexpr int kMH = E::kMHalves;
   static_assert(kMH == 1 || kMH == 2, "one or two 128-row halves");
-  static constexpr int kStages = kMH == 1 ? 4 : 3;
   static constexpr uint32_t kStageA = kMH * kGemmStageA;
-  static constexpr uint32_t kStageBytes = kStageA + kGemmStageB;
+  static constexpr uint32_t kStageB = kGemmStageB / kCG;
+  static constexpr uint32_t kStageBytes = kStageA + kStageB;
+  static constexpr size_t kFixed = 1024 + sizeof(GemmSync);
+  static constexpr int kFit = int((232448 - kFixed) / kStageBytes);
+  static constexpr int kStages = kFit < LP_GEMM_MAX_STAGES ? kFit : LP_GEMM_MAX_STAGES;
   static constexpr int kAcc = kMH == 1 ? 2 : 1;  // accumulators in flight
-  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + sizeof(GemmSync);
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr size_t kSmemBytes = kFixed + size_t(kStages) * kStageBytes;
+  static_assert(kStages >= 2 && kSmemBytes <= 232448, "shared memory budget");
 };
 
 template <class E>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ typename E::Params p) {
-  constexpr int kCM = E::kClusterM;
-  static_assert(kCM == 1 || kCM == 2 || kCM == 4, "cluster of one, two or four CTAs along M");
-  constexpr uint16_t kCtaMask = uint16_t((1u << kCM) - 1u);  // every CTA of the cluster
   using S = GemmShape<E>;
-  constexpr int kGemmStages = S::kStages;
+  constexpr int kCG = S::kCG;
+  constexpr int kStages = S::kStages;
   constexpr int kMH = S::kMH;
   static_assert(kMH == 1 || !E::kAMN, "256-row tiles take a K-major A operand");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kGemmStages * S::kStageA;
-  GemmSync* sync = reinterpret_cast<GemmSync*>(smem + kGemmStages * S::kStageBytes);
+  uint8_t* sB = smem + kStages * S::kStageA;
+  GemmSync* sync = reinterpret_cast<GemmSync*>(smem + kStages * S::kStageBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = kCM > 1 ? cluster_ctarank() : 0u;
-  const int cluster_id = int(blockIdx.x) / kCM;
-  const int num_clusters = int(gridDim.x) / kCM;
-  const int cluster_tiles = p.total_tiles / kCM;
+  const uint32_t rank = kCG > 1 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;  // the CTA that issues the MMAs
+  const int cluster_id = int(blockIdx.x) / kCG;
+  const int num_clusters = int(gridDim.x) / kCG;
+  const int cluster_tiles = p.total_tiles / kCG;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGemmStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&sync->full[s], 1);
-      mbar_init(&sync->empty[s], kCM);
+      mbar_init(&sync->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sync->tfull[b], 1);
-      mbar_init(&sync->tempty[b], 4);
+      mbar_init(&sync->tempty[b], 4 * kCG);
     }
     mbar_init(&sync->done, 1);
     sync->abort = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sync->tmem_base, kGemmTmemCols);
-    tmem_relinquish();
+    tmem_alloc<kCG>(&sync->tmem_base, kGemmTmemCols);
+    tmem_relinquish<kCG>();
   }
   tc_fence_before();
-  if constexpr (kCM > 1)
-    cluster_sync();  // the peers' barriers are initialised before anything targets them
+  if constexpr (kCG > 1)
+    cluster_sync();  // the pair's barriers and TMEM exist before anything targets them
   else
     __syncthreads();
   tc_fence_after();
@@ -186,16 +199,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       // --------------------------------------------------------- TMA producer
       const uint64_t pol_keep = l2_policy_evict_last();
       const uint64_t pol_norm = l2_policy_evict_normal();
-      uint32_t stage_tx = S::kStageBytes;  // bytes that complete one stage
+      uint32_t stage_tx = S::kStageBytes;  // bytes this CTA's copies deliver per stage
       if constexpr (E::kVarABox) {
-        static_assert(kMH == 1 && !E::kAMN, "short A boxes: one K-major 128-row half");
+        static_assert(kMH == 1 && !E::kAMN && kCG == 1, "short A boxes: one K-major 128-row half, one CTA");
         stage_tx = kGemmStageB + uint32_t(p.a_box_rows) * (kGemmBlockK * 2);
       }
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, armed_phase = 0;  // stages with a copy issued, and its phase
       bool ok = true;
       for (int ct = cluster_id; ok && ct < cluster_tiles; ct += num_clusters) {
-        const TileJob j = E::job(p, ct * kCM + int(rank));
+        const TileJob j = E::job(p, ct * kCG + int(rank));
         const uint64_t pa = ((p.keep_maps >> j.a_map) & 1u) ? pol_keep : pol_norm;
         const uint64_t pb = ((p.keep_maps >> j.b_map) & 1u) ? pol_keep : pol_norm;
         for (int kb = 0; kb < j.nkb; ++kb) {
@@ -206,61 +219,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           int am, ak, bm, bk;
           E::a_k(&p, j, kb, am, ak);
           E::b_k(&p, j, kb, bm, bk);
-          mbar_arrive_expect_tx(&sync->full[stage], stage_tx);
+          // the pair's copies all complete on the leader's barrier, which expects both CTAs' bytes
+          if (leader) mbar_arrive_expect_tx(&sync->full[stage], stage_tx * kCG);
           uint8_t* dA = sA + stage * S::kStageA;
-          uint8_t* dB = sB + stage * kGemmStageB;
+          uint8_t* dB = sB + stage * S::kStageB;
+          const uint32_t bar_cl = kCG > 1 ? cluster_addr(&sync->full[stage], 0) : 0u;
+          auto load = [&](void* dst, int map, int32_t x, int32_t y, uint64_t pol) {
+            if constexpr (kCG > 1)
+              tma_load_2d_pair(dst, &p.maps[map], bar_cl, x, y, pol);
+            else
+              tma_load_2d(dst, &p.maps[map], &sync->full[stage], x, y, pol);
+          };
           if constexpr (!E::kAMN) {
 #pragma unroll
-            for (int h = 0; h < kMH; ++h)
-              tma_load_2d(dA + h * kGemmStageA, &p.maps[am], &sync->full[stage], ak, j.a_y + h * kGemmBlockM, pa);
+            for (int h = 0; h < kMH; ++h) load(dA + h * kGemmStageA, am, ak, j.a_y + h * kGemmBlockM, pa);
           } else {  // MN-major: 64-element atoms of 64 K rows each
 #pragma unroll
-            for (int i = 0; i < kGemmBlockM / 64; ++i)
-              tma_load_2d(dA + i * kMNAtomBytes, &p.maps[am], &sync->full[stage], j.a_y + 64 * i, ak, pa);
+            for (int i = 0; i < kGemmBlockM / 64; ++i) load(dA + i * kMNAtomBytes, am, j.a_y + 64 * i, ak, pa);
           }
           if constexpr (!E::kBMN) {
-            if constexpr (kCM > 1)
-              tma_load_2d_multicast(dB + rank * (kGemmStageB / kCM), &p.maps[bm], &sync->full[stage], bk,
-                                    j.b_y + int(rank) * (kGemmBlockN / kCM), kCtaMask, pb);
-            else
-              tma_load_2d(dB, &p.maps[bm], &sync->full[stage], bk, j.b_y, pb);
+            load(dB, bm, bk, j.b_y + int(rank) * (kGemmBlockN / kCG), pb);
           } else {
-            constexpr int kAtoms = kGemmBlockN / 64;
+            constexpr int kAtoms = kGemmBlockN / 64 / kCG;  // this CTA's atoms of B
 #pragma unroll
-            for (int i = 0; i < kAtoms / kCM; ++i) {
-              const int a = int(rank) * (kAtoms / kCM) + i;
-              if constexpr (kCM > 1)
-                tma_load_2d_multicast(dB + a * kMNAtomBytes, &p.maps[bm], &sync->full[stage], j.b_y + 64 * a, bk,
-                                      kCtaMask, pb);
-              else
-                tma_load_2d(dB + a * kMNAtomBytes, &p.maps[bm], &sync->full[stage], j.b_y + 64 * a, bk, pb);
-            }
+            for (int i = 0; i < kAtoms; ++i)
+              load(dB + i * kMNAtomBytes, bm, j.b_y + 64 * (int(rank) * kAtoms + i), bk, pb);
           }
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kGemmStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) {
-        for (int s = 0; s < kGemmStages; ++s)
-          if (armed & (1u << s)) drain_wait(&sync->full[s], (armed_phase >> s) & 1u, p.wait_limit_ns);
+        // the leader's barriers count the pair's bytes, so its drain waits for both CTAs'
+        // armed copies; the other CTA cannot observe its own, and gives any copy still in
+        // flight (a few microseconds at most) time to land before the CTAs leave
+        if (leader) {
+          for (int s = 0; s < kStages; ++s)
+            if (armed & (1u << s)) drain_wait(&sync->full[s], (armed_phase >> s) & 1u, p.wait_limit_ns);
+        } else {
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 100000ull) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBlockM, kGemmBlockN, E::kAMN, E::kBMN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBlockM * kCG, kGemmBlockN, E::kAMN, E::kBMN);
       // per 16-deep K step: +32 bytes inside a K-major row, +2048 bytes (16 rows) in MN-major
       constexpr uint32_t a_step = E::kAMN ? 128u : 2u;
       constexpr uint32_t b_step = E::kBMN ? 128u : 2u;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int ct = cluster_id; ok && ct < cluster_tiles; ct += num_clusters) {
-        const TileJob j = E::job(p, ct * kCM + int(rank));
-        if (!mbar_wait(&sync->tempty[acc], acc_phase ^ 1u, abort, p.wait_limit_ns, p.err)) break;
+        const TileJob j = E::job(p, ct * kCG);
+        const bool free_acc = kCG > 1
+                                  ? mbar_wait_cluster(&sync->tempty[acc], acc_phase ^ 1u, abort, p.wait_limit_ns, p.err)
+                                  : mbar_wait(&sync->tempty[acc], acc_phase ^ 1u, abort, p.wait_limit_ns, p.err);
+        if (!free_acc) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * kGemmBlockN;  // half h at + h * kGemmBlockN
         for (int kb = 0; kb < j.nkb; ++kb) {
@@ -270,7 +291,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           }
           tc_fence_after();
           const uint32_t aa = smem_u32(sA + stage * S::kStageA);
-          const uint32_t ba = smem_u32(sB + stage * kGemmStageB);
+          const uint32_t ba = smem_u32(sB + stage * S::kStageB);
           const uint64_t b_desc = E::kBMN ? sw128_mnmajor_desc(ba, kMNAtomBytes) : sw128_kmajor_desc(ba);
 #pragma unroll
           for (int h = 0; h < kMH; ++h) {
@@ -278,26 +299,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             const uint64_t a_desc = E::kAMN ? sw128_mnmajor_desc(ah, kMNAtomBytes) : sw128_kmajor_desc(ah);
 #pragma unroll
             for (int k = 0; k < kGemmBlockK / 16; ++k)
-              umma_bf16(d_tmem + h * kGemmBlockN, a_desc + a_step * k, b_desc + b_step * k, idesc,
-                        (kb | k) != 0 ? 1u : 0u);
+              umma_bf16<kCG>(d_tmem + h * kGemmBlockN, a_desc + a_step * k, b_desc + b_step * k, idesc,
+                             (kb | k) != 0 ? 1u : 0u);
           }
-          if constexpr (kCM > 1)
-            umma_commit_multicast(&sync->empty[stage], kCtaMask);
+          if constexpr (kCG > 1)
+            umma_commit_pair(&sync->empty[stage]);
           else
-            umma_commit(&sync->empty[stage]);
-          if (++stage == kGemmStages) {
+            umma_commit<1>(&sync->empty[stage]);
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&sync->tfull[acc]);
+        if constexpr (kCG > 1)
+          umma_commit_pair(&sync->tfull[acc]);
+        else
+          umma_commit<1>(&sync->tfull[acc]);
         if (++acc == uint32_t(S::kAcc)) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      umma_commit(&sync->done);
+      umma_commit<kCG>(&sync->done);
       drain_wait(&sync->done, 0, p.wait_limit_ns);
     }
   } else {
@@ -311,10 +335,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       tc_fence_after();
 #pragma unroll 1
       for (int h = 0; h < kMH; ++h)
-        E::run(p, ct * kCM + int(rank), h, tmem + (uint32_t(q * 32) << 16) + (acc + h) * kGemmBlockN, q, lane);
+        E::run(p, ct * kCG + int(rank), h, tmem + (uint32_t(q * 32) << 16) + (acc + h) * kGemmBlockN, q, lane);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sync->tempty[acc]);
+      if (lane == 0) {
+        if constexpr (kCG > 1)
+          mbar_arrive_cluster(cluster_addr(&sync->tempty[acc], 0));  // the leader's barrier
+        else
+          mbar_arrive(&sync->tempty[acc]);
+      }
       if (++acc == uint32_t(S::kAcc)) {
         acc = 0;
         acc_phase ^= 1u;
@@ -323,13 +352,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   }
 
   tc_fence_before();
-  if constexpr (kCM > 1)
-    cluster_sync();  // no CTA leaves while a peer may still signal or write into it
+  if constexpr (kCG > 1)
+    cluster_sync();  // no CTA leaves while the pair's MMAs or copies may still touch it
   else
     __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kGemmTmemCols);
+    tmem_dealloc<kCG>(tmem, kGemmTmemCols);
   }
 }
 
@@ -340,6 +369,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 template <class E>
 int gemm_clusters_for_device(int num_sms) {
   constexpr int kCM = E::kClusterM;
+  static_assert(kCM == 1 || kCM == 2, "one CTA or a CTA pair");
   static std::atomic<int> cache[64];  // 0 = unresolved, > 0 = clusters, < 0 = error
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
