@@ -15,9 +15,9 @@ Every input is synthetic and seeded; the weights and logits are larger than the
 CPU oracle on the host cores on a bounded row sample of the same workload (under
 torchrun, rank 0 alone runs it).
 
-One GPU only: the projection GEMMs share each W tile between the two CTAs of a cluster
-with TMA multicast loads, which this library runs on single-GPU calls only, so the GPU arm
-refuses a run with more than one rank (or --gpus > 1) before it touches a GPU.
+One GPU only: the benchmark times the one-GPU hot path. The GPU arm refuses a run with
+more than one rank (or --gpus > 1) before it touches a GPU; the multi-GPU vocabulary-parallel
+path (lm_head_linear_tcgen05_gb300.vocab_parallel) is tested but not timed here.
 """
 from __future__ import annotations
 
@@ -230,9 +230,8 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-ONE_GPU_ONLY = ("one-GPU library: its projection GEMMs load each W tile once per pair of SMs with TMA "
-                "cluster multicast, which this build runs on single-GPU calls only; run bench.py with one rank "
-                "and --gpus 1")
+ONE_GPU_ONLY = ("bench.py times the one-GPU hot path only (the vocabulary-parallel multi-GPU path is tested, "
+                "not timed); run it with one rank and --gpus 1")
 
 
 def refuse_multi_gpu(args, world: int) -> bool:

@@ -1,6 +1,5 @@
-"""The benchmark's GPU arm is one-GPU only (its projection GEMMs use TMA cluster multicast,
-which this library runs on single-GPU calls only): with more than one rank, or --gpus > 1,
-it refuses before any GPU or process-group work. The reference arm (the CPU oracle) runs on
+"""The benchmark's GPU arm times the one-GPU hot path only: with more than one rank, or
+--gpus > 1, it refuses before any GPU or process-group work. The reference arm (the CPU oracle) runs on
 rank 0 alone under torchrun; the other ranks exit without work. CPU only."""
 import json
 
