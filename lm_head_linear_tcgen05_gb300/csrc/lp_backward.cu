@@ -75,11 +75,52 @@ BwdLayout bwd_layout(int64_t T, int64_t H, const Shards& sh) {
 
 __device__ __forceinline__ float f32(uint32_t r) { return __uint_as_float(r); }
 
+// The backward's large outputs (G, 1.2 GB at the headline size, and dW) stream through L2
+// once; storing them with an evict-first policy keeps the GEMM operands (X, W, G slices)
+// resident instead. LP_BWD_STORE_EVICT_FIRST=0 stores them with the default policy.
+#ifndef LP_BWD_STORE_EVICT_FIRST
+#define LP_BWD_STORE_EVICT_FIRST 1
+#endif
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // one 32-byte store (a whole sector per lane); p must be 32-byte aligned
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v, uint64_t pol) {
+#if LP_BWD_STORE_EVICT_FIRST
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "l"(pol)
+               : "memory");
+#else
+  (void)pol;
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
                "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
+#endif
+}
+
+__device__ __forceinline__ void st_global_f32(float* p, float v, uint64_t pol) {
+#if LP_BWD_STORE_EVICT_FIRST
+  asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(__float_as_uint(v)), "l"(pol) : "memory");
+#else
+  (void)pol;
+  *p = v;
+#endif
+}
+
+__device__ __forceinline__ void st_global_bf16(__nv_bfloat16* p, float v, uint64_t pol) {
+#if LP_BWD_STORE_EVICT_FIRST
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p), "h"(*reinterpret_cast<const uint16_t*>(&b)),
+               "l"(pol)
+               : "memory");
+#else
+  (void)pol;
+  *p = __float2bfloat16_rn(v);
+#endif
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -242,6 +283,7 @@ struct GradEpi : GemmEpiBase {
       }
     }
     const __nv_bfloat16* bias = p.bias[c.shard];
+    const uint64_t pol = l2_policy_evict_first();
     const int64_t col_base = p.coff[c.shard] + n0;
     uint16_t* grow = p.G + size_t(in_rows ? row : 0) * size_t(p.Vc) + size_t(col_base);
     float* dbrow = p.dbp != nullptr ? p.dbp + (size_t(c.mb) * 4 + size_t(q)) * size_t(p.Vc) + size_t(col_base) : nullptr;
@@ -275,8 +317,8 @@ struct GradEpi : GemmEpiBase {
         uint32_t packed[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) packed[j] = pack_bf16(gv[2 * j], gv[2 * j + 1]);
-        st_global_v8(grow + ch * 32, packed);
-        st_global_v8(grow + ch * 32 + 16, packed + 8);
+        st_global_v8(grow + ch * 32, packed, pol);
+        st_global_v8(grow + ch * 32 + 16, packed + 8, pol);
       }
       // bias gradient: this warp's 32 rows of the chunk's 32 columns, summed in fp32
       if (dbrow != nullptr) dbrow[ch * 32 + lane] = warp_column_sum(gv, lane);
@@ -349,6 +391,7 @@ struct DwEpi : GemmEpiBase {
     const int valid = int(left < kGemmBlockN ? left : kGemmBlockN);
     const bool ok = h < p.H;
     const size_t off = size_t(v0) * size_t(p.H) + size_t(ok ? h : 0);
+    const uint64_t pol = l2_policy_evict_first();
     if (p.dw_bf16) {  // a warp stores 64 contiguous bytes of one dW row per instruction
       __nv_bfloat16* b16 = static_cast<__nv_bfloat16*>(p.dW[c.shard]) + off;
 #pragma unroll 1
@@ -359,7 +402,7 @@ struct DwEpi : GemmEpiBase {
         if (ok) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (ch * 32 + j < valid) b16[size_t(ch * 32 + j) * size_t(p.H)] = __float2bfloat16_rn(f32(r[j]));
+            if (ch * 32 + j < valid) st_global_bf16(b16 + size_t(ch * 32 + j) * size_t(p.H), f32(r[j]), pol);
         }
       }
       return;
@@ -381,12 +424,12 @@ struct DwEpi : GemmEpiBase {
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             if (ch * 32 + j0 + j < valid)
-              base[size_t(ch * 32 + j0 + j) * size_t(p.H)] = __fadd_rn(old[j], f32(r[j0 + j]));
+              st_global_f32(base + size_t(ch * 32 + j0 + j) * size_t(p.H), __fadd_rn(old[j], f32(r[j0 + j])), pol);
         }
       } else if (ok) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (ch * 32 + j < valid) base[size_t(ch * 32 + j) * size_t(p.H)] = f32(r[j]);
+          if (ch * 32 + j < valid) st_global_f32(base + size_t(ch * 32 + j) * size_t(p.H), f32(r[j]), pol);
       }
     }
   }
