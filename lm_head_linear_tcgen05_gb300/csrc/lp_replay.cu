@@ -21,8 +21,9 @@
 //      in ascending order. The order depends only on each shard's own ids.
 // The dense keep-mask route compacts each mask row into the same canonical slots
 // and runs this very kernel, so both routes produce identical bits for equal sets.
-// The logits-gather variant (reused unscaled logits instead of x . W) replaces step 3
-// by one gather per id and keeps steps 1 and 4.
+// The logits-gather variant (reused unscaled logits instead of x . W) runs one warp per
+// row: the same steps 1 and 4 (the same device functions), and one gather per id in place
+// of steps 2 and 3.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -122,156 +123,181 @@ __device__ __forceinline__ int shard_of(const ReplayParams& p, int64_t v) {
 
 }  // namespace
 
-template <bool kFromLogits>
+// 1. Canonicalise one row's replay slots (one warp): unused and invalid slots, and valid
+// ids outside this call's range [lo, hi) (another rank's ids in a rank-local partition),
+// become the key 0xFFFFFFFF, above every id; the 64 keys are sorted ascending, a key is
+// kept if it differs from its predecessor, and its rank is the number of kept keys before
+// it. Writes the distinct ids ascending to uniq[0..n) and returns n (0 for a row with an
+// invalid id, which is recorded as a device error and fails closed).
+__device__ __forceinline__ int canon_row(const ReplayParams& p, int row, int lane, int32_t* uniq) {
+  const int32_t* ids = p.ids + size_t(row) * LP_REPLAY_SLOTS;
+  const int32_t v0 = __ldg(ids + 2 * lane), v1 = __ldg(ids + 2 * lane + 1);
+  const bool bad0 = v0 != -1 && (v0 < 0 || int64_t(v0) >= p.vocab_real);
+  const bool bad1 = v1 != -1 && (v1 < 0 || int64_t(v1) >= p.vocab_real);
+  const unsigned any_bad = __ballot_sync(0xffffffffu, bad0 || bad1);
+  const int64_t lo = p.shard_start[0], hi = p.shard_end[p.n_shards - 1];
+  const bool here0 = int64_t(v0) >= lo && int64_t(v0) < hi, here1 = int64_t(v1) >= lo && int64_t(v1) < hi;
+  uint32_t k0 = (bad0 || v0 < 0 || !here0) ? 0xFFFFFFFFu : uint32_t(v0);
+  uint32_t k1 = (bad1 || v1 < 0 || !here1) ? 0xFFFFFFFFu : uint32_t(v1);
+  warp_sort64(k0, k1, lane);
+  const uint32_t prev0 = __shfl_up_sync(0xffffffffu, k1, 1);
+  const bool keep0 = k0 != 0xFFFFFFFFu && (lane == 0 || k0 != prev0);
+  const bool keep1 = k1 != 0xFFFFFFFFu && k1 != k0;
+  const unsigned b0 = __ballot_sync(0xffffffffu, keep0), b1 = __ballot_sync(0xffffffffu, keep1);
+  const unsigned lower = (1u << lane) - 1u;
+  const int before = __popc(b0 & lower) + __popc(b1 & lower);
+  if (keep0) uniq[before] = int32_t(k0);
+  if (keep1) uniq[before + (keep0 ? 1 : 0)] = int32_t(k1);
+  if (any_bad && lane == 0) record_error(p.err, LP_ERR_REPLAY_ID_OUT_OF_RANGE);
+  __syncwarp();
+  return any_bad ? 0 : __popc(b0) + __popc(b1);
+}
+
+// 4. Fold one row's scores (one warp), shard by shard: the shard's ids are a contiguous
+// run [i0, i1) of the ascending list; lane l takes its ids i0 + 2l and i0 + 2l + 1, the
+// lanes' statistics combine by a fixed shuffle tree, and the shards are reduced in
+// ascending order by row_finish - an order fixed by each shard's own ids alone, so a
+// rank-local call that holds only some of the shards folds each of them exactly as a call
+// holding all does, and every route that produces the same scores gives the same bits.
+// A row that failed closed arrives with n = 0: every shard is empty, LSE = logp = -inf.
+__device__ __forceinline__ void fold_row(const ReplayParams& p, int row, int lane, const int32_t* uniq,
+                                         const float* zs, int n) {
+  const size_t T = size_t(p.T);
+  const int yv = __ldg(p.y + row);
+  const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
+  if (lane == 0 && !y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
+  const int64_t id0 = 2 * lane < n ? int64_t(uniq[2 * lane]) : INT64_MAX;
+  const int64_t id1 = 2 * lane + 1 < n ? int64_t(uniq[2 * lane + 1]) : INT64_MAX;
+  // the target logit, if y is in the set: the lane holding it says which of its two ids
+  const bool own0 = y_ok && id0 == yv, own1 = y_ok && id1 == yv;
+  const unsigned tb = __ballot_sync(0xffffffffu, own0 || own1);
+  const bool t_found = tb != 0u;
+  const int src = t_found ? __ffs(tb) - 1 : 0;
+  const int t_idx = 2 * src + __shfl_sync(0xffffffffu, own0 ? 0 : 1, src);
+  const float t_val = t_found ? zs[t_idx] : 0.f;
+  int owner = -1;
+  float lse[LP_MAX_SHARDS], hz[LP_MAX_SHARDS], t[LP_MAX_SHARDS];
+#pragma unroll
+  for (int k = 0; k < LP_MAX_SHARDS; ++k) {
+    lse[k] = -INFINITY;
+    hz[k] = 0.f;
+    t[k] = 0.f;
+    if (k < p.n_shards) {
+      const int64_t s0 = p.shard_start[k], s1 = p.shard_end[k];
+      const int i0 = __popc(__ballot_sync(0xffffffffu, id0 < s0)) + __popc(__ballot_sync(0xffffffffu, id1 < s0));
+      const int i1 = __popc(__ballot_sync(0xffffffffu, id0 < s1)) + __popc(__ballot_sync(0xffffffffu, id1 < s1));
+      Stat loc = stat_empty();
+      if (i1 > i0) {
+        const int j0 = i0 + 2 * lane, j1 = j0 + 1;
+        if (j0 < i1) stat_push(loc, __fmul_rn(zs[j0], kLog2e));
+        if (j1 < i1) stat_push(loc, __fmul_rn(zs[j1], kLog2e));
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const Stat o{__shfl_down_sync(0xffffffffu, loc.m, off), __shfl_down_sync(0xffffffffu, loc.s, off),
+                       __shfl_down_sync(0xffffffffu, loc.a, off)};
+          if (lane < off) stat_merge(loc, o);
+        }
+      }
+      lse[k] = stat_lse(loc);
+      if (y_ok && yv >= s0 && yv < s1) {
+        owner = k;
+        // the target's logit over the support: z_y if kept, -inf if the shard keeps
+        // other ids but not y (an excluded id), 0 if the shard keeps none (empty shard)
+        t[k] = t_found ? t_val : (i1 > i0 ? -INFINITY : 0.f);
+      }
+    }
+  }
+  if (lane == 0) {
+    if (p.shard_stats != nullptr) {
+#pragma unroll
+      for (int k = 0; k < LP_MAX_SHARDS; ++k) {
+        if (k < p.n_shards) {
+          float* ss = p.shard_stats + size_t(k) * 3 * T;
+          ss[row] = lse[k];
+          ss[T + row] = t[k];
+          ss[2 * T + row] = 0.f;
+        }
+      }
+    }
+    const RowOut o = row_finish(lse, hz, t, p.n_shards, owner);
+    p.lse[row] = o.lse;
+    p.logp[row] = o.logp;
+  }
+}
+
+// Gather-GEMV replay: one CTA per row. Warp 0 canonicalises the slots while all threads
+// stage x; the warps then score the row's distinct ids (2, 3); warp 0 folds (4).
 __global__ void __launch_bounds__(kReplayThreads, LP_REPLAY_MIN_BLOCKS) replay_kernel(const __grid_constant__ ReplayParams p) {
   extern __shared__ uint4 xs[];  // the row of X, H / 8 vectors
   __shared__ int32_t uniq[LP_REPLAY_SLOTS];
   __shared__ float zs[LP_REPLAY_SLOTS];
   __shared__ int n_uniq;
-  __shared__ int bad_row;
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const size_t T = size_t(p.T);
   const int nvec = p.H >> 3;
 
-  // 1. validate, sort ascending, deduplicate (warp 0): unused and invalid slots, and valid
-  // ids outside this call's range [lo, hi) (another rank's ids in a rank-local partition),
-  // become the key 0xFFFFFFFF, above every id; after the sort a key is kept if it differs
-  // from its predecessor, and its rank is the number of kept keys before it
   if (warp == 0) {
-    const int32_t* ids = p.ids + size_t(row) * LP_REPLAY_SLOTS;
-    const int32_t v0 = __ldg(ids + 2 * lane), v1 = __ldg(ids + 2 * lane + 1);
-    const bool bad0 = v0 != -1 && (v0 < 0 || int64_t(v0) >= p.vocab_real);
-    const bool bad1 = v1 != -1 && (v1 < 0 || int64_t(v1) >= p.vocab_real);
-    const unsigned any_bad = __ballot_sync(0xffffffffu, bad0 || bad1);
-    const int64_t lo = p.shard_start[0], hi = p.shard_end[p.n_shards - 1];
-    const bool here0 = int64_t(v0) >= lo && int64_t(v0) < hi, here1 = int64_t(v1) >= lo && int64_t(v1) < hi;
-    uint32_t k0 = (bad0 || v0 < 0 || !here0) ? 0xFFFFFFFFu : uint32_t(v0);
-    uint32_t k1 = (bad1 || v1 < 0 || !here1) ? 0xFFFFFFFFu : uint32_t(v1);
-    warp_sort64(k0, k1, lane);
-    const uint32_t prev0 = __shfl_up_sync(0xffffffffu, k1, 1);
-    const bool keep0 = k0 != 0xFFFFFFFFu && (lane == 0 || k0 != prev0);
-    const bool keep1 = k1 != 0xFFFFFFFFu && k1 != k0;
-    const unsigned b0 = __ballot_sync(0xffffffffu, keep0), b1 = __ballot_sync(0xffffffffu, keep1);
-    const unsigned lower = (1u << lane) - 1u;
-    const int before = __popc(b0 & lower) + __popc(b1 & lower);
-    if (keep0) uniq[before] = int32_t(k0);
-    if (keep1) uniq[before + (keep0 ? 1 : 0)] = int32_t(k1);
-    if (lane == 0) {
-      n_uniq = __popc(b0) + __popc(b1);
-      bad_row = any_bad != 0u;
-      if (any_bad) record_error(p.err, LP_ERR_REPLAY_ID_OUT_OF_RANGE);
-    }
+    const int n = canon_row(p, row, lane, uniq);
+    if (lane == 0) n_uniq = n;
   }
-  if constexpr (!kFromLogits) {
-    // 2. stage x
-    const uint4* xrow = reinterpret_cast<const uint4*>(p.X) + size_t(row) * size_t(nvec);
-    for (int v = tid; v < nvec; v += kReplayThreads) xs[v] = __ldg(xrow + v);
+  // 2. stage x
+  const uint4* xrow = reinterpret_cast<const uint4*>(p.X) + size_t(row) * size_t(nvec);
+  for (int v = tid; v < nvec; v += kReplayThreads) xs[v] = __ldg(xrow + v);
+  __syncthreads();
+
+  const int n = n_uniq;
+  // 3. gather GEMV
+  for (int i = warp; i < n; i += kReplayWarps) {
+    const int64_t v = uniq[i];
+    const int k = shard_of(p, v);
+    const int64_t local = v - p.shard_start[k];
+    // the gathered row lies inside shard k's weight (the same for every lane)
+    if (!in_bounds(local >= 0 && v < p.shard_end[k] && v < p.vocab_real, p.err)) {
+      if (lane == 0) zs[i] = 0.f;
+      continue;
+    }
+    const uint4* wrow = reinterpret_cast<const uint4*>(p.W[k]) + size_t(local) * size_t(nvec);
+    const float dot = warp_dot(wrow, xs, nvec, lane);
+    if (lane == 0) {
+      const float b = p.bias[k] != nullptr ? __bfloat162float(p.bias[k][local]) : 0.f;
+      zs[i] = __fmul_rn(__fadd_rn(dot, b), p.inv_tau);
+    }
   }
   __syncthreads();
 
-  const int n = bad_row ? 0 : n_uniq;
-  if constexpr (!kFromLogits) {
-    // 3. gather GEMV
-    for (int i = warp; i < n; i += kReplayWarps) {
+  if (warp == 0) fold_row(p, row, lane, uniq, zs, n);
+}
+
+// Logits-gather replay: one warp per row (kReplayWarps rows per CTA), every step warp-wide -
+// canonicalise, one gather of the reused unscaled logit per distinct id (temperature
+// applied here, once), fold - so many rows' dependent loads are in flight per SM.
+__global__ void __launch_bounds__(kReplayThreads) replay_logits_kernel(const __grid_constant__ ReplayParams p) {
+  __shared__ int32_t uniq_s[kReplayWarps][LP_REPLAY_SLOTS];
+  __shared__ float zs_s[kReplayWarps][LP_REPLAY_SLOTS];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int row = int(blockIdx.x) * kReplayWarps + warp;
+  if (row >= p.T) return;
+  int32_t* uniq = uniq_s[warp];
+  float* zs = zs_s[warp];
+  const int n = canon_row(p, row, lane, uniq);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = 2 * lane + h;
+    if (i < n) {
       const int64_t v = uniq[i];
-      const int k = shard_of(p, v);
-      const int64_t local = v - p.shard_start[k];
-      // the gathered row lies inside shard k's weight (the same for every lane)
-      if (!in_bounds(local >= 0 && v < p.shard_end[k] && v < p.vocab_real, p.err)) {
-        if (lane == 0) zs[i] = 0.f;
-        continue;
-      }
-      const uint4* wrow = reinterpret_cast<const uint4*>(p.W[k]) + size_t(local) * size_t(nvec);
-      const float dot = warp_dot(wrow, xs, nvec, lane);
-      if (lane == 0) {
-        const float b = p.bias[k] != nullptr ? __bfloat162float(p.bias[k][local]) : 0.f;
-        zs[i] = __fmul_rn(__fadd_rn(dot, b), p.inv_tau);
-      }
-    }
-  } else {
-    // 3. gather of the reused logits, temperature applied here (once)
-    if (tid < n) {
-      const int64_t v = uniq[tid];
       const int k = shard_of(p, v);
       const int64_t col = v - p.shard_start[k];
       const bool ok = in_bounds(col >= 0 && v < p.shard_end[k] && col < p.ld[k] && v < p.vocab_real, p.err);
       const float l = ok ? __bfloat162float(p.logits[k][size_t(row) * size_t(p.ld[k]) + size_t(col)]) : 0.f;
-      zs[tid] = __fmul_rn(l, p.inv_tau);
+      zs[i] = __fmul_rn(l, p.inv_tau);
     }
   }
-  __syncthreads();
-
-  // 4. fold (warp 0), shard by shard: the shard's ids are a contiguous run [i0, i1) of the
-  // ascending list; lane l takes its ids i0 + 2l and i0 + 2l + 1, the lanes' statistics
-  // combine by a fixed shuffle tree, and the shards are reduced in ascending order by
-  // row_finish - an order fixed by the shard's own ids alone, so a rank-local call that
-  // holds only some of the shards folds each of them exactly as a call holding all does
-  if (warp == 0) {
-    const int yv = __ldg(p.y + row);
-    const bool y_ok = yv >= 0 && int64_t(yv) < p.vocab_real;
-    if (lane == 0 && !y_ok) record_error(p.err, LP_ERR_TARGET_OUT_OF_RANGE);
-    const int64_t id0 = 2 * lane < n ? int64_t(uniq[2 * lane]) : INT64_MAX;
-    const int64_t id1 = 2 * lane + 1 < n ? int64_t(uniq[2 * lane + 1]) : INT64_MAX;
-    // the target logit, if y is in the set: the lane holding it says which of its two ids
-    const bool own0 = y_ok && id0 == yv, own1 = y_ok && id1 == yv;
-    const unsigned tb = __ballot_sync(0xffffffffu, own0 || own1);
-    const bool t_found = tb != 0u;
-    const int src = t_found ? __ffs(tb) - 1 : 0;
-    const int t_idx = 2 * src + __shfl_sync(0xffffffffu, own0 ? 0 : 1, src);
-    const float t_val = t_found ? zs[t_idx] : 0.f;
-    int owner = -1;
-    float lse[LP_MAX_SHARDS], hz[LP_MAX_SHARDS], t[LP_MAX_SHARDS];
-#pragma unroll
-    for (int k = 0; k < LP_MAX_SHARDS; ++k) {
-      lse[k] = -INFINITY;
-      hz[k] = 0.f;
-      t[k] = 0.f;
-      if (k < p.n_shards) {
-        const int64_t s0 = p.shard_start[k], s1 = p.shard_end[k];
-        const int i0 = __popc(__ballot_sync(0xffffffffu, id0 < s0)) + __popc(__ballot_sync(0xffffffffu, id1 < s0));
-        const int i1 = __popc(__ballot_sync(0xffffffffu, id0 < s1)) + __popc(__ballot_sync(0xffffffffu, id1 < s1));
-        Stat loc = stat_empty();
-        if (i1 > i0) {
-          const int j0 = i0 + 2 * lane, j1 = j0 + 1;
-          if (j0 < i1) stat_push(loc, __fmul_rn(zs[j0], kLog2e));
-          if (j1 < i1) stat_push(loc, __fmul_rn(zs[j1], kLog2e));
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            const Stat o{__shfl_down_sync(0xffffffffu, loc.m, off), __shfl_down_sync(0xffffffffu, loc.s, off),
-                         __shfl_down_sync(0xffffffffu, loc.a, off)};
-            if (lane < off) stat_merge(loc, o);
-          }
-        }
-        lse[k] = stat_lse(loc);
-        if (y_ok && yv >= s0 && yv < s1) {
-          owner = k;
-          // the target's logit over the support: z_y if kept, -inf if the shard keeps
-          // other ids but not y (an excluded id), 0 if the shard keeps none (empty shard)
-          t[k] = t_found ? t_val : (i1 > i0 ? -INFINITY : 0.f);
-        }
-      }
-    }
-    if (lane == 0) {
-      if (p.shard_stats != nullptr) {
-#pragma unroll
-        for (int k = 0; k < LP_MAX_SHARDS; ++k) {
-          if (k < p.n_shards) {
-            float* ss = p.shard_stats + size_t(k) * 3 * T;
-            ss[row] = bad_row ? -INFINITY : lse[k];
-            ss[T + row] = bad_row ? 0.f : t[k];
-            ss[2 * T + row] = 0.f;
-          }
-        }
-      }
-      const RowOut o = row_finish(lse, hz, t, p.n_shards, owner);
-      p.lse[row] = bad_row ? -INFINITY : o.lse;
-      p.logp[row] = bad_row ? -INFINITY : o.logp;
-    }
-  }
+  __syncwarp();
+  fold_row(p, row, lane, uniq, zs, n);
 }
 
 // Dense keep-mask route: one CTA (256 threads) per row scans the masks of all shards
@@ -330,18 +356,17 @@ cudaError_t launch_replay(const ReplayParams& p, cudaStream_t s) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!ready[dev].load(std::memory_order_acquire)) {
-      cudaError_t e =
-          cudaFuncSetAttribute(replay_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536 / 8 * 16);
+      cudaError_t e = cudaFuncSetAttribute(replay_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536 / 8 * 16);
       if (e != cudaSuccess) return e;
       ready[dev].store(true, std::memory_order_release);
     }
   }
-  replay_kernel<false><<<p.T, kReplayThreads, smem, s>>>(p);
+  replay_kernel<<<p.T, kReplayThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_replay_from_logits(const ReplayParams& p, cudaStream_t s) {
-  replay_kernel<true><<<p.T, kReplayThreads, 0, s>>>(p);
+  replay_logits_kernel<<<(p.T + kReplayWarps - 1) / kReplayWarps, kReplayThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
