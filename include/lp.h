@@ -172,6 +172,10 @@ LP_API lp_status lp_forward(const void* X, int64_t T, int64_t H,
  * asynchronously: the host buffers hold the results once the stream has been
  * synchronised, and must stay valid until then. Page-locked host buffers make the copies
  * truly asynchronous; pageable ones also work. Results are bitwise those of lp_forward.
+ * Batches of T >= 4096 rows run as two halves whose second half is copied in on an
+ * auxiliary stream while the first half computes (a row's bits do not depend on its
+ * batch); the first such call on a device creates that stream and three events, kept
+ * until the process exits (make it before any stream capture).
  * Workspace: lp_workspace_size(LP_OP_FORWARD_HOST, T, H, part) bytes of device memory. */
 LP_API lp_status lp_forward_host(const void* X_host, int64_t T, int64_t H,
                                  const void* const* W, const void* const* bias,

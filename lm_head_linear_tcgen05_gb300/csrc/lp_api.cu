@@ -50,6 +50,10 @@ struct DeviceState {
   bool supported = false;
   int num_sms = 0;
   unsigned int* err = nullptr;
+  // lp_forward_host's copy stream and its three events, created on its first call
+  bool copy_init = false;
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
 };
 
 std::mutex g_mu;
@@ -98,6 +102,25 @@ lp_status device_state(DeviceState** out) {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   *out = &st;
+  return LP_OK;
+}
+
+// The copy stream of lp_forward_host on the current device (created once, with that
+// device current): a non-blocking stream and three events without timing.
+lp_status device_copy_stream(DeviceState* st) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!st->copy_init) {
+    if (cudaStreamCreateWithFlags(&st->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaGetLastError();
+      return LP_ERR_CUDA;
+    }
+    for (auto& e : st->ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return LP_ERR_CUDA;
+      }
+    st->copy_init = true;
+  }
   return LP_OK;
 }
 
@@ -160,6 +183,9 @@ lp_status check_partition(const lp_vocab_partition* part, Shards* sh) {
 bool valid_rows(int64_t T) { return T >= 0 && T <= (int64_t(1) << 30); }
 bool valid_hidden(int64_t H) { return H >= 8 && H <= 65536 && H % 8 == 0; }
 bool valid_tau(float tau) { return std::isfinite(tau) && tau > 0.f; }
+
+// lp_forward_host splits batches of at least this many rows in two halves
+constexpr int64_t kHostSplitRows = 4096;
 
 size_t forward_ws_bytes(int64_t T, const Shards& sh) {
   int64_t nb = 0;
@@ -348,35 +374,70 @@ lp_status lp_forward_host(const void* X_host, int64_t T, int64_t H, const void* 
   if (workspace == nullptr || ws_bytes < L.total) return LP_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return LP_ERR_ALIGNMENT;
   DeviceState* dev = nullptr;
-  const lp_status dst = device_state(&dev);
+  lp_status dst = device_state(&dev);
   if (dst != LP_OK) return dst;
+  // Large batches run as two halves (rows split at a multiple of 256): the second half's
+  // rows cross the host link on the copy stream while the first half's GEMM runs. A
+  // row's bits do not depend on the batch it is computed in, so the results are those of
+  // one call over all rows.
+  const int64_t T0 = T >= kHostSplitRows ? (T / 2 + 255) / 256 * 256 : T;
+  const int nparts = T0 < T ? 2 : 1;
+  if (nparts == 2 && (dst = device_copy_stream(dev)) != LP_OK) return dst;
   char* ws = static_cast<char*>(workspace);
-  void* dX = ws + L.off_x;
+  char* dX = ws + L.off_x;
   int32_t* dy = reinterpret_cast<int32_t*>(ws + L.off_y);
-  lp_outputs dout;
-  dout.logp = reinterpret_cast<float*>(ws + L.off_logp);
-  dout.lse = reinterpret_cast<float*>(ws + L.off_lse);
-  dout.entropy = out_host->entropy != nullptr ? reinterpret_cast<float*>(ws + L.off_ent) : nullptr;
-  dout.shard_stats = out_host->shard_stats != nullptr ? reinterpret_cast<float*>(ws + L.off_ss) : nullptr;
-  // lp_forward validates everything else (W, bias, device) before it launches anything,
-  // so a rejected call has enqueued at most the two input copies
+  float* d_logp = reinterpret_cast<float*>(ws + L.off_logp);
+  float* d_lse = reinterpret_cast<float*>(ws + L.off_lse);
+  float* d_ent = out_host->entropy != nullptr ? reinterpret_cast<float*>(ws + L.off_ent) : nullptr;
+  float* d_ss = out_host->shard_stats != nullptr ? reinterpret_cast<float*>(ws + L.off_ss) : nullptr;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t tb = size_t(T) * 4;
-  if (cudaMemcpyAsync(dX, X_host, size_t(T) * size_t(H) * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(dy, y_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+  cudaStream_t cs = nparts == 2 ? dev->copy_stream : s;
+  const size_t row_x = size_t(H) * 2;
+  auto fail = [] {
     cudaGetLastError();
     return LP_ERR_CUDA;
+  };
+  // copies: on the caller's stream (one part), or on the copy stream after the caller's
+  // earlier work (which may still use the staging), one event per part
+  if (nparts == 2 && (cudaEventRecord(dev->ev[0], s) != cudaSuccess || cudaStreamWaitEvent(cs, dev->ev[0], 0) != cudaSuccess))
+    return fail();
+  for (int c = 0; c < nparts; ++c) {
+    const int64_t r0 = c == 0 ? 0 : T0, rows = (c == 0 ? T0 : T) - r0;
+    if (cudaMemcpyAsync(dX + size_t(r0) * row_x, static_cast<const char*>(X_host) + size_t(r0) * row_x,
+                        size_t(rows) * row_x, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dy + r0, y_host + r0, size_t(rows) * 4, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+      return fail();
+    if (nparts == 2 && cudaEventRecord(dev->ev[1 + c], cs) != cudaSuccess) return fail();
   }
-  const lp_status st = lp_forward(dX, T, H, W, bias, part, dy, tau, &dout, ws, forward_ws_bytes(T, sh), stream);
-  if (st != LP_OK) return st;
-  if (cudaMemcpyAsync(out_host->logp, dout.logp, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(out_host->lse, dout.lse, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      (dout.entropy != nullptr &&
-       cudaMemcpyAsync(out_host->entropy, dout.entropy, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
-      (dout.shard_stats != nullptr && cudaMemcpyAsync(out_host->shard_stats, dout.shard_stats, size_t(sh.n) * 3 * tb,
-                                                      cudaMemcpyDeviceToHost, s) != cudaSuccess)) {
-    cudaGetLastError();
-    return LP_ERR_CUDA;
+  // the forward of each part on the caller's stream, once its rows have arrived. lp_forward
+  // validates W, bias and the device before it launches anything, so a rejected call has
+  // enqueued at most the input copies.
+  const size_t fws = forward_ws_bytes(T0, sh);
+  for (int c = 0; c < nparts; ++c) {
+    const int64_t r0 = c == 0 ? 0 : T0, rows = (c == 0 ? T0 : T) - r0;
+    if (nparts == 2 && cudaStreamWaitEvent(s, dev->ev[1 + c], 0) != cudaSuccess) return fail();
+    lp_outputs o;
+    o.logp = d_logp + r0;
+    o.lse = d_lse + r0;
+    o.entropy = d_ent != nullptr ? d_ent + r0 : nullptr;
+    o.shard_stats = d_ss != nullptr ? d_ss + size_t(sh.n) * 3 * size_t(r0) : nullptr;  // [K][3][rows] per part
+    const lp_status st = lp_forward(dX + size_t(r0) * row_x, rows, H, W, bias, part, dy + r0, tau, &o, ws, fws, stream);
+    if (st != LP_OK) return st;
+  }
+  // outputs back on the caller's stream
+  const size_t tb = size_t(T) * 4;
+  if (cudaMemcpyAsync(out_host->logp, d_logp, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(out_host->lse, d_lse, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      (d_ent != nullptr && cudaMemcpyAsync(out_host->entropy, d_ent, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess))
+    return fail();
+  if (d_ss != nullptr) {
+    // part c's statistics are [K * 3][rows_c] rows of floats; host rows are T floats apart
+    for (int c = 0; c < nparts; ++c) {
+      const int64_t r0 = c == 0 ? 0 : T0, rows = (c == 0 ? T0 : T) - r0;
+      if (cudaMemcpy2DAsync(out_host->shard_stats + r0, tb, d_ss + size_t(sh.n) * 3 * size_t(r0), size_t(rows) * 4,
+                            size_t(rows) * 4, size_t(sh.n) * 3, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return fail();
+    }
   }
   return LP_OK;
 }

@@ -1,6 +1,8 @@
 """lp_forward_host (the C entry point on host-resident rows): its results are bitwise those
 of lp_forward on device-resident inputs, with page-locked or pageable host buffers, with
-every optional output, with reused workspace and output buffers, and for an empty batch."""
+every optional output, with reused workspace and output buffers, for an empty batch, and
+for batches of 4096 rows and more, which run as two halves whose second half is copied in
+on another stream while the first computes (ragged halves included)."""
 import numpy as np
 import pytest
 
@@ -21,7 +23,8 @@ def lp():
     return mod
 
 
-@pytest.mark.parametrize("T,pinned", [(3000, True), (700, False), (64, True)])
+@pytest.mark.parametrize("T,pinned", [(3000, True), (700, False), (64, True), (4096, True), (5001, True),
+                                      (4099, False)])
 def test_host_forward_is_bitwise_the_device_forward(lp, T, pinned):
     import torch
     part = synth.ranges_partition(5000, 5120, [0, 2560, 2560, 5120])     # an empty shard, padding
