@@ -503,8 +503,12 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
         wsb = torch.empty(lp.lp_workspace_size(lp.LP_OP_BACKWARD, T_FWD, H, P3), dtype=torch.uint8, device=dev)
         fwd = lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf)
         ms_f, clk_f = timed(lambda: lp.lp_forward(X, W, b, P3, y, TAU, workspace=wsf), args.steps)
+        bwd = lambda: lp.lp_backward(X, W, b, P3, y, TAU, fwd["lse"], g, workspace=wsb)
+        # a short burst first (5 calls, ~45 ms: the clock has not yet met the power cap), then
+        # the 20-call figure, long enough for the power cap to set the clock
+        ms_bb, clk_bb = timed(bwd, 5)
         bsteps = max(20, args.steps)
-        ms_b, clk_b = timed(lambda: lp.lp_backward(X, W, b, P3, y, TAU, fwd["lse"], g, workspace=wsb), bsteps)
+        ms_b, clk_b = timed(bwd, bsteps)
         f_fl = 2.0 * T_FWD * H * Vp
         b_tf = 3 * f_fl / (ms_b * 1e-3) / 1e12
         out["sharded_fwd_bwd"] = {
@@ -520,7 +524,10 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
             "bwd_roofline": {"bound": "tensor", "achieved": b_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                              "frac": b_tf / peaks["bf16_tflops"],
                              "frac_of_sustained": b_tf / peaks["bf16_tflops_sustained"],
-                             "flops_per_call": 3 * f_fl}}
+                             "flops_per_call": 3 * f_fl},
+            "bwd_burst": {"steps": 5, "ms": ms_bb, "clocks": clk_bb,
+                          "achieved": 3 * f_fl / (ms_bb * 1e-3) / 1e12,
+                          "frac": 3 * f_fl / (ms_bb * 1e-3) / 1e12 / peaks["bf16_tflops"]}}
     if lp.lp_get_device_error() != 0:
         raise RuntimeError("device error in the path timings")
     return out
