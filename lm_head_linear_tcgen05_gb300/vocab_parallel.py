@@ -19,9 +19,10 @@ exchange what the rank-ordered reduction needs:
             rank order -> lp_sum_partials adds them in that fixed order (never a
             reduction whose order can vary).
 
-This module only moves data (torch.distributed collectives) and calls the library; every
-arithmetic step runs in the library's kernels. Collectives work on any backend: NCCL for
-GPU tensors, gloo for the host-side tests of the exchange.
+`linear_logp` wraps forward and backward for autograd. This module only moves data
+(torch.distributed collectives) and calls the library; every arithmetic step runs in the
+library's kernels. Collectives work on any backend: NCCL for GPU tensors, gloo for the
+host-side tests of the exchange.
 """
 from __future__ import annotations
 
@@ -34,7 +35,7 @@ from . import (VocabPartition, lp_backward_ex, lp_forward, lp_forward_from_logit
                lp_sum_partials, lp_top_p_replay)
 
 __all__ = ["rank_partition", "gather_in_rank_order", "gather_shard_stats", "merge", "forward",
-           "forward_from_logits", "top_p_replay", "backward", "sum_over_ranks"]
+           "forward_from_logits", "top_p_replay", "backward", "sum_over_ranks", "linear_logp"]
 
 
 def rank_partition(full: VocabPartition, shard_ids: Sequence[int]) -> VocabPartition:
@@ -129,3 +130,56 @@ def backward(X: torch.Tensor, W_local, b_local, full: VocabPartition, shard_ids:
     dx_share = g["dX"]
     return {"dX": sum_over_ranks(dx_share, group, out_dtype=dx_dtype), "dW": g["dW"], "db": g["db"],
             "dX_local": dx_share}
+
+
+class _VocabParallelLogp(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, X, full, shard_ids, y, tau, group, n, has_bias, *wb):
+        W = list(wb[:n])
+        bias = list(wb[n:]) if has_bias else None
+        out = forward(X, W, bias, full, shard_ids, y, tau, group=group, entropy=True)
+        ctx.full, ctx.shard_ids, ctx.tau, ctx.group, ctx.n, ctx.has_bias = full, shard_ids, tau, group, n, has_bias
+        ctx.save_for_backward(X, y, out["lse"], out["entropy"], *wb)
+        ctx.mark_non_differentiable(out["lse"])
+        ctx.set_materialize_grads(False)
+        return out["logp"], out["entropy"], out["lse"]
+
+    @staticmethod
+    def backward(ctx, g_logp, g_entropy, _g_lse):
+        X, y, lse, entropy, *wb = ctx.saved_tensors
+        n = ctx.n
+        W = wb[:n]
+        bias = wb[n:] if ctx.has_bias else None
+        if g_logp is None and g_entropy is None:
+            return (None,) * (8 + len(wb))
+        g = g_logp.to(torch.float32).contiguous() if g_logp is not None else \
+            torch.zeros(X.shape[0], dtype=torch.float32, device=X.device)
+        h = g_entropy.to(torch.float32).contiguous() if g_entropy is not None else None
+        part = rank_partition(ctx.full, ctx.shard_ids)
+        want_db = bias is not None and any(b is not None and b.requires_grad for b in bias)
+        r = lp_backward_ex(X, W, bias, part, y, ctx.tau, lse, g, bias_grad=want_db,
+                           entropy=entropy if h is not None else None, grad_entropy=h,
+                           dw_dtype=torch.bfloat16)
+        # every rank's fp32 share of dX, added in rank order and rounded once to X's type
+        dX = sum_over_ranks(r["dX"], ctx.group, out_dtype=torch.bfloat16) if ctx.needs_input_grad[0] else None
+        dW = [d if ctx.needs_input_grad[8 + k] else None for k, d in enumerate(r["dW"])]
+        db = [None] * n
+        if want_db:
+            db = [d if ctx.needs_input_grad[8 + n + k] else None for k, d in enumerate(r["db"])]
+        return (dX, None, None, None, None, None, None, None, *dW, *(db if ctx.has_bias else []))
+
+
+def linear_logp(X: torch.Tensor, W_local, b_local, full: VocabPartition, shard_ids: Sequence[int],
+                y: torch.Tensor, tau: float, group=None):
+    """Vocabulary-parallel linear-logp with autograd, called by every rank of the group with
+    the same X, y and upstream gradients: returns (logp, entropy) of the whole vocabulary,
+    differentiable with respect to X (the rank-ordered sum of every rank's share, the same on
+    every rank) and this rank's W and bias (bf16 gradients)."""
+    ids = list(shard_ids)
+    n = len(ids)
+    if len(W_local) != n:
+        raise ValueError("W_local must have one entry per local shard")
+    wb = list(W_local) + (list(b_local) if b_local is not None else [])
+    logp, entropy, _ = _VocabParallelLogp.apply(X, full, tuple(ids), y, float(tau), group, n, b_local is not None,
+                                                *wb)
+    return logp, entropy
