@@ -134,3 +134,39 @@ def test_valid_calls_reach_the_device_check(lp, pt, T, H):
     assert L.lp_forward(A, T, H, Wa, None, ctypes.byref(cp), A, 0.7, ctypes.byref(out), A, need, None) == 3
     assert L.lp_forward(A, T, H, Wa, None, ctypes.byref(cp), A, 0.7, ctypes.byref(out), A, max(need, 1) - 1,
                         None) == (4 if need > 0 else 3)
+
+
+@st.composite
+def local_runs(draw):
+    """A valid partition and one tensor-parallel rank's consecutive run of its shards."""
+    vreal, vpad, bounds = draw(partitions())
+    n = len(bounds) - 1
+    k0 = draw(st.integers(0, n - 1))
+    k1 = draw(st.integers(k0 + 1, n))
+    return vreal, vpad, bounds, k0, k1
+
+
+@settings(max_examples=200, deadline=None)
+@given(lr=local_runs(), T=st.integers(0, 4000), mutate=st.sampled_from(["none", "hole", "past_end", "flag"]))
+def test_rank_local_partitions(lp, lr, T, mutate):
+    # a rank's run of shards, flagged local, is accepted and sized like those shards alone;
+    # a gap inside it, an end past vocab_padded or a flag other than 0 / 1 is rejected
+    vreal, vpad, bounds, k0, k1 = lr
+    ranges = [(bounds[i], bounds[i + 1]) for i in range(k0, k1)]
+    flag = 1
+    if mutate == "hole" and len(ranges) >= 2:
+        ranges[1] = (ranges[1][0] + 1, ranges[1][1] + 1)
+    elif mutate == "past_end":
+        ranges[-1] = (ranges[-1][0], vpad + 1)
+    elif mutate == "flag":
+        flag = 2
+    else:
+        mutate = "none"
+    cp, keep = _raw_partition(lp, vreal, vpad, ranges)
+    cp.local = flag
+    got = lp.lib().lp_workspace_size(lp.LP_OP_FORWARD, T, 256, ctypes.byref(cp))
+    if mutate != "none":
+        assert got == 0
+        return
+    nb = sum((max(min(e, vreal) - s, 0) + 255) // 256 for s, e in ranges)
+    assert got == 3 * _align(nb * T * 4) + _align(T * 4)
