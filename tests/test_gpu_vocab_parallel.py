@@ -109,6 +109,19 @@ def test_rank_local_forward_and_replay_merge_to_the_whole_call(lp, T, H, bounds,
     _same(lp.lp_merge_shard_stats(gathered, yld, P), full_l, ("logp", "lse", "entropy"))
     ref_l = oracle.forward_from_logits(L, part, yl, tau)
     assert max_abs(_np(full_l["entropy"]), ref_l.entropy) <= TOL_ENT
+    # the gradient with respect to the reused logits: each rank, given the merged LSE and
+    # entropy, writes its own shards' gradient, bitwise the whole call's
+    gl, hl = dev_f32(synth.upstream_grad(T, seed=T + 7)), dev_f32(synth.upstream_grad(T, seed=T + 8))
+    whole_g = lp.lp_backward_from_logits(Ld, P, yld, tau, full_l["lse"], gl, entropy=full_l["entropy"],
+                                         grad_entropy=hl, out_dtype=torch.float32)
+    for ks in ranks:
+        loc_g = lp.lp_backward_from_logits([Ld[k] for k in ks], _local(lp, part, ks), yld, tau, full_l["lse"], gl,
+                                           entropy=full_l["entropy"], grad_entropy=hl, out_dtype=torch.float32)
+        for j, k in enumerate(ks):
+            assert (loc_g[j] is None) == (whole_g[k] is None)
+            if whole_g[k] is not None:
+                assert torch.equal(loc_g[j], whole_g[k]), k
+    assert lp.lp_get_device_error() == 0
 
     # replay, all three routes; every rank gets every row's ids and skips the others' ones.
     # Some targets are made excluded ids (in a shard that keeps other ids, not in the set).

@@ -71,4 +71,17 @@ def test_single_rank_group_forward_and_autograd(lp, group):
     assert torch.equal(a[2], r[2])                        # dX: the one rank's share, rounded once
     for k in range(3):
         assert torch.equal(a[3][k], r[3][k]) and torch.equal(a[4][k], r[4][k])
+    # the logits-reuse and replay routes through the module
+    L, yl, tau = synth.logits_inputs(300, part, 0.7, seed=57)
+    from lp_util import dev_bf16, dev_i32
+    Ld = [dev_bf16(t) for t in L]
+    yld = dev_i32(yl)
+    ol = vp.forward_from_logits(Ld, P, [0, 1, 2], yld, tau, group=group)
+    wl = lp.lp_forward_from_logits(Ld, P, yld, tau)
+    for k in ("logp", "lse", "entropy"):
+        assert torch.equal(ol[k], wl[k]), k
+    ids, yr = synth.replay_ids(300, part, seed=58)
+    orp = vp.top_p_replay(X, W, b, P, [0, 1, 2], dev_i32(ids), dev_i32(yr), inp.tau, group=group)
+    wr = lp.lp_top_p_replay(X, W, b, P, dev_i32(ids), dev_i32(yr), inp.tau)
+    assert torch.equal(orp["logp"], wr["logp"]) and torch.equal(orp["lse"], wr["lse"])
     assert lp.lp_get_device_error() == 0
