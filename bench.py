@@ -5,10 +5,13 @@
 Headline (one JSON line on rank 0): the fused forward on the Qwen3-8B-shaped LM head,
 T=4096 rows, H=4096, V=151936 bf16, tau=0.7, logp + LSE + entropy, in tokens/s, with
 the tensor-core roofline of the fused GEMM kernel. The other hot-path rows are timed
-alongside in "paths": logits reuse (T=8192 x 151936 bf16 logits, HBM-bound) and the
-gradient with respect to those logits, compact top-p replay (T=8192, 4 shards), and the
-vocabulary-sharded forward + backward
-(T=4096, V=151936 padded to 152064 in 4 shards, bias).
+alongside in "paths": the tiny configuration (T=64, H=256, V=1000), logits reuse
+(T=8192 x 151936 bf16 logits, HBM-bound) and the gradient with respect to those logits,
+compact top-p replay (T=8192, 4 shards) from x.W and from the logits, and the
+vocabulary-sharded forward + backward (T=4096, V=151936 padded to 152064 in 4 shards,
+bias). Each leg carries its own clock record and roofline, and (unless --no-cpu-baseline)
+the fp64 oracle timed on a bounded row sample of the same workload with the GPU's largest
+deviation from it on those rows.
 
 Every input is synthetic and seeded; the weights and logits are larger than the
 129 MB L2, so no flush is needed between timed steps. --impl reference times the fp64
@@ -400,6 +403,43 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def _host_bits(t):
+    """A CUDA bf16 tensor's bits as a host uint16 array (oracle input)."""
+    import numpy as np
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _sample_rows(T: int, n: int):
+    import numpy as np
+    return np.unique(np.linspace(0, T - 1, min(n, T)).round().astype(np.int64))
+
+
+def _oracle_leg(run, rows: int, sample: str, compare):
+    """Time `run()` (an oracle call on a bounded row sample) on the host cores; compare(result)
+    returns the GPU outputs' largest deviations on those rows."""
+    t0 = time.perf_counter()
+    res = run()
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{sample}; {dt:.1f} s", "parity": compare(res)}
+
+
+def _maxdev(gpu, ref):
+    import numpy as np
+    a = np.asarray(gpu, dtype=np.float64)
+    b = np.asarray(ref, dtype=np.float64)
+    both = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
+    return float(np.max(np.abs(np.where(both, 0.0, a) - np.where(both, 0.0, b)))) if a.size else 0.0
+
+
+def _relfro(gpu, ref):
+    import numpy as np
+    a = np.asarray(gpu, dtype=np.float64)
+    b = np.asarray(ref, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
 def time_other_paths(args, lp, synth, dev, stream, peaks):
     """The other hot-path rows, each on its own workload (vocabulary args.vocab), each timed
     with its own clock record."""
@@ -423,6 +463,33 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
         return r
 
     wanted = set(args.paths.split(","))
+    oracle_on = not args.no_cpu_baseline
+    tau32 = float(__import__("numpy").float32(TAU))
+    if oracle_on:
+        import oracle
+    if "tiny" in wanted:
+        # the tiny configuration (T=64, H=256, V=1000, tau 1): launch-bound, timed from a graph
+        pt = synth.even_partition(1000, 1)
+        Pt = lp.VocabPartition(pt.vocab_real, pt.vocab_padded, pt.ranges)
+        inp = synth.forward_inputs(64, 256, pt, tau=1.0, seed=0)
+        import numpy as np
+        import torch
+        Xt = torch.from_numpy(inp.X.view(np.int16)).to(dev).view(torch.bfloat16)
+        Wt = [torch.from_numpy(inp.W[0].view(np.int16)).to(dev).view(torch.bfloat16)]
+        yt = torch.from_numpy(inp.y).to(dev)
+        clk_t = clock_sampler(dev)
+        ms = time_graph(lambda: lp.lp_forward(Xt, Wt, None, Pt, yt, inp.tau), args.steps, args.warmup, stream,
+                        sampler=clk_t)
+        leg = {"workload": "T=64, H=256, V=1000, one shard, no bias, tau=1.0", "ms": ms,
+               "tokens_per_s": 64 / (ms * 1e-3), "steps": args.steps, "clocks": clk_t.summary(),
+               "timed": "one CUDA graph of the timed calls (a call is launch-bound)"}
+        if oracle_on:
+            got = lp.lp_forward(Xt, Wt, None, Pt, yt, inp.tau)
+            leg["cpu_baseline"] = _oracle_leg(
+                lambda: oracle.forward(inp.X, inp.W, None, pt, inp.y, inp.tau), 64, "all 64 rows, fp64 numpy oracle",
+                lambda r: {"max_abs_dlogp": _maxdev(got["logp"].cpu(), r.logp),
+                           "max_abs_dentropy": _maxdev(got["entropy"].cpu(), r.entropy)})
+        out["tiny"] = leg
     if wanted & {"logits", "replay"}:
         part = synth.even_partition(Vp, 1)
         P = lp.VocabPartition(part.vocab_real, part.vocab_padded, part.ranges)
@@ -442,8 +509,19 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                 "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "steps": args.steps, "clocks": clk,
                 "roofline": hbm_roofline(nbytes, ms, "stream_logits",
                                          frac_of_8tbs=nbytes / (ms * 1e-3) / 1e9 / 8000.0)}
-            # its backward: the gradient with respect to those logits, bf16, out of place
             fl = lp.lp_forward_from_logits(L, P, y, TAU)
+            if oracle_on:
+                idx = _sample_rows(TP, 1024)
+                idx_d = torch.from_numpy(idx).to(dev)
+                Lb = [_host_bits(L[0][idx_d])]
+                ys = y[idx_d].cpu().numpy()
+                out["logits_reuse"]["cpu_baseline"] = _oracle_leg(
+                    lambda: oracle.forward_from_logits(Lb, part, ys, tau32), len(idx),
+                    f"{len(idx)} of {TP} rows (full V), fp64 numpy oracle",
+                    lambda r: {"max_abs_dlogp": _maxdev(fl["logp"][idx_d].cpu(), r.logp),
+                               "max_abs_dlse": _maxdev(fl["lse"][idx_d].cpu(), r.lse),
+                               "max_abs_dentropy": _maxdev(fl["entropy"][idx_d].cpu(), r.entropy)})
+            # its backward: the gradient with respect to those logits, bf16, out of place
             gl = torch.randn(TP, generator=torch.Generator(device=dev).manual_seed(4), device=dev)
             dL = [torch.empty_like(L[0])]
             ms, clk = timed(lambda: lp.lp_backward_from_logits(L, P, y, TAU, fl["lse"], gl, entropy=fl["entropy"],
@@ -452,6 +530,16 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                 "workload": f"gradient w.r.t. the T={TP} x V={Vp} logits above (logp + entropy terms), bf16 out",
                 "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "steps": args.steps, "clocks": clk,
                 "roofline": hbm_roofline(2 * TP * Vp * 2, ms, "logits_backward")}
+            if oracle_on:
+                idx = _sample_rows(TP, 256)
+                idx_d = torch.from_numpy(idx).to(dev)
+                Lb = [_host_bits(L[0][idx_d])]
+                ys, gs = y[idx_d].cpu().numpy(), gl[idx_d].cpu().numpy()
+                got = dL[0][idx_d].float().cpu().numpy()
+                out["logits_backward"]["cpu_baseline"] = _oracle_leg(
+                    lambda: oracle.backward_from_logits(Lb, part, ys, tau32, gs, h=gs), len(idx),
+                    f"{len(idx)} of {TP} rows (full V), fp64 numpy oracle",
+                    lambda r: {"rel_fro_dlogits": _relfro(got, r[0])})
             del dL, fl
         if "replay" in wanted:
             # the compact replay scored from the reused logits above: per row its 64 id slots
@@ -462,6 +550,16 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                             args.warmup, stream, sampler=clk_g)
             clk = clk_g.summary()
             sector_bytes = TP * (64 * 4 + 4) + uniq * 32
+            if oracle_on:
+                got = lp.lp_top_p_replay_from_logits(L4, P4, ids_d, yr_d, TAU)
+                idx = _sample_rows(TP, TP)
+                idx_d = torch.from_numpy(idx).to(dev)
+                L4b = [_host_bits(t[idx_d]) for t in L4]
+                replay_from_logits_cpu = _oracle_leg(
+                    lambda: oracle.top_p_replay_from_logits(L4b, part4, ids[idx], yr[idx], tau32), len(idx),
+                    f"{len(idx)} of {TP} rows, fp64 oracle (a Python loop over each row's ids)",
+                    lambda r: {"max_abs_dlogp": _maxdev(got["logp"][idx_d].cpu(), r.logp),
+                               "max_abs_dlse": _maxdev(got["lse"][idx_d].cpu(), r.lse)})
             out["top_p_replay_from_logits"] = {
                 "workload": f"T={TP} rows of the logits above in 4 shards, 1-64 ids/row",
                 "tokens_per_s": TP / (ms * 1e-3), "ms": ms, "steps": args.steps, "clocks": clk,
@@ -473,6 +571,8 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                                               "plus the id slots and targets); bound by the rate of scattered sector "
                                               "reads and each row's dependent steps (ids, sort, gather, fold), not "
                                               "by bandwidth")}
+            if oracle_on:
+                out["top_p_replay_from_logits"]["cpu_baseline"] = replay_from_logits_cpu
         del L
         torch.cuda.empty_cache()
         if "replay" in wanted:
@@ -488,6 +588,17 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                 "gathered_bytes": gathered, "distinct_bytes": distinct_b,
                 "roofline": hbm_roofline(gathered, ms, "replay",
                                          frac_distinct=distinct_b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"])}
+            if oracle_on:
+                got = lp.lp_top_p_replay(X, W, None, P4, ids_d, yr_d, TAU)
+                idx = _sample_rows(TP, 4096)
+                idx_d = torch.from_numpy(idx).to(dev)
+                Xb, Wb = _host_bits(X), [_host_bits(w) for w in W]
+                out["top_p_replay"]["cpu_baseline"] = _oracle_leg(
+                    lambda: oracle.top_p_replay(Xb, Wb, None, part4, ids, yr, tau32, rows=idx), len(idx),
+                    f"{len(idx)} of {TP} rows (full H), fp64 oracle (a Python loop over each row's ids)",
+                    lambda r: {"max_abs_dlogp": _maxdev(got["logp"][idx_d].cpu(), r.logp),
+                               "max_abs_dlse": _maxdev(got["lse"][idx_d].cpu(), r.lse)})
+                del Xb, Wb
             del X, W
             torch.cuda.empty_cache()
 
@@ -528,6 +639,26 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
             "bwd_burst": {"steps": 5, "ms": ms_bb, "clocks": clk_bb,
                           "achieved": 3 * f_fl / (ms_bb * 1e-3) / 1e12,
                           "frac": 3 * f_fl / (ms_bb * 1e-3) / 1e12 / peaks["bf16_tflops"]}}
+        if oracle_on:
+            import numpy as np
+            Xb, Wb, bb = _host_bits(X), [_host_bits(w) for w in W], [_host_bits(t) for t in b]
+            yb = y.cpu().numpy()
+            idx = _sample_rows(T_FWD, 256)
+            idx_d = torch.from_numpy(idx).to(dev)
+            out["sharded_fwd_bwd"]["fwd_cpu_baseline"] = _oracle_leg(
+                lambda: oracle.forward(Xb, Wb, bb, part3, yb, tau32, rows=idx), len(idx),
+                f"{len(idx)} of {T_FWD} rows (full H, V), fp64 numpy oracle",
+                lambda r: {"max_abs_dlogp": _maxdev(fwd["logp"][idx_d].cpu(), r.logp),
+                           "max_abs_dentropy": _maxdev(fwd["entropy"][idx_d].cpu(), r.entropy)})
+            bw_out = bwd()
+            dx_rows = _sample_rows(T_FWD, 64)
+            gb = g.cpu().numpy()
+            out["sharded_fwd_bwd"]["bwd_cpu_baseline"] = _oracle_leg(
+                lambda: oracle.backward_sampled(Xb, Wb, bb, part3, yb, tau32, gb, dx_rows,
+                                                [np.zeros(0, np.int64)] * 4), len(dx_rows),
+                f"dX of {len(dx_rows)} of {T_FWD} rows (full H, V), fp64 numpy oracle",
+                lambda r: {"rel_fro_dX": _relfro(bw_out["dX"][torch.from_numpy(dx_rows).to(dev)].cpu(), r[0])})
+            del Xb, Wb, bb, bw_out
     if lp.lp_get_device_error() != 0:
         raise RuntimeError("device error in the path timings")
     return out
@@ -614,8 +745,8 @@ def main(argv=None):
     ap.add_argument("--path-rows", type=int, default=8192,
                     help="rows of the logits-reuse and replay workloads (profiling of smaller cases)")
     ap.add_argument("--vocab", type=int, default=V, help="vocabulary V of every path (profiling of smaller cases)")
-    ap.add_argument("--paths", default="logits,replay,backward",
-                    help="comma list of the other paths to time: logits, replay, backward")
+    ap.add_argument("--paths", default="tiny,logits,replay,backward",
+                    help="comma list of the other paths to time: tiny, logits, replay, backward")
     ap.add_argument("--skip-headline", action="store_true", help="time only --paths (profiling)")
     ap.add_argument("--sustained-steps", type=int, default=200,
                     help="calls of the headline held long enough for the power cap to set the clock")
