@@ -385,6 +385,14 @@ LP_API lp_status lp_get_device_error(lp_stream_t stream);
  * result with lp_get_device_error(). Nothing hangs and nothing faults. */
 LP_API lp_status lp_selftest_wait_timeout(uint64_t limit_ns, lp_stream_t stream);
 
+/* The time limit of every pipeline wait of the GEMM kernels launched after this call, in
+ * nanoseconds (1 us .. 10 s; 0 restores the default of 2 s), for the whole process. A wait
+ * that runs past it gives up: the kernel records LP_ERR_DEVICE_TIMEOUT, lets the copies and
+ * MMAs it already started finish, frees its tensor memory and returns, leaving the context
+ * usable and the call's outputs undefined. Failure detection is tested by setting a limit
+ * too short for any wait to be met. Returns LP_ERR_INVALID_ARG outside the range. */
+LP_API lp_status lp_set_wait_limit(uint64_t limit_ns);
+
 /* 1 if this library was built with device-side bounds checks (LP_DEBUG_BOUNDS=1), else 0.
  * The compute sanitizer is not available on every machine; such a build stands in for its
  * out-of-bounds checks: every global index a kernel computes (from the grid, the partition,

@@ -64,7 +64,7 @@ EXPORTED = ("lp_workspace_size", "lp_forward", "lp_forward_noalloc", "lp_forward
             "lp_top_p_replay", "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask", "lp_backward",
             "lp_backward_ex", "lp_backward_from_logits", "lp_get_device_error", "lp_selftest_wait_timeout",
             "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported", "lp_status_string",
-            "lp_build_id", "lp_merge_shard_stats", "lp_sum_partials")
+            "lp_build_id", "lp_merge_shard_stats", "lp_sum_partials", "lp_set_wait_limit")
 
 
 class LPError(RuntimeError):
@@ -154,6 +154,7 @@ def lib() -> ctypes.CDLL:
     L.lp_sum_partials.argtypes = [P(vp), i32, i64, vp, ctypes.c_int, vp]
     L.lp_get_device_error.argtypes = [vp]
     L.lp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    L.lp_set_wait_limit.argtypes = [ctypes.c_uint64]
     L.lp_selftest_bounds.argtypes = [vp]
     L.lp_debug_bounds_build.argtypes = []
     L.lp_device_supported.argtypes = []
@@ -163,7 +164,7 @@ def lib() -> ctypes.CDLL:
                  "lp_top_p_replay_from_logits", "lp_top_p_replay_dense_mask",
                  "lp_backward", "lp_backward_ex", "lp_backward_from_logits", "lp_forward_host", "lp_get_device_error",
                  "lp_selftest_wait_timeout", "lp_selftest_bounds", "lp_debug_bounds_build", "lp_device_supported",
-                 "lp_merge_shard_stats", "lp_sum_partials"):
+                 "lp_merge_shard_stats", "lp_sum_partials", "lp_set_wait_limit"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -262,6 +263,11 @@ def lp_selftest_bounds(stream: Optional[int] = None) -> None:
     bounds-checked build, nothing in the regular one)."""
     s = _stream(torch.cuda.current_device()) if stream is None else stream
     _raise(lib().lp_selftest_bounds(s), "lp_selftest_bounds")
+
+
+def lp_set_wait_limit(limit_ns: int) -> None:
+    """Set the pipeline wait limit of later GEMM launches (ns; 0 restores the 2 s default)."""
+    _raise(lib().lp_set_wait_limit(int(limit_ns)), "lp_set_wait_limit")
 
 
 def lp_selftest_wait_timeout(limit_ns: int, stream: Optional[int] = None) -> None:

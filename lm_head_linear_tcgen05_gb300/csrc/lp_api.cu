@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -58,6 +59,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_wait_limit{kDefaultWaitLimitNs};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Resolves, once per device (with that device current), whether this library's
@@ -125,6 +127,8 @@ lp_status device_copy_stream(DeviceState* st) {
 }
 
 }  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 // bf16 row-major matrix [rows, inner] with row stride ld elements, boxes of
 // 64 (inner) x box_rows, 128-byte swizzle, out-of-bounds elements read as zero.
@@ -320,7 +324,7 @@ lp_status lp_forward(const void* X, int64_t T, int64_t H, const void* const* W, 
   p.m_chunk = proj_row_chunk(H, p.num_m_blocks);
   p.total_tiles = nb * p.num_m_blocks;
   p.err = dev->err;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.wait_limit_ns = wait_limit_ns();
   p.y = y;
   p.vocab_real = sh.vocab_real;
   p.scale_log2 = float(1.4426950408889634 / double(tau));
@@ -856,6 +860,13 @@ lp_status lp_selftest_bounds(lp_stream_t stream) {
   if (st != LP_OK) return st;
   bounds_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(int64_t(1), dev->err);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
+}
+
+lp_status lp_set_wait_limit(uint64_t limit_ns) {
+  if (limit_ns == 0) limit_ns = kDefaultWaitLimitNs;
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull) return LP_ERR_INVALID_ARG;
+  g_wait_limit.store(limit_ns, std::memory_order_relaxed);
+  return LP_OK;
 }
 
 lp_status lp_selftest_wait_timeout(uint64_t limit_ns, lp_stream_t stream) {

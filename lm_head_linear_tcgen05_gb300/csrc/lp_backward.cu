@@ -609,7 +609,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.m_chunk = proj_row_chunk(H, p.num_m_blocks);
     p.total_tiles = nb * p.num_m_blocks;
     p.err = a.err;
-    p.wait_limit_ns = kDefaultWaitLimitNs;
+    p.wait_limit_ns = wait_limit_ns();
     p.y = a.y;
     p.lse = a.lse;
     p.grad = a.grad;
@@ -651,7 +651,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.accumulate = a.accumulate;
     p.dw_bf16 = a.dw_bf16;
     p.err = a.err;
-    p.wait_limit_ns = kDefaultWaitLimitNs;
+    p.wait_limit_ns = wait_limit_ns();
     if (launch_tc_gemm<DwEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
     const size_t esz = a.dw_bf16 ? 2 : 4;
     for (int k = 0; k < sh.n && !a.accumulate; ++k) {
@@ -684,7 +684,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.out_bf16 = (splits == 1 && a.dx_bf16) ? static_cast<uint16_t*>(a.dX) : nullptr;
     p.total_tiles = p.num_m_blocks * p.num_n * splits;
     p.err = a.err;
-    p.wait_limit_ns = kDefaultWaitLimitNs;
+    p.wait_limit_ns = wait_limit_ns();
     if (launch_tc_gemm<DxEpi>(p, a.num_sms, s) != cudaSuccess) return LP_ERR_CUDA;
     if (splits > 1) {
       const size_t n4 = size_t(T) * size_t(H) / 4;

@@ -97,20 +97,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with the given parity to complete. Gives up (returns
 // false) when `*abort` is raised by another role or when `limit_ns` has elapsed; in
-// the latter case it raises `*abort` and records LP_ERR_DEVICE_TIMEOUT.
+// the latter case it raises `*abort` and records LP_ERR_DEVICE_TIMEOUT. Each try_wait may
+// suspend the thread for a while in hardware, so the flag and the clock are checked after
+// every unsuccessful try: the limit holds to within one suspension.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns, unsigned int* err) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t n = 1;; ++n) {
+  for (;;) {
     if (mbar_test(bar, parity)) return true;
-    if ((n & 31u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        *abort = 1;
-        record_error(err, LP_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      record_error(err, LP_ERR_DEVICE_TIMEOUT);
+      return false;
     }
   }
 }
@@ -133,25 +133,27 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
                                                   uint64_t limit_ns, unsigned int* err) {
   if (mbar_test_cluster(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t n = 1;; ++n) {
+  for (;;) {
     if (mbar_test_cluster(bar, parity)) return true;
-    if ((n & 31u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        *abort = 1;
-        record_error(err, LP_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      record_error(err, LP_ERR_DEVICE_TIMEOUT);
+      return false;
     }
   }
 }
 
-// Bounded wait used on teardown paths: ignores the abort flag, still time-limited.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
+// Bounded wait used on teardown paths: ignores the abort flag, gives up at `deadline`
+// (global timer, ns).
+__device__ __forceinline__ void drain_until(uint64_t* bar, uint32_t parity, uint64_t deadline) {
   while (!mbar_test(bar, parity)) {
-    if (global_timer_ns() - t0 > limit_ns) break;
+    if (global_timer_ns() > deadline) break;
   }
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  drain_until(bar, parity, global_timer_ns() + limit_ns);
 }
 
 // -------------------------------------------------------------------- TMA

@@ -37,7 +37,13 @@ struct Shards {
 // ------------------------------------------------------------- fused forward
 // Tensor-map slots of the GEMM kernels: maps[0] is the row operand (X, or G / G^T
 // in the backward), maps[1 + k] the operand of shard k.
-constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait (lp_set_wait_limit)
+// Teardown after a wait gave up: the time a CTA allows its own copies and MMAs already in
+// flight to finish. Those always finish, so this is generous and independent of the limit.
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
+// The pipeline wait limit every launch carries (lp_set_wait_limit; kDefaultWaitLimitNs).
+uint64_t wait_limit_ns();
 
 struct FwdParams {
   CUtensorMap maps[LP_MAX_SHARDS + 1];  // [0] X [T, H]; [1 + k] W_k [V_k, H]; 128B swizzle

@@ -26,10 +26,11 @@
 // warps of the pair release an accumulator on the even CTA's barrier.
 //
 // Every mbarrier wait is bounded in time (see lp_device.cuh): a wait that runs past
-// the limit records LP_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag and every
-// role leaves its loop; the producer then waits (bounded) for its copies in flight,
-// the MMA thread for its MMAs, a cluster barrier keeps both CTAs of a pair alive until
-// neither can touch the other, and TMEM is freed before the CTA exits.
+// the limit (p.wait_limit_ns) records LP_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag
+// and every role leaves its loop; the producer then waits for its copies in flight and the
+// MMA thread for its MMAs (up to kDrainLimitNs, whatever the limit), a cluster barrier keeps
+// both CTAs of a pair alive until neither can touch the other, and TMEM is freed before the
+// CTA exits.
 //
 // An epilogue type E derives from GemmEpiBase and provides
 //   static constexpr int kClusterM;       1, or 2 for the CTA pairs above
@@ -258,8 +259,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         // armed copies; the other CTA cannot observe its own, and gives any copy still in
         // flight (a few microseconds at most) time to land before the CTAs leave
         if (leader) {
+          const uint64_t deadline = global_timer_ns() + kDrainLimitNs;
           for (int s = 0; s < kStages; ++s)
-            if (armed & (1u << s)) drain_wait(&sync->full[s], (armed_phase >> s) & 1u, p.wait_limit_ns);
+            if (armed & (1u << s)) drain_until(&sync->full[s], (armed_phase >> s) & 1u, deadline);
         } else {
           const uint64_t t0 = global_timer_ns();
           while (global_timer_ns() - t0 < 100000ull) {
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         }
       }
       umma_commit<kCG>(&sync->done);
-      drain_wait(&sync->done, 0, p.wait_limit_ns);
+      drain_wait(&sync->done, 0, kDrainLimitNs);
     }
   } else {
     // -------------------------------------------------------------- epilogue

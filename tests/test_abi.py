@@ -61,6 +61,13 @@ def test_build_provenance(lp):
     assert _build.source_hash(debug_bounds=True) != _build.source_hash()
 
 
+def test_wait_limit_range(lp):
+    L = lp.lib()
+    assert L.lp_set_wait_limit(999) == 1 and L.lp_set_wait_limit(10_000_000_001) == 1
+    assert L.lp_set_wait_limit(1000) == 0 and L.lp_set_wait_limit(10_000_000_000) == 0
+    assert L.lp_set_wait_limit(0) == 0                   # the 2 s default again
+
+
 def test_status_strings(lp):
     for code, name in lp.STATUS_NAMES.items():
         assert lp.lp_status_string(code).startswith(name)
