@@ -123,6 +123,14 @@ __device__ __forceinline__ void st_global_bf16(__nv_bfloat16* p, float v, uint64
 #endif
 }
 
+// r[i] for a run-time i in [0, 32) without indexing the register array
+__device__ __forceinline__ float reg_pick(const uint32_t (&r)[32], int i) {
+  float v = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v = j == i ? __uint_as_float(r[j]) : v;
+  return v;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&b);
@@ -287,27 +295,65 @@ struct GradEpi : GemmEpiBase {
     const int64_t col_base = p.coff[c.shard] + n0;
     uint16_t* grow = p.G + size_t(in_rows ? row : 0) * size_t(p.Vc) + size_t(col_base);
     float* dbrow = p.dbp != nullptr ? p.dbp + (size_t(c.mb) * 4 + size_t(q)) * size_t(p.Vc) + size_t(col_base) : nullptr;
+    // the bias of column 32 ch + j sits in lane j; the next chunk's is fetched while this
+    // chunk is formed
+    auto bias_of = [&](int ch) {
+      return (bias != nullptr && ch * 32 + lane < valid) ? __bfloat162float(bias[n0 + ch * 32 + lane]) : 0.f;
+    };
+    float bl_next = bias_of(0);
 #pragma unroll 1
     for (int ch = 0; ch < kGemmBlockN / 32; ++ch) {
       if (ch * 32 >= wlim) break;
-      float bl = 0.f;
-      if (bias != nullptr && ch * 32 + lane < valid) bl = __bfloat162float(bias[n0 + ch * 32 + lane]);
+      const float bl = bl_next;
+      if (ch + 1 < kGemmBlockN / 32) bl_next = bias_of(ch + 1);
       float gv[32];
       if (ch * 32 < valid) {
         uint32_t r[32];
         tmem_ld32(tbase + ch * 32, r);
+        if (p.grad_entropy == nullptr) {
+          // logp term only. Every column first takes the non-target value g (0 - p) / tau
+          // (the same two roundings as the general form below, so the bits agree with it);
+          // the lane whose target falls in this chunk then replaces that one column.
+          if (bias != nullptr) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = ch * 32 + j;
-          const float v = __fadd_rn(f32(r[j]), __shfl_sync(0xffffffffu, bl, j));
-          const float pr = hw_ex2(__fmaf_rn(v, p.scale_log2, -lse2));
-          const float oh = (int64_t(col) == ycol) ? 1.f : 0.f;
-          // logp term g (1[v = y] - p) / tau, entropy term - h p (z - mu) / tau
-          float gval = __fmul_rn(gi, __fsub_rn(oh, pr));
-          // (p = 0 adds nothing; skipping it keeps a -inf-biased id from forming 0 * -inf)
-          if (hi != 0.f && pr != 0.f)
-            gval = __fsub_rn(gval, __fmul_rn(__fmul_rn(hi, pr), __fsub_rn(__fmul_rn(v, p.inv_tau), mu)));
-          gv[j] = (col < valid && live) ? gval : 0.f;
+            for (int j = 0; j < 32; ++j) {
+              const float v = __fadd_rn(f32(r[j]), __shfl_sync(0xffffffffu, bl, j));
+              gv[j] = __fmul_rn(gi, __fsub_rn(0.f, hw_ex2(__fmaf_rn(v, p.scale_log2, -lse2))));
+            }
+          } else {  // acc + 0 differs from acc only in the sign of a zero, which 2^d ignores
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              gv[j] = __fmul_rn(gi, __fsub_rn(0.f, hw_ex2(__fmaf_rn(f32(r[j]), p.scale_log2, -lse2))));
+          }
+          // (a target in a later shard can fall past `valid` of this shard's last block;
+          // that column is masked below and its bias is not read)
+          const int64_t tc = ycol - ch * 32;
+          if (tc >= 0 && tc < 32 && ch * 32 + tc < valid) {
+            const int t = int(tc);
+            const float b = bias != nullptr ? __bfloat162float(bias[n0 + ch * 32 + t]) : 0.f;
+            const float pr = hw_ex2(__fmaf_rn(__fadd_rn(reg_pick(r, t), b), p.scale_log2, -lse2));
+            const float gt = __fmul_rn(gi, __fsub_rn(1.f, pr));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) gv[j] = j == t ? gt : gv[j];
+          }
+          if (!live || ch * 32 + 32 > valid) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) gv[j] = (live && ch * 32 + j < valid) ? gv[j] : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = ch * 32 + j;
+            const float v = __fadd_rn(f32(r[j]), __shfl_sync(0xffffffffu, bl, j));
+            const float pr = hw_ex2(__fmaf_rn(v, p.scale_log2, -lse2));
+            const float oh = (int64_t(col) == ycol) ? 1.f : 0.f;
+            // logp term g (1[v = y] - p) / tau, entropy term - h p (z - mu) / tau
+            float gval = __fmul_rn(gi, __fsub_rn(oh, pr));
+            // (p = 0 adds nothing; skipping it keeps a -inf-biased id from forming 0 * -inf)
+            if (hi != 0.f && pr != 0.f)
+              gval = __fsub_rn(gval, __fmul_rn(__fmul_rn(hi, pr), __fsub_rn(__fmul_rn(v, p.inv_tau), mu)));
+            gv[j] = (col < valid && live) ? gval : 0.f;
+          }
         }
       } else {
 #pragma unroll
