@@ -5,7 +5,8 @@
 Headline (one JSON line on rank 0): the fused forward on the Qwen3-8B-shaped LM head,
 T=4096 rows, H=4096, V=151936 bf16, tau=0.7, logp + LSE + entropy, in tokens/s, with
 the tensor-core roofline of the fused GEMM kernel. The other hot-path rows are timed
-alongside in "paths": the tiny configuration (T=64, H=256, V=1000), logits reuse
+alongside in "paths": the tiny configuration (T=64, H=256, V=1000), the headline's shapes
+at micro-batch sizes (T=512 and 1024), logits reuse
 (T=8192 x 151936 bf16 logits, HBM-bound) and the gradient with respect to those logits,
 compact top-p replay (T=8192, 4 shards) from x.W and from the logits, and the
 vocabulary-sharded forward + backward (T=4096, V=151936 padded to 152064 in 4 shards,
@@ -490,6 +491,43 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                 lambda r: {"max_abs_dlogp": _maxdev(got["logp"].cpu(), r.logp),
                            "max_abs_dentropy": _maxdev(got["entropy"].cpu(), r.entropy)})
         out["tiny"] = leg
+    if "batches" in wanted:
+        # the headline workload at micro-batch sizes (T = 512, 1024 rows of the same X, W): one
+        # read of W (1.245 GB) is spread over fewer rows, so the call is bound by the tensor
+        # pipe or by streaming W, whichever is slower; both fractions are reported
+        pb = synth.even_partition(Vp, 1)
+        Pb = lp.VocabPartition(pb.vocab_real, pb.vocab_padded, pb.ranges)
+        Xb, Wb, _, yb = synth.device_forward_inputs(1024, H, pb, TAU, dev, seed=6)
+        w_bytes = float(sum(w.numel() * 2 for w in Wb))
+        legs = {}
+        for T in (512, 1024):
+            Xt, yt = Xb[:T].contiguous(), yb[:T].contiguous()
+            wst = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD, T, H, Pb), dtype=torch.uint8, device=dev)
+            ms, clk = timed(lambda: lp.lp_forward(Xt, Wb, None, Pb, yt, TAU, workspace=wst), args.steps)
+            tf = 2.0 * T * H * Vp / (ms * 1e-3) / 1e12
+            w_gbs = (w_bytes + Xt.numel() * 2) / (ms * 1e-3) / 1e9
+            leg = {"ms": ms, "tokens_per_s": T / (ms * 1e-3), "steps": args.steps, "clocks": clk,
+                   "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": tf / peaks["bf16_tflops"],
+                                "w_stream_gbs": w_gbs, "w_stream_frac": w_gbs / peaks["hbm_gbs"]}}
+            if oracle_on:
+                import numpy as np
+                got = lp.lp_forward(Xt, Wb, None, Pb, yt, TAU, workspace=wst)
+                idx = _sample_rows(T, 64)
+                idx_d = torch.from_numpy(idx).to(dev)
+                Xh, Wh, yh = _host_bits(Xt[idx_d]), [_host_bits(w) for w in Wb], yt[idx_d].cpu().numpy()
+                leg["cpu_baseline"] = _oracle_leg(
+                    lambda: oracle.forward(Xh, Wh, None, pb, yh, tau32), len(idx),
+                    f"{len(idx)} of {T} rows (full H, V), fp64 numpy oracle",
+                    lambda r: {"max_abs_dlogp": _maxdev(got["logp"][idx_d].cpu(), r.logp),
+                               "max_abs_dentropy": _maxdev(got["entropy"][idx_d].cpu(), r.entropy)})
+                del Wh
+            legs[f"T{T}"] = leg
+        out["fused_forward_batches"] = {
+            "workload": f"T=512 and 1024 rows, H=4096, V={Vp}, tau=0.7, no bias (the headline's shapes at "
+                        "micro-batch sizes)", **legs}
+        del Xb, Wb
+        torch.cuda.empty_cache()
     if wanted & {"logits", "replay"}:
         part = synth.even_partition(Vp, 1)
         P = lp.VocabPartition(part.vocab_real, part.vocab_padded, part.ranges)
@@ -745,8 +783,8 @@ def main(argv=None):
     ap.add_argument("--path-rows", type=int, default=8192,
                     help="rows of the logits-reuse and replay workloads (profiling of smaller cases)")
     ap.add_argument("--vocab", type=int, default=V, help="vocabulary V of every path (profiling of smaller cases)")
-    ap.add_argument("--paths", default="tiny,logits,replay,backward",
-                    help="comma list of the other paths to time: tiny, logits, replay, backward")
+    ap.add_argument("--paths", default="tiny,batches,logits,replay,backward",
+                    help="comma list of the other paths to time: tiny, batches, logits, replay, backward")
     ap.add_argument("--skip-headline", action="store_true", help="time only --paths (profiling)")
     ap.add_argument("--sustained-steps", type=int, default=200,
                     help="calls of the headline held long enough for the power cap to set the clock")
