@@ -1,6 +1,6 @@
 """Seeded random sweep: small configurations drawn at random (rows, hidden size, shard
-layout with empty and all-padding shards, bias on/off, temperature) through every entry
-point, each compared with the fp64 oracle; the option and host entry points are checked
+layout with empty and all-padding shards, bias on/off, temperature), and a few fixed tiny
+shapes, through every entry point, each compared with the fp64 oracle; the option and host entry points are checked
 bit for bit against their plain counterparts on the same configurations."""
 import numpy as np
 import pytest
@@ -44,8 +44,23 @@ def _random_case(seed):
 
 @pytest.mark.parametrize("seed", range(24))
 def test_random_configuration_all_entry_points(lp, seed):
+    _check_all_entry_points(lp, *_random_case(seed), seed=seed)
+
+
+# a few rows, H = 16 or 8, vocabularies smaller than one 256-id tile: shards of 8 ids, an
+# empty shard, padding inside the only tile
+@pytest.mark.parametrize("T,H,bounds,vreal,bias,tau", [
+    (1, 16, [0, 40, 96], 90, 0.5, 0.7),
+    (2, 16, [0, 0, 200], 200, None, 1.0),
+    (3, 16, [0, 8, 16, 24], 20, 0.05, 2.5),
+    (3, 8, [0, 248], 247, None, 0.3),
+])
+def test_tiny_shapes_all_entry_points(lp, T, H, bounds, vreal, bias, tau):
+    _check_all_entry_points(lp, T, H, bounds, vreal, bounds[-1], bias, tau, seed=100 * T + H)
+
+
+def _check_all_entry_points(lp, T, H, bounds, vreal, vpad, bias, tau, seed):
     import torch
-    T, H, bounds, vreal, vpad, bias, tau = _random_case(seed)
     part = synth.ranges_partition(vreal, vpad, bounds)
     inp = synth.forward_inputs(T, H, part, tau=tau, seed=seed, w_std=0.5 / np.sqrt(H), bias_std=bias)
     X, W, b, y = dev_inputs(inp)
@@ -114,8 +129,19 @@ def test_random_configuration_all_entry_points(lp, seed):
     qref = oracle.top_p_replay_from_logits(Lbits, part, ids, yr, inp.tau)
     assert max_abs(_np(rq["lse"]), qref.lse) <= TOL_LSE, ctx
 
-    # backward with the entropy term
+    # backward of logp alone (the G epilogue without an entropy gradient)
     g = synth.upstream_grad(T, seed=seed)
+    bw0 = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], dev_f32(g))
+    assert lp.lp_get_device_error() == 0, ctx
+    bref0 = oracle.backward(inp.X, inp.W, inp.bias, part, inp.y, inp.tau, g)
+    assert rel_fro(_np(bw0["dX"]), bref0.dX) <= TOL_GRAD_REL, ctx
+    for k, (s, e) in enumerate(part.ranges):
+        if e == s:
+            continue
+        assert rel_fro(_np(bw0["dW"][k]), bref0.dW[k]) <= TOL_GRAD_REL, (ctx, k)
+        assert rel_fro(_np(bw0["db"][k]), bref0.db[k]) <= TOL_GRAD_REL, (ctx, k)
+
+    # backward with the entropy term
     h = synth.upstream_grad(T, seed=seed + 50)
     bw = lp.lp_backward(X, W, b, P, y, inp.tau, fwd["lse"], dev_f32(g), entropy=fwd["entropy"],
                         grad_entropy=dev_f32(h))
