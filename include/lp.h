@@ -395,11 +395,14 @@ LP_API lp_status lp_set_wait_limit(uint64_t limit_ns);
 
 /* 1 if this library was built with device-side bounds checks (LP_DEBUG_BOUNDS=1), else 0.
  * The compute sanitizer is not available on every machine; such a build stands in for its
- * out-of-bounds checks: every global index a kernel computes (from the grid, the partition,
- * the targets or the replay ids) is compared with the extent of its buffer before the
- * access, and a failed comparison records LP_ERR_BOUNDS in the device error word and skips
- * the access instead of touching memory. Results are otherwise bitwise those of the
- * regular build, which compiles the checks away. */
+ * out-of-bounds checks: the index of every plain (non-TMA) load or store a kernel computes
+ * from the grid, the partition, the targets or the replay ids - in the streaming, replay
+ * and gradient kernels and in the epilogues of the tensor-core GEMMs (bias reads, the
+ * forward's statistics, G, dW and dX stores) - is compared with the extent of its buffer
+ * as the host computed it, before the access; a failed comparison records LP_ERR_BOUNDS in
+ * the device error word and skips the access instead of touching memory. TMA copies are
+ * bounded by their tensor maps. Results are otherwise bitwise those of the regular build,
+ * which compiles the checks away. */
 LP_API int lp_debug_bounds_build(void);
 
 /* Self-test of the bounds checks: one thread checks an index equal to its extent. A

@@ -212,9 +212,11 @@ struct GradParams {
   uint16_t* G;  // [T][Vc]
   float* dbp;   // [4 * num_m_blocks][Vc] per-warp column sums of G, or NULL (no bias gradient)
   int64_t Vc;
+  int64_t db_chunks;  // rows of dbp (the extent the bounds-checked build compares with)
   int64_t coff[LP_MAX_SHARDS + 1];
   int64_t shard_start[LP_MAX_SHARDS];
   int32_t real[LP_MAX_SHARDS];
+  int32_t width[LP_MAX_SHARDS];  // ids of each shard: the length of its bias
   int32_t nb_start[LP_MAX_SHARDS + 1];
   int64_t vocab_real;
   int32_t n_shards;
@@ -298,7 +300,10 @@ struct GradEpi : GemmEpiBase {
     // the bias of column 32 ch + j sits in lane j; the next chunk's is fetched while this
     // chunk is formed
     auto bias_of = [&](int ch) {
-      return (bias != nullptr && ch * 32 + lane < valid) ? __bfloat162float(bias[n0 + ch * 32 + lane]) : 0.f;
+      return (bias != nullptr && ch * 32 + lane < valid &&
+              in_bounds(n0 + ch * 32 + lane < p.width[c.shard], p.err))
+                 ? __bfloat162float(bias[n0 + ch * 32 + lane])
+                 : 0.f;
     };
     float bl_next = bias_of(0);
 #pragma unroll 1
@@ -330,7 +335,9 @@ struct GradEpi : GemmEpiBase {
           const int64_t tc = ycol - ch * 32;
           if (tc >= 0 && tc < 32 && ch * 32 + tc < valid) {
             const int t = int(tc);
-            const float b = bias != nullptr ? __bfloat162float(bias[n0 + ch * 32 + t]) : 0.f;
+            const float b = (bias != nullptr && in_bounds(n0 + ch * 32 + t < p.width[c.shard], p.err))
+                                ? __bfloat162float(bias[n0 + ch * 32 + t])
+                                : 0.f;
             const float pr = hw_ex2(__fmaf_rn(__fadd_rn(reg_pick(r, t), b), p.scale_log2, -lse2));
             const float gt = __fmul_rn(gi, __fsub_rn(1.f, pr));
 #pragma unroll
@@ -359,7 +366,8 @@ struct GradEpi : GemmEpiBase {
 #pragma unroll
         for (int j = 0; j < 32; ++j) gv[j] = 0.f;
       }
-      if (in_rows) {  // 64 bytes of this row: two whole-sector stores
+      // 64 bytes of this row (two whole-sector stores) inside its Vc columns
+      if (in_rows && in_bounds(col_base + ch * 32 + 32 <= p.Vc, p.err)) {
         uint32_t packed[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) packed[j] = pack_bf16(gv[2 * j], gv[2 * j + 1]);
@@ -367,7 +375,9 @@ struct GradEpi : GemmEpiBase {
         st_global_v8(grow + ch * 32 + 16, packed + 8, pol);
       }
       // bias gradient: this warp's 32 rows of the chunk's 32 columns, summed in fp32
-      if (dbrow != nullptr) dbrow[ch * 32 + lane] = warp_column_sum(gv, lane);
+      if (dbrow != nullptr &&
+          in_bounds(int64_t(c.mb) * 4 + q < p.db_chunks && col_base + ch * 32 + 32 <= p.Vc, p.err))
+        dbrow[ch * 32 + lane] = warp_column_sum(gv, lane);
     }
   }
 };
@@ -384,6 +394,7 @@ struct DwParams {
   unsigned int* err;
   uint64_t wait_limit_ns;
   void* dW[LP_MAX_SHARDS];  // float, or bf16 with dw_bf16
+  int64_t width[LP_MAX_SHARDS];  // rows of dW_k
   int64_t coff[LP_MAX_SHARDS];
   int32_t real[LP_MAX_SHARDS];
   int32_t nb_start[LP_MAX_SHARDS + 1];
@@ -435,7 +446,8 @@ struct DwEpi : GemmEpiBase {
     const int64_t v0 = int64_t(c.nb_local) * kGemmBlockN;
     const int64_t left = p.real[c.shard] - v0;
     const int valid = int(left < kGemmBlockN ? left : kGemmBlockN);
-    const bool ok = h < p.H;
+    // rows v0 .. v0 + valid of dW_k: within its width rows
+    const bool ok = h < p.H && in_bounds(v0 + valid <= p.width[c.shard], p.err);
     const size_t off = size_t(v0) * size_t(p.H) + size_t(ok ? h : 0);
     const uint64_t pol = l2_policy_evict_first();
     if (p.dw_bf16) {  // a warp stores 64 contiguous bytes of one dW row per instruction
@@ -504,6 +516,7 @@ struct DxParams {
   int32_t num_n;
   int32_t nkb_total;
   int32_t kb_per_split;
+  int32_t splits;  // fp32 partials in out (the extent the bounds-checked build compares with)
   int64_t T, H;
 };
 
@@ -561,9 +574,9 @@ struct DxEpi : GemmEpiBase {
                                              int lane) {
     const Coord c = coord(p, tile);
     const int64_t row = int64_t(c.mb) * kRows + half * kGemmBlockM + q * 32 + lane;
-    const bool ok = row < p.T;
     const int64_t c0 = int64_t(c.nb) * kGemmBlockN;
     const int64_t cols = p.H - c0 < kGemmBlockN ? p.H - c0 : kGemmBlockN;
+    const bool ok = row < p.T && in_bounds(c.s < p.splits && c0 + cols <= p.H, p.err);
     if (p.out_bf16 != nullptr) {
       // H % 8 == 0, so 8-column groups are whole: one 16-byte store per group
       uint16_t* dst = p.out_bf16 + size_t(ok ? row : 0) * size_t(p.H) + size_t(c0);
@@ -642,6 +655,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
       p.coff[k] = L.coff[k];
       p.shard_start[k] = sh.start[k];
       p.real[k] = int32_t(sh.real[k]);
+      p.width[k] = int32_t(sh.width[k]);
       p.nb_start[k] = nb;
       nb += int((sh.real[k] + kFwdBlockN - 1) / kFwdBlockN);
     }
@@ -663,6 +677,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.grad_entropy = a.grad_entropy;
     p.G = G;
     p.Vc = L.Vc;
+    p.db_chunks = L.db_chunks;
     bool any_db = false;
     for (int k = 0; k < sh.n; ++k) any_db = any_db || (a.db[k] != nullptr && sh.width[k] > 0);
     p.dbp = any_db ? dbp : nullptr;
@@ -683,6 +698,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     int nb = 0;
     for (int k = 0; k < sh.n; ++k) {
       p.dW[k] = a.dW[k];
+      p.width[k] = sh.width[k];
       p.coff[k] = L.coff[k];
       p.real[k] = int32_t(sh.real[k]);
       p.nb_start[k] = nb;
@@ -724,6 +740,7 @@ lp_status run_backward(const BackwardArgs& a, const Shards& sh, cudaStream_t s) 
     p.nkb_total = int32_t(L.Vc / kFwdBlockK);
     p.kb_per_split = (p.nkb_total + L.split - 1) / L.split;
     const int splits = (p.nkb_total + p.kb_per_split - 1) / p.kb_per_split;
+    p.splits = splits;
     p.T = T;
     p.H = H;
     p.out = splits > 1 ? part : static_cast<float*>(a.dX);

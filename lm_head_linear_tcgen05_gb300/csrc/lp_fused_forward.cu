@@ -145,7 +145,9 @@ struct LogpEpi : GemmEpiBase {
 #pragma unroll
     for (int ch = 0; ch < kChunks; ++ch) {
       const int col = ch * 32 + lane;
-      bl[ch] = (bias != nullptr && col < valid) ? __bfloat162float(bias[n0 + col]) : 0.f;
+      bl[ch] = (bias != nullptr && col < valid && in_bounds(n0 + col < p.shard_width[c.shard], p.err))
+                   ? __bfloat162float(bias[n0 + col])
+                   : 0.f;
     }
 
     // pass 1: row maximum of (acc + b) over the valid columns
@@ -182,7 +184,9 @@ struct LogpEpi : GemmEpiBase {
         const int64_t tc = ycol - ch * 32;
         if (tc >= 0 && tc < 32 && tc < lim) {
           const float v = pick(r, int(tc));
-          const float b = bias != nullptr ? __bfloat162float(bias[n0 + ch * 32 + tc]) : 0.f;
+          const float b = (bias != nullptr && in_bounds(n0 + ch * 32 + tc < p.shard_width[c.shard], p.err))
+                              ? __bfloat162float(bias[n0 + ch * 32 + tc])
+                              : 0.f;
           t_val = __fmul_rn(__fadd_rn(v, b), p.inv_tau);
           t_here = true;
         }
@@ -191,7 +195,8 @@ struct LogpEpi : GemmEpiBase {
     const float s_tot = __fadd_rn(__fadd_rn(acc4.s[0], acc4.s[1]), __fadd_rn(acc4.s[2], acc4.s[3]));
     const float a_tot = __fadd_rn(__fadd_rn(acc4.a[0], acc4.a[1]), __fadd_rn(acc4.a[2], acc4.a[3]));
 
-    if (row < p.T) {
+    // the statistics arrays hold nb_total x T slots
+    if (row < p.T && in_bounds(c.nb_global < p.nb_start[p.n_shards], p.err)) {
       const size_t slot = size_t(c.nb_global) * size_t(p.T) + size_t(row);
       p.ws_m[slot] = valid > 0 ? m_u : -INFINITY;
       p.ws_s[slot] = s_tot;
