@@ -6,7 +6,7 @@ Headline (one JSON line on rank 0): the fused forward on the Qwen3-8B-shaped LM 
 T=4096 rows, H=4096, V=151936 bf16, tau=0.7, logp + LSE + entropy, in tokens/s, with
 the tensor-core roofline of the fused GEMM kernel. The other hot-path rows are timed
 alongside in "paths": the tiny configuration (T=64, H=256, V=1000), the headline's shapes
-at micro-batch sizes (T=512 and 1024), logits reuse
+at micro-batch sizes (T=128, 512 and 1024), logits reuse
 (T=8192 x 151936 bf16 logits, HBM-bound) and the gradient with respect to those logits,
 compact top-p replay (T=8192, 4 shards) from x.W and from the logits, and the
 vocabulary-sharded forward + backward (T=4096, V=151936 padded to 152064 in 4 shards,
@@ -492,15 +492,16 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                            "max_abs_dentropy": _maxdev(got["entropy"].cpu(), r.entropy)})
         out["tiny"] = leg
     if "batches" in wanted:
-        # the headline workload at micro-batch sizes (T = 512, 1024 rows of the same X, W): one
-        # read of W (1.245 GB) is spread over fewer rows, so the call is bound by the tensor
-        # pipe or by streaming W, whichever is slower; both fractions are reported
+        # the headline workload at micro-batch sizes (T = 128, 512, 1024 rows of the same X, W):
+        # one read of W (1.245 GB) is spread over fewer rows, so the call is bound by the tensor
+        # pipe or by streaming W, whichever is slower (W at T = 128, a single row block); both
+        # fractions are reported
         pb = synth.even_partition(Vp, 1)
         Pb = lp.VocabPartition(pb.vocab_real, pb.vocab_padded, pb.ranges)
         Xb, Wb, _, yb = synth.device_forward_inputs(1024, H, pb, TAU, dev, seed=6)
         w_bytes = float(sum(w.numel() * 2 for w in Wb))
         legs = {}
-        for T in (512, 1024):
+        for T in (128, 512, 1024):
             Xt, yt = Xb[:T].contiguous(), yb[:T].contiguous()
             wst = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD, T, H, Pb), dtype=torch.uint8, device=dev)
             ms, clk = timed(lambda: lp.lp_forward(Xt, Wb, None, Pb, yt, TAU, workspace=wst), args.steps)
@@ -524,8 +525,8 @@ def time_other_paths(args, lp, synth, dev, stream, peaks):
                 del Wh
             legs[f"T{T}"] = leg
         out["fused_forward_batches"] = {
-            "workload": f"T=512 and 1024 rows, H=4096, V={Vp}, tau=0.7, no bias (the headline's shapes at "
-                        "micro-batch sizes)", **legs}
+            "workload": f"T=128, 512 and 1024 rows, H=4096, V={Vp}, tau=0.7, no bias (the headline's shapes "
+                        "at micro-batch sizes)", **legs}
         del Xb, Wb
         torch.cuda.empty_cache()
     if wanted & {"logits", "replay"}:
