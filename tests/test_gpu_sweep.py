@@ -59,6 +59,15 @@ def test_tiny_shapes_all_entry_points(lp, T, H, bounds, vreal, bias, tau):
     _check_all_entry_points(lp, T, H, bounds, vreal, bounds[-1], bias, tau, seed=100 * T + H)
 
 
+def test_most_shards_all_entry_points(lp):
+    """LP_MAX_SHARDS = 8 shards (every per-shard slot in use, the last tensor map included):
+    an empty shard, two 8-id shards, widths that are not multiples of the 256-id tile, padding
+    in the last shard."""
+    bounds = [0, 512, 520, 1000, 1000, 1600, 2048, 2056, 2600]
+    assert len(bounds) - 1 == 8
+    _check_all_entry_points(lp, 300, 136, bounds, 2590, 2600, 0.05, 0.7, seed=8)
+
+
 def _check_all_entry_points(lp, T, H, bounds, vreal, vpad, bias, tau, seed):
     import torch
     part = synth.ranges_partition(vreal, vpad, bounds)
