@@ -175,7 +175,9 @@ LP_API lp_status lp_forward(const void* X, int64_t T, int64_t H,
  * Batches of T >= 4096 rows run as two halves whose second half is copied in on an
  * auxiliary stream while the first half computes (a row's bits do not depend on its
  * batch); the first such call on a device creates that stream and three events, kept
- * until the process exits (make it before any stream capture).
+ * until the process exits (make it before any stream capture). Calls from several host
+ * threads may run at once: each call enqueues its uses of those events under a per-device
+ * lock, which it holds only while enqueueing.
  * Workspace: lp_workspace_size(LP_OP_FORWARD_HOST, T, H, part) bytes of device memory. */
 LP_API lp_status lp_forward_host(const void* X_host, int64_t T, int64_t H,
                                  const void* const* W, const void* const* bias,

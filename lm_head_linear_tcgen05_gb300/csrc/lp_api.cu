@@ -51,10 +51,13 @@ struct DeviceState {
   bool supported = false;
   int num_sms = 0;
   unsigned int* err = nullptr;
-  // lp_forward_host's copy stream and its three events, created on its first call
+  // lp_forward_host's copy stream and its three events, created on its first call; a
+  // call holds host_mu while it records and waits on them, so that calls from several
+  // host threads never wait on one another's records
   bool copy_init = false;
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  std::mutex host_mu;
 };
 
 std::mutex g_mu;
@@ -387,6 +390,10 @@ lp_status lp_forward_host(const void* X_host, int64_t T, int64_t H, const void* 
   const int64_t T0 = T >= kHostSplitRows ? (T / 2 + 255) / 256 * 256 : T;
   const int nparts = T0 < T ? 2 : 1;
   if (nparts == 2 && (dst = device_copy_stream(dev)) != LP_OK) return dst;
+  // the shared events are recorded and waited on under the device's lock (only enqueueing
+  // happens while it is held)
+  std::unique_lock<std::mutex> host_lock(dev->host_mu, std::defer_lock);
+  if (nparts == 2) host_lock.lock();
   char* ws = static_cast<char*>(workspace);
   char* dX = ws + L.off_x;
   int32_t* dy = reinterpret_cast<int32_t*>(ws + L.off_y);

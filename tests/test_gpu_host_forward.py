@@ -68,3 +68,46 @@ def test_host_forward_empty_batch_and_errors(lp):
     with pytest.raises(ValueError):
         lp.lp_forward_host(hX, W, b, P, hy[:4].contiguous(), inp.tau)     # y of another length
     assert lp.lp_get_device_error() == 0
+
+
+def test_host_forward_from_concurrent_threads(lp):
+    """Two host threads, each on its own stream with its own workspace and host buffers,
+    call lp_forward_host on two-part batches at the same time: the calls share the
+    device's copy stream and events, and every result is still bitwise lp_forward's."""
+    import threading
+
+    import torch
+    part = synth.ranges_partition(2000, 2048, [0, 1024, 2048])
+    P = part_of(part)
+    cases = []
+    for i, T in enumerate((4096, 4357)):
+        inp = synth.forward_inputs(T, 256, part, tau=0.7, seed=40 + i, bias_std=0.1)
+        X, W, b, y = dev_inputs(inp)
+        ref = lp.lp_forward(X, W, b, P, y, inp.tau, shard_stats=True)
+        hX = torch.from_numpy(inp.X.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hy = torch.from_numpy(inp.y).pin_memory()
+        ws = torch.empty(lp.lp_workspace_size(lp.LP_OP_FORWARD_HOST, T, 256, P), dtype=torch.uint8,
+                         device="cuda")
+        cases.append((hX, W, b, hy, inp.tau, ws, {k: ref[k].cpu() for k in ref if ref[k] is not None}))
+    torch.cuda.synchronize()
+    failures = []
+
+    def worker(case):
+        hX, W, b, hy, tau, ws, ref = case
+        torch.cuda.set_device(0)
+        with torch.cuda.stream(torch.cuda.Stream()):
+            out = None
+            for it in range(25):
+                got = lp.lp_forward_host(hX, W, b, P, hy, tau, shard_stats=True, workspace=ws, out=out)
+                out = got
+                for k in ("logp", "lse", "entropy", "shard_stats"):
+                    if not torch.equal(got[k], ref[k]):
+                        failures.append((hX.shape[0], it, k))
+
+    threads = [threading.Thread(target=worker, args=(c,)) for c in cases]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not failures, failures[:5]
+    assert lp.lp_get_device_error() == 0
