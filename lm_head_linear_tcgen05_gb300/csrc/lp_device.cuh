@@ -201,6 +201,16 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 }
 
 // All threads of every CTA of the cluster: release/acquire barrier.
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation
+// may start before the kernel it follows on the stream has finished, once every CTA of that
+// kernel has signalled launch_dependents (or exited); grid_dependency_wait then blocks
+// until that kernel has completed and its memory operations are visible. Without such a
+// launch both are no-ops.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -226,6 +226,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   __shared__ Stat part[kMergeWarps][kMergeRows];
   __shared__ float sh_lse[LP_MAX_SHARDS][kMergeRows];
   __shared__ float sh_h[LP_MAX_SHARDS][kMergeRows];
+  // launched as the GEMM's programmatic dependent: its statistics are complete and visible
+  // once this returns
+  grid_dependency_wait();
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -310,10 +313,22 @@ cudaError_t launch_fused_forward(const FwdParams& p, int num_sms, cudaStream_t s
   return launch_tc_gemm<LogpEpi<kFwdClusterM>>(p, num_sms, s);
 }
 
+// Launched with programmatic stream serialisation, so that its launch overlaps the end of the
+// GEMM that precedes it on the stream (merge_kernel waits for that GEMM's completion first).
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
-  const int grid = (p.T + kMergeRows - 1) / kMergeRows;
-  merge_kernel<<<grid, kMergeThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((p.T + kMergeRows - 1) / kMergeRows), 1, 1);
+  cfg.blockDim = dim3(kMergeThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel, p);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
 }
 
 }  // namespace lp

@@ -358,6 +358,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     cluster_sync();  // no CTA leaves while the pair's MMAs or copies may still touch it
   else
     __syncthreads();
+  // this CTA's work is done: a kernel launched as this grid's programmatic dependent (the
+  // forward's row merge) may be scheduled once every CTA gets here; it waits for the grid's
+  // completion itself
+  if (threadIdx.x == 0) grid_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<kCG>(tmem, kGemmTmemCols);
